@@ -1,0 +1,437 @@
+"""Benchmark of libringred's ring AllReduce on one GB300 (or N independent replicas).
+
+Workload (the ring AllReduce sweep): R = 8 virtual ranks, binary16 storage and
+wire (a rounding after every hop), values normal with sigma 1e-3, per-rank
+message of 512 MiB (268,435,456 elements).  One step = one ring_allreduce call
+through the C ABI over all 8 rank buffers (partition, reduce-scatter fold and
+allgather copies fused in one kernel).  The step's inputs (4 GiB) and outputs
+(4 GiB) are far larger than L2, so no flush is needed between timed steps.
+
+Printed value: algbw = per-rank message bytes / step time (GB/s, 1e9), the
+whole job's aggregate over replicas at N > 1 (weak scaling: every GPU runs its
+own full workload; the path has no exchange between GPUs).
+
+Also reported: the roofline of the kernel (2 R msg bytes per launch over its
+CUDA-event time against the measured HBM copy bandwidth), the sweep over 1,
+16, 128 and 512 MiB with an L2 flush before every timed launch, an end-to-end
+figure through the same C ABI with pinned host buffers (host-to-device copies
+of the inputs and device-to-host copies of all outputs inside the timed
+region), the CPU oracle's throughput on a bounded sample, and the SM clocks
+sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "allreduce algbw GB/s and % of HBM roofline vs message size at R ranks, 1 GB300"
+UNIT = "GB/s"
+MIB = 1 << 20
+R = 8
+MSG_MIB = 512
+SWEEP_MIB = (1, 16, 128, 512)
+CPU_SAMPLE_MIB = 64
+REF_SAMPLE_MIB = 64
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_digest():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "ring_allreduce_reducescatter_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(digest):
+    """DRAM bytes per launch of the AllReduce kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        with open(p) as f:
+            text = f.read()
+        m = re.search(r"traffic_per_launch_bytes:\s*(\d+)\s*\(kernel sources ([0-9a-f]+)\)", text)
+        if m and m.group(2) == digest:
+            return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples (200 ms) with host timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        source = "timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples
+            inside = [p for (t, p) in self.samples if t0 - 1.0 <= t <= t1 + 1.0]
+            source = "within 1 s of the timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "none"}
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for p in inside for k in range(4) if p[4 + k].lower().startswith("active")})
+        pw = [num(p[2]) for p in inside if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "source": source,
+                "power_w_max": max(pw) if pw else None}
+
+
+def combine_ranks(pg, local_ms, device=None):
+    """Max over ranks of each timing (ms), the slowest replica sets the job time."""
+    if pg is None:
+        return list(local_ms)
+    import torch
+
+    t = torch.tensor(list(local_ms), dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world, msg_bytes, ms_per_step):
+    """Whole-job algbw (GB/s): every replica moves msg_bytes per rank per step."""
+    return world * msg_bytes / (ms_per_step * 1e-3) / 1e9
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the baseline, and the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_inputs(msg_mib, seed0):
+    import numpy as np
+
+    n = int(msg_mib * MIB) // 2
+    rng = np.random.default_rng(seed0)
+    return [(rng.standard_normal(n, dtype=np.float32) * np.float32(1e-3)).astype(np.float16).view(np.uint16)
+            for _ in range(R)], n
+
+
+def time_oracle(msg_mib, seed0=2000):
+    import oracle
+
+    oracle.build()
+    xs, n = oracle_inputs(msg_mib, seed0)
+    t0 = time.perf_counter()
+    res = oracle.allreduce(xs, "f16")
+    dt = time.perf_counter() - t0
+    assert res.status == oracle.OK
+    return n * 2 / dt / 1e9, dt, n
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+
+    if local == 0:
+        __graft_entry__.build()
+    if pg:
+        pg.barrier()
+    import ring_allreduce_reducescatter_gb300 as rr
+    from ring_allreduce_reducescatter_gb300 import workloads as wl
+
+    props = torch.cuda.get_device_properties(dev)
+    l2_bytes = int(getattr(props, "L2_cache_size", 128 * MIB))
+    w = wl.config2(args.msg_mib)
+    N = w.count
+    msg = N * 2
+    xs = wl.inputs(w, dev)
+    outs = [torch.empty_like(x) for x in xs]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rr.allreduce(xs, outs=outs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if rr.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else (gpu_id or local)
+    sampler = ClockSampler(gpu_id) if local == 0 else None
+    time.sleep(0.5 if sampler else 0)
+
+    # timed region: exactly K steps, barrier + synchronize on both sides
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    region0.record(stream)
+    for k in range(args.steps):
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    if pg:
+        pg.barrier()
+    region_ms = region0.elapsed_time(region1)
+    kern_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if rr.device_status() != 0:
+        raise RuntimeError("device status set during the timed region")
+    gpu_launches = args.steps  # one ring_allreduce kernel per step
+
+    region_ms, kern_ms = combine_ranks(pg, [region_ms, kern_ms], dev)
+    ms_per_step = region_ms / args.steps
+    value = job_throughput(world, msg, ms_per_step)
+    peak, peak_kind = measured_hbm_peak()
+    achieved = 2 * R * msg / (kern_ms * 1e-3) / 1e9
+    digest = kernel_sources_digest()
+    traffic = recorded_traffic(digest)
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+
+    # sweep with an L2 flush before every timed launch
+    sweep = []
+    if not args.no_sweep:
+        flush = torch.empty(2 * l2_bytes // 4 + 1024, dtype=torch.float32, device=dev)
+        del outs
+        for mib in SWEEP_MIB:
+            if mib == args.msg_mib:
+                sx, so = xs, [torch.empty_like(x) for x in xs]
+            else:
+                sw = wl.config2(mib)
+                sx = wl.inputs(sw, dev)
+                so = [torch.empty_like(x) for x in sx]
+            times = []
+            for it in range(args.sweep_iters + 2):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                rr.allreduce(sx, outs=so)
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                if it >= 2:
+                    times.append(a.elapsed_time(b))
+            t_ms = statistics.median(times)
+            m = sx[0].numel() * 2
+            sweep.append({"msg_mib": mib, "ms": round(t_ms, 5), "algbw_gbs": round(m / t_ms / 1e6, 2),
+                          "busbw_gbs": round(m / t_ms / 1e6 * 2 * (R - 1) / R, 2),
+                          "hbm_gbs": round(2 * R * m / t_ms / 1e6, 1),
+                          "roofline_frac": round(2 * R * m / t_ms / 1e6 / peak, 4),
+                          "plan": rr.plan(rr.OP_ALLREDUCE, sx, so, sx[0].numel())})
+            del so
+            if sx is not xs:
+                del sx
+        del flush
+        torch.cuda.empty_cache()
+        outs = [torch.empty_like(x) for x in xs]
+
+    # end to end through the same C ABI, with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = [torch.empty(N, dtype=torch.float16, pin_memory=True) for _ in range(R)]
+        host_out = [torch.empty(N, dtype=torch.float16, pin_memory=True) for _ in range(R)]
+        for r in range(R):
+            host_in[r].copy_(xs[r])
+
+        def e2e_step():
+            for r in range(R):
+                xs[r].copy_(host_in[r], non_blocking=True)
+            rr.allreduce(xs, outs=outs)
+            for r in range(R):
+                host_out[r].copy_(outs[r], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg:
+            pg.barrier()
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = combine_ranks(pg, [a.elapsed_time(b) / args.e2e_steps], dev)[0]
+        e2e = {"value": round(job_throughput(world, msg, e_ms), 3), "unit": UNIT,
+               "h2d_bytes_per_step": R * msg, "d2h_bytes_per_step": R * msg, "ms_per_step": round(e_ms, 4),
+               "steps": args.e2e_steps}
+        del host_in, host_out
+
+    if sampler:
+        sampler.stop()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, n = time_oracle(args.cpu_sample_mib)
+        cpu = {"value": round(v, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the same workload at {args.cpu_sample_mib} MiB per rank ({n} fp16 elements x {R} "
+                         f"ranks), one literal ring simulation, {dt:.2f} s on 1 host core"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": f"ring allreduce R={R} fp16 per-hop fp16, {args.msg_mib} MiB per rank, "
+                                   f"N(0,1e-3)", "R": R, "count": N, "msg_bytes": msg,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (2 x R x msg bytes per step)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                         "kernel_ms": round(kern_ms, 5), "algorithmic_bytes_per_launch": 2 * R * msg},
+            "busbw_gbs": round(value / world * 2 * (R - 1) / R, 3),
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
+            "sweep": sweep, "kernel_sources": digest,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle, timed as it stands
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    # size each step's sample so the whole run stays within about two minutes
+    _, dt_cal, n_cal = time_oracle(0.25, seed0=1999)
+    per_elem = dt_cal / n_cal
+    budget = min(2.0, 120.0 / (args.warmup + args.steps))
+    n = max(2048, int(budget / per_elem) // 256 * 256)
+    if args.ref_sample_mib:
+        n = min(n, args.ref_sample_mib * MIB // 2)
+    mib = n * 2 / MIB
+    times = []
+    for k in range(args.warmup + args.steps):
+        v, dt, n = time_oracle(mib, seed0=2000 + k)
+        if k >= args.warmup:
+            times.append(dt)
+    ms = statistics.mean(times) * 1e3
+    value = n * 2 / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"ring allreduce R={R} fp16 per-hop fp16, {args.msg_mib} MiB per rank, "
+                               f"N(0,1e-3)", "R": R, "count": args.msg_mib * MIB // 2,
+                   "sample_elements_per_rank": n},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the workload at {n} fp16 elements per rank x {R} ranks "
+                                   f"({mib:.3f} MiB per rank), one literal ring simulation on 1 host core"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--msg-mib", type=int, default=MSG_MIB)
+    ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-sample-mib", type=int, default=CPU_SAMPLE_MIB)
+    ap.add_argument("--ref-sample-mib", type=int, default=REF_SAMPLE_MIB)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * ringred.h -- C ABI of libringred.
+ *
+ * libringred computes the ring AllReduce, ReduceScatter and AllGather of R
+ * "ranks" whose buffers all live in the memory of one GPU.  It reproduces the
+ * data semantics of the ring collective described on these pages:
+ *
+ *   [p3] ai6s.net/6a102b5410ee7a33f2746c06.html, section "hcomm 与 HCCL 的关系":
+ *        AllReduce = ReduceScatter + AllGather; the ReduceScatter runs N-1 steps
+ *        in which every rank passes one chunk to the next rank, which adds it
+ *        element-wise to its own copy of that chunk.
+ *   [p5] hwcomputing.csdn.net/6a0dc11a10ee7a33f273f7fd.html, section
+ *        "Ring 通信为什么常见": block c starts on card c and is passed around
+ *        the ring; after the reduce-scatter phase each card holds one summed
+ *        block, and the AllGather phase hands the summed blocks to all cards.
+ *   [p2] ai6s.net/6a157e6510ee7a33f27553e9.html, section "自定义通信模式":
+ *        chunk c has floor(count / R) elements, the last chunk takes the rest.
+ *   [p5] section "大模型训练中的通信优化": gradients travel in FP16.
+ *   [p5] section "通信拓扑与带宽利用率": one exchange between nodes per
+ *        AllReduce (the two-level ring).
+ *
+ * Result, element by element.  With L ranks per group (L = R for the flat
+ * ring), G = R / L groups, and c = the chunk of element i in the partition of
+ * `count` into L chunks:
+ *     S_g[i] = x_{gL+c}[i] (+) x_{gL+c+1}[i] (+) ... (+) x_{gL+c+L-1}[i]
+ *              (ranks taken mod L inside group g, folded left to right)
+ *     y[i]   = S_0[i] (+) S_1[i] (+) ... (+) S_{G-1}[i]
+ * where (+) is one hop: the binary32 sum of its two operands rounded once to
+ * the wire format (round to nearest even; no fused multiply-add; subnormals
+ * kept).  With a binary32 wire the hop is the binary32 addition.  On a 16-bit
+ * wire with binary32 storage, every input is first rounded to the wire format
+ * and the result is widened back exactly.  The result is the same on every
+ * GPU and every launch configuration: it depends only on the inputs, R, L,
+ * count and the formats.
+ *
+ * Common rules for every collective below:
+ *   - in_bufs and out_bufs are HOST arrays of R DEVICE pointers (current
+ *     device).  The library reads the arrays during the call only.
+ *   - The caller owns every buffer and the stream.  The library allocates no
+ *     memory and keeps no pointer after the call returns.
+ *   - The call is asynchronous: it validates its arguments, enqueues work on
+ *     `stream` and returns.  Errors of the enqueued work surface when the
+ *     caller synchronizes the stream; a bounded wait inside a kernel that gave
+ *     up is recorded in the device status word (ring_device_status).
+ *   - Argument errors are detected before anything is enqueued and return
+ *     RR_ERR_INVALID_ARG / RR_ERR_UNSUPPORTED / RR_ERR_ALIAS; nothing is
+ *     written then.  A failed launch returns RR_ERR_CUDA.
+ *   - count == 0 returns RR_OK and enqueues nothing.  A buffer of zero
+ *     elements may be NULL.  Every other buffer must be non-NULL and aligned
+ *     to its element size; 16-byte aligned buffers take the fast path.
+ *   - A buffer written by the call (an output) must not overlap any other
+ *     buffer, with one exception: ring_allreduce* accepts out_bufs[r] ==
+ *     in_bufs[r] (in place).  Inputs may overlap one another.
+ *   - 1 <= R <= RR_MAX_RANKS.
+ */
+#ifndef RINGRED_H
+#define RINGRED_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (the same declaration as the runtime's). */
+typedef struct CUstream_st *cudaStream_t;
+
+#define RR_MAX_RANKS 64
+#define RR_ABI_VERSION 1
+
+typedef enum { RR_FP32 = 0, RR_FP16 = 1, RR_BF16 = 2 } rr_dtype;
+
+typedef enum {
+  RR_OK = 0,
+  RR_ERR_INVALID_ARG = 1, /* bad R, count, group size, NULL or misaligned pointer */
+  RR_ERR_UNSUPPORTED = 2, /* (storage, wire) pair or forced path not available */
+  RR_ERR_ALIAS = 3,       /* an output overlaps another buffer */
+  RR_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  RR_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up */
+} rr_status;
+
+typedef enum { RR_OP_ALLREDUCE = 0, RR_OP_REDUCE_SCATTER = 1, RR_OP_ALLGATHER = 2 } rr_op;
+
+/*
+ * ring_allreduce -- [p3] AllReduce = ReduceScatter + AllGather; [p5] ring walkthrough.
+ * in_bufs[r], out_bufs[r]: `count` elements of `dtype` each.  Every out_bufs[r]
+ * receives y (above) with L = R and the wire format equal to `dtype`.
+ */
+rr_status ring_allreduce(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                         rr_dtype dtype, cudaStream_t stream);
+
+/*
+ * ring_allreduce_ex -- ring_allreduce with a wire format and a two-level ring.
+ * wire: RR_FP32 only for RR_FP32 storage, or the storage type itself, or a
+ *   16-bit wire under RR_FP32 storage ([p5] FP16 communication).  Supported
+ *   (dtype, wire): (FP32,FP32) (FP16,FP16) (BF16,BF16) (FP32,BF16) (FP32,FP16).
+ * group_size: L, ranks per group ([p5] "通信拓扑与带宽利用率"); 0 or R = the
+ *   flat ring; otherwise L must divide R, and group g holds ranks gL..gL+L-1.
+ */
+rr_status ring_allreduce_ex(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                            rr_dtype dtype, rr_dtype wire, int group_size, cudaStream_t stream);
+
+/*
+ * ring_reduce_scatter -- [p3] the simplified ReduceScatter code.
+ * in_bufs[r]: `count` elements.  out_bufs[r]: ring_chunk_count(count, R, r)
+ * elements, receiving chunk r of y (the NCCL placement: rank r gets chunk r).
+ * count is the full per-rank input length, not the per-rank output length.
+ */
+rr_status ring_reduce_scatter(const void *const *in_bufs, void *const *out_bufs, int R,
+                              size_t count, rr_dtype dtype, cudaStream_t stream);
+
+/* ring_reduce_scatter_ex -- ring_reduce_scatter with a wire format (pairs as above). */
+rr_status ring_reduce_scatter_ex(const void *const *in_bufs, void *const *out_bufs, int R,
+                                 size_t count, rr_dtype dtype, rr_dtype wire, cudaStream_t stream);
+
+/*
+ * ring_allgather -- [p5] the AllGather phase; [p3] "分布式推理中的通信".
+ * in_bufs[c]: ring_chunk_count(count, R, c) elements (chunk c).  out_bufs[r]:
+ * `count` elements; every output receives all chunks in order:
+ *   out_bufs[r][ring_chunk_offset(count, R, c) + j] = in_bufs[c][j].
+ */
+rr_status ring_allgather(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                         rr_dtype dtype, cudaStream_t stream);
+
+/* Launch paths: RR_PATH_BULK stages tiles through shared memory with bulk
+ * asynchronous copies (needs 16-byte aligned buffers, and for ReduceScatter /
+ * AllGather chunk offsets that are multiples of 16 bytes); RR_PATH_SIMPLE is
+ * one element per thread with plain loads and stores (any alignment). */
+typedef enum { RR_PATH_AUTO = 0, RR_PATH_BULK = 1, RR_PATH_SIMPLE = 2 } rr_path;
+
+/* Optional launch configuration; zero fields mean "choose automatically". */
+typedef struct {
+  int path;        /* rr_path */
+  int tile_bytes;  /* bulk path: bytes per rank per tile, a multiple of 16 */
+  int stages;      /* bulk path: tiles in flight per CTA, 2..8 */
+  int ctas_per_sm; /* bulk path: 1..4 */
+  int threads;     /* threads per CTA: 64..1024, a multiple of 32 */
+} rr_launch_cfg;
+
+/*
+ * ring_collective -- every collective through one entry point with an
+ * explicit launch configuration (cfg may be NULL).  op selects the
+ * collective; buffer layouts are those of the named entry points; wire and
+ * group_size as for ring_allreduce_ex (ReduceScatter: group_size 0 or R;
+ * AllGather: wire == dtype, group_size 0 or R).  The launch configuration
+ * never changes the result, only the speed.  A forced RR_PATH_BULK that the
+ * buffers do not allow returns RR_ERR_UNSUPPORTED.
+ */
+rr_status ring_collective(rr_op op, const void *const *in_bufs, void *const *out_bufs, int R,
+                          size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
+                          const rr_launch_cfg *cfg, cudaStream_t stream);
+
+/*
+ * ring_plan -- the launch configuration ring_collective would use for these
+ * arguments (after validation; nothing is enqueued).  *chosen receives the
+ * path and the resolved tile / stage / CTA / thread counts.
+ */
+rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs, int R,
+                    size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
+                    const rr_launch_cfg *cfg, rr_launch_cfg *chosen);
+
+/* [p2] chunk table: length and offset of chunk c of `count` elements split
+ * over R ranks (0 when R < 1 or c is out of range). */
+size_t ring_chunk_count(size_t count, int R, int c);
+size_t ring_chunk_offset(size_t count, int R, int c);
+
+/* A static English description of a status code. */
+const char *ring_status_string(rr_status status);
+
+/*
+ * ring_device_status -- reads and clears the current device's sticky status
+ * word.  Bit 0 set: a bounded wait inside a kernel gave up (its collective
+ * did not complete).  Synchronizes the current device first.  Returns RR_OK,
+ * or RR_ERR_CUDA if the CUDA runtime reported an error.
+ */
+rr_status ring_device_status(unsigned int *flags);
+
+/*
+ * ring_selftest_bounded_wait -- launches one CTA that waits on a shared-memory
+ * barrier no one completes, with a limit of limit_ns nanoseconds (1e3..1e10),
+ * then synchronizes `stream`.  Returns RR_ERR_TIMEOUT when the wait gave up and
+ * set the status bit (the expected outcome, which the call then clears), RR_OK
+ * if it did not, RR_ERR_CUDA on a runtime error.  It exercises the bounded
+ * wait that every pipelined kernel in the library uses.
+ */
+rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t stream);
+
+/* RR_ABI_VERSION of the library. */
+int ring_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RINGRED_H */

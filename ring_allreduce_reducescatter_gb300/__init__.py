@@ -1,0 +1,217 @@
+"""libringred: ring AllReduce / ReduceScatter / AllGather over R virtual ranks on one GPU.
+
+This module is a thin ctypes binding of the C ABI in ``include/ringred.h``.  It
+only marshals arguments (tensor lists to device-pointer arrays, the current
+CUDA stream); every step of the collective runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  There is no fallback:
+if ``libringred.so`` has not been built, importing the library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = [
+    "RingError", "lib", "allreduce", "reduce_scatter", "allgather", "collective", "plan",
+    "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg",
+    "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
+    "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE",
+]
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_DIR, "libringred.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT = range(6)
+OP_ALLREDUCE, OP_REDUCE_SCATTER, OP_ALLGATHER = 0, 1, 2
+PATH_AUTO, PATH_BULK, PATH_SIMPLE = 0, 1, 2
+FP32, FP16, BF16 = 0, 1, 2
+
+_TORCH_CODE = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}
+_NAME_CODE = {"f32": FP32, "fp32": FP32, "float32": FP32, "f16": FP16, "fp16": FP16,
+              "float16": FP16, "bf16": BF16, "bfloat16": BF16}
+
+
+class RingError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class LaunchCfg(ctypes.Structure):
+    """rr_launch_cfg: zero fields mean automatic."""
+
+    _fields_ = [("path", ctypes.c_int), ("tile_bytes", ctypes.c_int), ("stages", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int), ("threads", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libringred.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vpp = ctypes.POINTER(ctypes.c_void_p)
+        sz, i, vp = ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+        L.ring_collective.argtypes = [i, vpp, vpp, i, sz, i, i, i, ctypes.POINTER(LaunchCfg), vp]
+        L.ring_plan.argtypes = [i, vpp, vpp, i, sz, i, i, i, ctypes.POINTER(LaunchCfg),
+                                ctypes.POINTER(LaunchCfg)]
+        L.ring_allreduce.argtypes = [vpp, vpp, i, sz, i, vp]
+        L.ring_allreduce_ex.argtypes = [vpp, vpp, i, sz, i, i, i, vp]
+        L.ring_reduce_scatter.argtypes = [vpp, vpp, i, sz, i, vp]
+        L.ring_reduce_scatter_ex.argtypes = [vpp, vpp, i, sz, i, i, vp]
+        L.ring_allgather.argtypes = [vpp, vpp, i, sz, i, vp]
+        for f in ("ring_collective", "ring_plan", "ring_allreduce", "ring_allreduce_ex",
+                  "ring_reduce_scatter", "ring_reduce_scatter_ex", "ring_allgather",
+                  "ring_device_status", "ring_selftest_bounded_wait"):
+            getattr(L, f).restype = i
+        L.ring_chunk_count.argtypes = [sz, i, i]
+        L.ring_chunk_count.restype = sz
+        L.ring_chunk_offset.argtypes = [sz, i, i]
+        L.ring_chunk_offset.restype = sz
+        L.ring_status_string.argtypes = [i]
+        L.ring_status_string.restype = ctypes.c_char_p
+        L.ring_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        L.ring_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
+        L.ring_abi_version.argtypes = []
+        L.ring_abi_version.restype = i
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ring_status_string(status).decode()
+
+
+def chunk_count(count: int, R: int, c: int) -> int:
+    return int(lib().ring_chunk_count(count, R, c))
+
+
+def chunk_offset(count: int, R: int, c: int) -> int:
+    return int(lib().ring_chunk_offset(count, R, c))
+
+
+def _code(t) -> int:
+    if isinstance(t, torch.dtype):
+        return _TORCH_CODE[t]
+    if isinstance(t, str):
+        return _NAME_CODE[t.lower()]
+    return int(t)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _ptr_array(tensors: Sequence[Optional[torch.Tensor]]):
+    arr = (ctypes.c_void_p * len(tensors))()
+    for k, t in enumerate(tensors):
+        arr[k] = None if t is None or t.numel() == 0 else t.data_ptr()
+    return arr
+
+
+def _check_tensors(ts, dtype, name):
+    for t in ts:
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise ValueError(f"{name}: every buffer must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise ValueError(f"{name}: mixed dtypes ({t.dtype} vs {dtype})")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: buffers must be contiguous")
+
+
+def collective(op: int, ins, outs, count: int, wire=None, group_size: int = 0, stream=None,
+               cfg: Optional[LaunchCfg] = None) -> None:
+    """ring_collective on tensor lists (outputs preallocated by the caller)."""
+    dtype = next(t.dtype for t in list(ins) + list(outs) if t is not None)
+    _check_tensors(ins, dtype, "ins")
+    _check_tensors(outs, dtype, "outs")
+    if len(ins) != len(outs):
+        raise ValueError("ins and outs must have one buffer per rank")
+    dt = _code(dtype)
+    wt = dt if wire is None else _code(wire)
+    st = lib().ring_collective(op, _ptr_array(ins), _ptr_array(outs), len(ins), count, dt, wt,
+                               group_size, ctypes.byref(cfg) if cfg is not None else None,
+                               _stream_handle(stream))
+    if st != OK:
+        raise RingError(st, "ring_collective")
+
+
+def plan(op: int, ins, outs, count: int, wire=None, group_size: int = 0,
+         cfg: Optional[LaunchCfg] = None) -> dict:
+    """The launch configuration ring_collective would pick (ring_plan)."""
+    dtype = next(t.dtype for t in list(ins) + list(outs) if t is not None)
+    dt = _code(dtype)
+    wt = dt if wire is None else _code(wire)
+    chosen = LaunchCfg()
+    st = lib().ring_plan(op, _ptr_array(ins), _ptr_array(outs), len(ins), count, dt, wt, group_size,
+                         ctypes.byref(cfg) if cfg is not None else None, ctypes.byref(chosen))
+    if st != OK:
+        raise RingError(st, "ring_plan")
+    return chosen.as_dict()
+
+
+def allreduce(ins: Sequence[torch.Tensor], outs: Optional[Sequence[torch.Tensor]] = None, wire=None,
+              group_size: int = 0, stream=None, cfg: Optional[LaunchCfg] = None):
+    """Ring AllReduce; ``outs`` defaults to new tensors (pass ``ins`` for in place)."""
+    ins = list(ins)
+    if outs is None:
+        outs = [torch.empty_like(t) for t in ins]
+    collective(OP_ALLREDUCE, ins, list(outs), ins[0].numel(), wire, group_size, stream, cfg)
+    return outs
+
+
+def reduce_scatter(ins: Sequence[torch.Tensor], outs: Optional[Sequence[torch.Tensor]] = None,
+                   wire=None, stream=None, cfg: Optional[LaunchCfg] = None):
+    """Ring ReduceScatter: outs[r] receives chunk r (chunk_count(N, R, r) elements)."""
+    ins = list(ins)
+    R, N = len(ins), ins[0].numel()
+    if outs is None:
+        outs = [torch.empty(chunk_count(N, R, r), dtype=ins[0].dtype, device=ins[0].device)
+                for r in range(R)]
+    collective(OP_REDUCE_SCATTER, ins, list(outs), N, wire, 0, stream, cfg)
+    return outs
+
+
+def allgather(ins: Sequence[torch.Tensor], count: Optional[int] = None,
+              outs: Optional[Sequence[torch.Tensor]] = None, stream=None,
+              cfg: Optional[LaunchCfg] = None):
+    """Ring AllGather: ins[c] is chunk c of a ``count``-element vector."""
+    ins = list(ins)
+    if count is None:
+        count = sum(t.numel() for t in ins)
+    ref = next(t for t in ins if t is not None)
+    if outs is None:
+        outs = [torch.empty(count, dtype=ref.dtype, device=ref.device) for _ in ins]
+    collective(OP_ALLGATHER, ins, list(outs), count, None, 0, stream, cfg)
+    return outs
+
+
+def device_status() -> int:
+    """Read and clear the current device's sticky status word (synchronizes the device)."""
+    v = ctypes.c_uint(0)
+    st = lib().ring_device_status(ctypes.byref(v))
+    if st != OK:
+        raise RingError(st, "ring_device_status")
+    return int(v.value)
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> int:
+    """Run the bounded-wait self test; returns its status (ERR_TIMEOUT is the expected one)."""
+    return int(lib().ring_selftest_bounded_wait(limit_ns, _stream_handle(stream)))

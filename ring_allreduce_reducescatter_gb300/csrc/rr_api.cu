@@ -1,0 +1,353 @@
+// rr_api.cu -- the C ABI of libringred (include/ringred.h): argument
+// validation, the chunk table, launch planning and dispatch.
+//
+// Validation runs entirely on the host and before any CUDA call, so every
+// argument error returns without touching the device.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "ringred.h"
+#include "rr_params.h"
+
+namespace {
+
+// Sticky device status word (bit rr::kStatusWaitTimeout).  Kernels get its
+// device address, taken with cudaGetSymbolAddress for each device.
+__device__ unsigned int g_rr_status_word;
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_per_sm = 0;
+  int smem_optin = 0;
+  unsigned int *status = nullptr;
+  bool valid = false;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+rr_status current_device(DeviceInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_devices_mu);
+  DeviceInfo &d = g_devices[dev];
+  if (!d.valid) {
+    void *addr = nullptr;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaGetSymbolAddress(&addr, g_rr_status_word) != cudaSuccess)
+      return RR_ERR_CUDA;
+    d.status = static_cast<unsigned int *>(addr);
+    d.valid = true;
+  }
+  *out = d;
+  return RR_OK;
+}
+
+size_t elem_bytes(int t) { return t == RR_FP32 ? 4 : 2; }
+bool valid_type(int t) { return t == RR_FP32 || t == RR_FP16 || t == RR_BF16; }
+
+size_t chunk_len(size_t count, int R, int c) {
+  const size_t base = count / (size_t)R;
+  return c < R - 1 ? base : count - (size_t)(R - 1) * base;
+}
+
+struct Buf {
+  uintptr_t lo, hi;  // [lo, hi)
+  bool written;
+  int rank;
+  bool is_in;
+};
+
+// Everything that can be checked without the device.
+struct Checked {
+  int op, R, L, dtype, wire;
+  size_t count;
+  size_t E;
+  bool all_16b_aligned;
+};
+
+rr_status check_args(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
+                     int group_size, const rr_launch_cfg *cfg, Checked *ck) {
+  if (op != RR_OP_ALLREDUCE && op != RR_OP_REDUCE_SCATTER && op != RR_OP_ALLGATHER) return RR_ERR_INVALID_ARG;
+  if (R < 1 || R > RR_MAX_RANKS) return RR_ERR_INVALID_ARG;
+  if (!valid_type(dtype) || !valid_type(wire)) return RR_ERR_INVALID_ARG;
+  if (!(dtype == wire || dtype == RR_FP32)) return RR_ERR_UNSUPPORTED;
+  if (op == RR_OP_ALLGATHER && wire != dtype) return RR_ERR_UNSUPPORTED;
+  const int L = group_size == 0 ? R : group_size;
+  if (L < 1 || L > R || R % L != 0) return RR_ERR_INVALID_ARG;
+  if (op != RR_OP_ALLREDUCE && L != R) return RR_ERR_INVALID_ARG;
+  if (!in || !out) return RR_ERR_INVALID_ARG;
+  if (cfg) {
+    if (cfg->path < RR_PATH_AUTO || cfg->path > RR_PATH_SIMPLE) return RR_ERR_INVALID_ARG;
+    if (cfg->tile_bytes != 0 && (cfg->tile_bytes < 16 || cfg->tile_bytes % 16 != 0 || cfg->tile_bytes > (1 << 20)))
+      return RR_ERR_INVALID_ARG;
+    if (cfg->stages != 0 && (cfg->stages < 2 || cfg->stages > 8)) return RR_ERR_INVALID_ARG;
+    if (cfg->ctas_per_sm != 0 && (cfg->ctas_per_sm < 1 || cfg->ctas_per_sm > 4)) return RR_ERR_INVALID_ARG;
+    if (cfg->threads != 0 && (cfg->threads < 64 || cfg->threads > 1024 || cfg->threads % 32 != 0))
+      return RR_ERR_INVALID_ARG;
+  }
+  ck->op = op;
+  ck->R = R;
+  ck->L = L;
+  ck->dtype = dtype;
+  ck->wire = wire;
+  ck->count = count;
+  ck->E = elem_bytes(dtype);
+  ck->all_16b_aligned = true;
+  if (count == 0) return RR_OK;
+  const size_t E = ck->E;
+  if (count > (SIZE_MAX / 4) / E) return RR_ERR_INVALID_ARG;
+
+  // sizes, pointers, alignment
+  Buf bufs[2 * RR_MAX_RANKS];
+  int nb = 0;
+  for (int r = 0; r < R; ++r) {
+    const size_t n_in = (op == RR_OP_ALLGATHER) ? chunk_len(count, R, r) : count;
+    const size_t n_out = (op == RR_OP_REDUCE_SCATTER) ? chunk_len(count, R, r) : count;
+    for (int side = 0; side < 2; ++side) {
+      const void *ptr = side == 0 ? in[r] : out[r];
+      const size_t bytes = (side == 0 ? n_in : n_out) * E;
+      if (bytes == 0) continue;
+      const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+      if (a == 0 || a % E != 0) return RR_ERR_INVALID_ARG;
+      if (a > UINTPTR_MAX - bytes) return RR_ERR_INVALID_ARG;
+      if (a % 16 != 0) ck->all_16b_aligned = false;
+      bufs[nb++] = Buf{a, a + bytes, side == 1, r, side == 0};
+    }
+  }
+  // an output may overlap nothing, except its own input in an in-place AllReduce
+  for (int x = 0; x < nb; ++x) {
+    if (!bufs[x].written) continue;
+    for (int y = 0; y < nb; ++y) {
+      if (y == x) continue;
+      const Buf &o = bufs[x], &b = bufs[y];
+      if (o.lo >= b.hi || b.lo >= o.hi) continue;
+      const bool in_place = op == RR_OP_ALLREDUCE && b.is_in && b.rank == o.rank && b.lo == o.lo && b.hi == o.hi;
+      if (!in_place) return RR_ERR_ALIAS;
+    }
+  }
+  return RR_OK;
+}
+
+int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+// Resolve the launch and fill the kernel parameters.
+rr_status plan(const Checked &ck, const void *const *in, void *const *out, const rr_launch_cfg *cfg,
+               const DeviceInfo &dev, rr::RingParams *p, rr::Launch *l) {
+  const rr_launch_cfg zero = {0, 0, 0, 0, 0};
+  const rr_launch_cfg &c = cfg ? *cfg : zero;
+  const size_t E = ck.E;
+  const unsigned long long N = ck.count;
+
+  *p = rr::RingParams{};
+  for (int r = 0; r < ck.R; ++r) {
+    p->in[r] = in[r];
+    p->out[r] = out[r];
+  }
+  p->count = N;
+  p->R = ck.R;
+  p->L = ck.L;
+  p->G = ck.R / ck.L;
+  p->base = N / (unsigned long long)ck.L;
+  p->status = dev.status;
+
+  // bulk path: 16-byte aligned buffers, and for ReduceScatter / AllGather
+  // chunk boundaries on 16-byte multiples (segments are copied per chunk)
+  const bool chunks_aligned = ck.op == RR_OP_ALLREDUCE || (p->base * E) % 16 == 0;
+  const unsigned long long n_bulk = (N * E / 16) * 16 / E;
+  const bool bulk_ok = ck.all_16b_aligned && chunks_aligned && n_bulk > 0;
+  int path = c.path;
+  if (path == RR_PATH_BULK && !bulk_ok) return RR_ERR_UNSUPPORTED;
+  if (path == RR_PATH_AUTO) path = bulk_ok ? RR_PATH_BULK : RR_PATH_SIMPLE;
+
+  l->path = path;
+  l->threads = c.threads ? c.threads : 256;
+  if (path == RR_PATH_SIMPLE) {
+    const unsigned long long blocks = (N + l->threads - 1) / l->threads;
+    const unsigned long long cap = (unsigned long long)dev.sms * 8;
+    l->grid = (int)(blocks < cap ? blocks : cap);
+    l->smem = 0;
+    l->ctas_per_sm = 0;
+    p->n_bulk = 0;
+    p->n_tiles = 0;
+    return RR_OK;
+  }
+
+  const int slots = ck.op == RR_OP_ALLGATHER ? 1 : ck.R;
+  const int ctas = c.ctas_per_sm ? c.ctas_per_sm : 2;
+  // shared memory of one CTA: its share of the SM, less 1 KB the runtime keeps per CTA
+  int budget = dev.smem_per_sm / ctas - 1024;
+  if (budget > dev.smem_optin) budget = dev.smem_optin;
+  const unsigned long long total_bytes = n_bulk * E;
+
+  int tile = c.tile_bytes;
+  if (tile == 0) {
+    tile = clamp_int((32768 / slots) & ~15, 512, 16384);
+    // keep at least two tiles per CTA slot when the message is small
+    const unsigned long long want = 2ull * dev.sms * ctas;
+    while (tile > 1024 && (total_bytes + tile - 1) / tile < want) tile /= 2;
+    // keep two stages within the shared-memory budget
+    while (tile > 16 && 2ull * ((unsigned long long)tile * slots + 8) > (unsigned long long)budget) tile = (tile / 2) & ~15;
+  }
+  if (tile % (int)E != 0 || tile < 16) return RR_ERR_INVALID_ARG;
+  const unsigned long long stage_bytes = (unsigned long long)tile * slots;
+  int stages = c.stages;
+  if (stages == 0) stages = clamp_int((int)((unsigned long long)budget / (stage_bytes + 8)), 2, 8);
+  const unsigned long long smem = (unsigned long long)stages * (stage_bytes + 8);
+  if (smem > (unsigned long long)budget) return RR_ERR_UNSUPPORTED;
+
+  p->tile_elems = (int)(tile / (int)E);
+  p->n_bulk = n_bulk;
+  p->n_tiles = (n_bulk + p->tile_elems - 1) / p->tile_elems;
+  p->stages = stages;
+  p->slots = slots;
+  const unsigned long long cap = (unsigned long long)dev.sms * ctas;
+  l->grid = (int)(p->n_tiles < cap ? p->n_tiles : cap);
+  l->smem = (size_t)smem;
+  l->ctas_per_sm = ctas;
+  return RR_OK;
+}
+
+rr_status run(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
+              int group_size, const rr_launch_cfg *cfg, cudaStream_t stream) {
+  Checked ck;
+  rr_status st = check_args(op, in, out, R, count, dtype, wire, group_size, cfg, &ck);
+  if (st != RR_OK || count == 0) return st;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != RR_OK) return st;
+  rr::RingParams p;
+  rr::Launch l;
+  st = plan(ck, in, out, cfg, dev, &p, &l);
+  if (st != RR_OK) return st;
+  cudaError_t e;
+  if (dtype == RR_FP32)
+    e = rr::launch_f32(op, wire, p, l, stream);
+  else if (dtype == RR_FP16)
+    e = rr::launch_f16(op, wire, p, l, stream);
+  else
+    e = rr::launch_bf16(op, wire, p, l, stream);
+  return e == cudaSuccess ? RR_OK : RR_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+rr_status ring_collective(rr_op op, const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                          rr_dtype dtype, rr_dtype wire, int group_size, const rr_launch_cfg *cfg,
+                          cudaStream_t stream) {
+  return run(op, in_bufs, out_bufs, R, count, dtype, wire, group_size, cfg, stream);
+}
+
+rr_status ring_allreduce(const void *const *in_bufs, void *const *out_bufs, int R, size_t count, rr_dtype dtype,
+                         cudaStream_t stream) {
+  return run(RR_OP_ALLREDUCE, in_bufs, out_bufs, R, count, dtype, dtype, 0, nullptr, stream);
+}
+
+rr_status ring_allreduce_ex(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                            rr_dtype dtype, rr_dtype wire, int group_size, cudaStream_t stream) {
+  return run(RR_OP_ALLREDUCE, in_bufs, out_bufs, R, count, dtype, wire, group_size, nullptr, stream);
+}
+
+rr_status ring_reduce_scatter(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                              rr_dtype dtype, cudaStream_t stream) {
+  return run(RR_OP_REDUCE_SCATTER, in_bufs, out_bufs, R, count, dtype, dtype, 0, nullptr, stream);
+}
+
+rr_status ring_reduce_scatter_ex(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                                 rr_dtype dtype, rr_dtype wire, cudaStream_t stream) {
+  return run(RR_OP_REDUCE_SCATTER, in_bufs, out_bufs, R, count, dtype, wire, 0, nullptr, stream);
+}
+
+rr_status ring_allgather(const void *const *in_bufs, void *const *out_bufs, int R, size_t count, rr_dtype dtype,
+                         cudaStream_t stream) {
+  return run(RR_OP_ALLGATHER, in_bufs, out_bufs, R, count, dtype, dtype, 0, nullptr, stream);
+}
+
+rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                    rr_dtype dtype, rr_dtype wire, int group_size, const rr_launch_cfg *cfg,
+                    rr_launch_cfg *chosen) {
+  if (!chosen) return RR_ERR_INVALID_ARG;
+  Checked ck;
+  rr_status st = check_args(op, in_bufs, out_bufs, R, count, dtype, wire, group_size, cfg, &ck);
+  if (st != RR_OK) return st;
+  *chosen = rr_launch_cfg{RR_PATH_SIMPLE, 0, 0, 0, 0};
+  if (count == 0) return RR_OK;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != RR_OK) return st;
+  rr::RingParams p;
+  rr::Launch l;
+  st = plan(ck, in_bufs, out_bufs, cfg, dev, &p, &l);
+  if (st != RR_OK) return st;
+  chosen->path = l.path;
+  chosen->tile_bytes = l.path == RR_PATH_BULK ? p.tile_elems * (int)ck.E : 0;
+  chosen->stages = l.path == RR_PATH_BULK ? p.stages : 0;
+  chosen->ctas_per_sm = l.ctas_per_sm;
+  chosen->threads = l.threads;
+  return RR_OK;
+}
+
+size_t ring_chunk_count(size_t count, int R, int c) {
+  if (R < 1 || c < 0 || c >= R) return 0;
+  return chunk_len(count, R, c);
+}
+
+size_t ring_chunk_offset(size_t count, int R, int c) {
+  if (R < 1 || c < 0 || c >= R) return 0;
+  return (size_t)c * (count / (size_t)R);
+}
+
+const char *ring_status_string(rr_status status) {
+  switch (status) {
+    case RR_OK:
+      return "success";
+    case RR_ERR_INVALID_ARG:
+      return "invalid argument";
+    case RR_ERR_UNSUPPORTED:
+      return "unsupported dtype/wire combination or launch path";
+    case RR_ERR_ALIAS:
+      return "an output buffer overlaps another buffer";
+    case RR_ERR_CUDA:
+      return "CUDA runtime error";
+    case RR_ERR_TIMEOUT:
+      return "a bounded device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+rr_status ring_device_status(unsigned int *flags) {
+  if (!flags) return RR_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  rr_status st = current_device(&dev);
+  if (st != RR_OK) return st;
+  unsigned int v = 0, zero = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return RR_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_rr_status_word, sizeof(v)) != cudaSuccess) return RR_ERR_CUDA;
+  if (v != 0 && cudaMemcpyToSymbol(g_rr_status_word, &zero, sizeof(zero)) != cudaSuccess) return RR_ERR_CUDA;
+  *flags = v;
+  return RR_OK;
+}
+
+rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull) return RR_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  rr_status st = current_device(&dev);
+  if (st != RR_OK) return st;
+  if (rr::launch_wait_probe(dev.status, limit_ns, stream) != cudaSuccess) return RR_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return RR_ERR_CUDA;
+  unsigned int flags = 0;
+  st = ring_device_status(&flags);
+  if (st != RR_OK) return st;
+  return (flags & rr::kStatusWaitTimeout) ? RR_ERR_TIMEOUT : RR_OK;
+}
+
+int ring_abi_version(void) { return RR_ABI_VERSION; }
+
+}  // extern "C"

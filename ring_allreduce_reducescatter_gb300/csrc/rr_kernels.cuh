@@ -1,0 +1,327 @@
+// rr_kernels.cuh -- the kernels of libringred.
+//
+// Every kernel computes, for each element i of the N-element rank vectors,
+//   S_g = x_{gL+c} (+) x_{gL+c+1} (+) ... (+) x_{gL+c+L-1}   (ranks mod L)
+//   y   = S_0 (+) S_1 (+) ... (+) S_{G-1}
+// with c the chunk of i in the partition of N into L chunks and (+) one hop
+// on the wire.  That is the value the ring produces: on the page
+// hwcomputing.csdn.net/6a0dc11a10ee7a33f273f7fd.html, section
+// "Ring 通信为什么常见", block c starts on card c and picks up cards c+1, c+2,
+// ... in turn (the simplified ReduceScatter code on
+// ai6s.net/6a102b5410ee7a33f2746c06.html, section "hcomm 与 HCCL 的关系",
+// moves the chunk index back by one per step, which is the same order), and
+// the AllGather phase copies each finished block to every card.  The two-level
+// ring (page hwcomputing.csdn.net/6a0dc11a..., section "通信拓扑与带宽利用率")
+// folds the group sums of a chunk once, in group order.
+//
+// Instead of moving chunks between ranks, a kernel reads every rank's copy of
+// an element once, folds it in registers in exactly the ring's order, and
+// writes the result once per output: the zero-copy principle of
+// ai6s.net/6a102b54..., section "hcomm 的数据传输路径", carried to its end (no
+// staging buffers, each byte crosses HBM once).
+//
+//  rr_simple_kernel: one element per thread, grid-stride, plain loads/stores;
+//    any alignment.
+//  rr_bulk_kernel: persistent CTAs over tiles of the element range.  Thread 0
+//    fills S pipeline stages with bulk asynchronous copies (one tile per rank,
+//    completion counted on an mbarrier); all threads fold 16-byte vectors out
+//    of shared memory and write the result over slot 0 of the stage; thread 0
+//    then writes slot 0 to the outputs with bulk asynchronous stores and
+//    refills the previous stage.  Loads of S-1 tiles stay in flight while a
+//    tile is folded.  Every wait is bounded.
+#pragma once
+
+#include "rr_device.cuh"
+
+namespace rr {
+
+// --------------------------------------------------------------------------
+// one element, global memory
+// --------------------------------------------------------------------------
+
+template <int DT, int WT>
+__device__ __forceinline__ typename Scalar<DT, WT>::W fold_group_global(const RingParams &p, int g, int c,
+                                                                        unsigned long long i) {
+  using S = typename Fmt<DT>::type;
+  using SC = Scalar<DT, WT>;
+  const int L = p.L;
+  int r = c;
+  typename SC::W acc = SC::in(static_cast<const S *>(p.in[g * L + r])[i]);
+  for (int k = 1; k < L; ++k) {
+    r = (r + 1 == L) ? 0 : r + 1;
+    acc = hop(acc, SC::in(static_cast<const S *>(p.in[g * L + r])[i]));
+  }
+  return acc;
+}
+
+template <int DT, int WT>
+__device__ __forceinline__ typename Fmt<DT>::type fold_elem_global(const RingParams &p, unsigned long long i, int c) {
+  typename Scalar<DT, WT>::W total = fold_group_global<DT, WT>(p, 0, c, i);
+  for (int g = 1; g < p.G; ++g) total = hop(total, fold_group_global<DT, WT>(p, g, c, i));
+  return Scalar<DT, WT>::out(total);
+}
+
+// The whole collective at element i (every input read, then every output written).
+template <int OP, int DT, int WT>
+__device__ __forceinline__ void element_op(const RingParams &p, unsigned long long i) {
+  using S = typename Fmt<DT>::type;
+  const int c = chunk_of(i, p.base, p.L);
+  if (OP == kOpAllReduce) {
+    const S v = fold_elem_global<DT, WT>(p, i, c);
+    for (int r = 0; r < p.R; ++r) static_cast<S *>(p.out[r])[i] = v;
+  } else if (OP == kOpReduceScatter) {
+    const S v = fold_elem_global<DT, WT>(p, i, c);
+    static_cast<S *>(p.out[c])[i - (unsigned long long)c * p.base] = v;
+  } else {
+    const S v = static_cast<const S *>(p.in[c])[i - (unsigned long long)c * p.base];
+    for (int r = 0; r < p.R; ++r) static_cast<S *>(p.out[r])[i] = v;
+  }
+}
+
+template <int OP, int DT, int WT>
+__global__ void __launch_bounds__(1024) rr_simple_kernel(const __grid_constant__ RingParams p) {
+  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+  for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count; i += stride)
+    element_op<OP, DT, WT>(p, i);
+}
+
+// --------------------------------------------------------------------------
+// tiles in shared memory: slot r of a stage holds rank r's tile
+// --------------------------------------------------------------------------
+
+template <class VT>
+__device__ __forceinline__ typename VT::W fold_group_vec(const unsigned char *gstage, uint32_t slot_bytes, int L, int c,
+                                                         uint32_t off) {
+  int r = c;
+  typename VT::W acc = VT::in(*reinterpret_cast<const uint4 *>(gstage + (size_t)r * slot_bytes + off));
+  for (int k = 1; k < L; ++k) {
+    r = (r + 1 == L) ? 0 : r + 1;
+    acc = VT::hop(acc, VT::in(*reinterpret_cast<const uint4 *>(gstage + (size_t)r * slot_bytes + off)));
+  }
+  return acc;
+}
+
+// 16 bytes whose elements all lie in chunk c.
+template <class VT>
+__device__ __forceinline__ uint4 fold_vec_smem(const unsigned char *stage, uint32_t slot_bytes, int L, int G, int c,
+                                               uint32_t off) {
+  typename VT::W total = fold_group_vec<VT>(stage, slot_bytes, L, c, off);
+  for (int g = 1; g < G; ++g)
+    total = VT::hop(total, fold_group_vec<VT>(stage + (size_t)g * L * slot_bytes, slot_bytes, L, c, off));
+  return VT::out(total);
+}
+
+// 16 bytes that straddle a chunk boundary: element by element.
+template <int DT, int WT>
+__device__ __noinline__ uint4 fold_ragged_smem(const RingParams &p, const unsigned char *stage, uint32_t slot_bytes,
+                                               unsigned long long i0, uint32_t off) {
+  using S = typename Fmt<DT>::type;
+  using SC = Scalar<DT, WT>;
+  constexpr int V = 16 / (int)sizeof(S);
+  const int L = p.L;
+  S res[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) {
+    const int c = chunk_of(i0 + e, p.base, L);
+    const uint32_t eo = off + (uint32_t)(e * sizeof(S));
+    typename SC::W total;
+    for (int g = 0; g < p.G; ++g) {
+      const unsigned char *gs = stage + (size_t)g * L * slot_bytes + eo;
+      int r = c;
+      typename SC::W acc = SC::in(*reinterpret_cast<const S *>(gs + (size_t)r * slot_bytes));
+      for (int k = 1; k < L; ++k) {
+        r = (r + 1 == L) ? 0 : r + 1;
+        acc = hop(acc, SC::in(*reinterpret_cast<const S *>(gs + (size_t)r * slot_bytes)));
+      }
+      total = (g == 0) ? acc : hop(total, acc);
+    }
+    res[e] = SC::out(total);
+  }
+  uint4 out;
+  memcpy(&out, res, 16);
+  return out;
+}
+
+__device__ __forceinline__ unsigned long long tile_begin(const RingParams &p, unsigned long long t) {
+  return t * (unsigned long long)p.tile_elems;
+}
+__device__ __forceinline__ unsigned long long tile_end(const RingParams &p, unsigned long long t) {
+  const unsigned long long e = (t + 1) * (unsigned long long)p.tile_elems;
+  return e < p.n_bulk ? e : p.n_bulk;
+}
+
+// Fold tile t (AllReduce / ReduceScatter); the result replaces slot 0.
+template <int DT, int WT>
+__device__ __forceinline__ void compute_tile(const RingParams &p, unsigned char *stage, uint32_t slot_bytes,
+                                             unsigned long long t) {
+  using VT = Vec<DT, WT>;
+  constexpr int V = VT::V;
+  const unsigned long long t0 = tile_begin(p, t), t1 = tile_end(p, t);
+  const uint32_t nvec = (uint32_t)((t1 - t0) / V);
+  const int L = p.L, G = p.G;
+  const int c_first = chunk_of(t0, p.base, L), c_last = chunk_of(t1 - 1, p.base, L);
+  for (uint32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const uint32_t off = v * 16u;
+    int c = c_first, c1 = c_last;
+    if (c != c1) {
+      const unsigned long long i0 = t0 + (unsigned long long)v * V;
+      c = chunk_of(i0, p.base, L);
+      c1 = chunk_of(i0 + V - 1, p.base, L);
+    }
+    uint4 res;
+    if (c == c1)
+      res = fold_vec_smem<VT>(stage, slot_bytes, L, G, c, off);
+    else
+      res = fold_ragged_smem<DT, WT>(p, stage, slot_bytes, t0 + (unsigned long long)v * V, off);
+    *reinterpret_cast<uint4 *>(stage + off) = res;
+  }
+}
+
+// Fill a stage with tile t.  AllReduce / ReduceScatter: rank r's tile into
+// slot r.  AllGather: the tile of the output vector, gathered chunk by chunk
+// from the inputs into slot 0.
+template <int OP, int DT>
+__device__ __forceinline__ void issue_loads(const RingParams &p, unsigned char *stage, uint32_t slot_bytes,
+                                            uint64_t *bar, unsigned long long t, uint64_t pol) {
+  constexpr int E = Fmt<DT>::bytes;
+  const unsigned long long t0 = tile_begin(p, t), t1 = tile_end(p, t);
+  const uint32_t bytes = (uint32_t)((t1 - t0) * E);
+  if (OP != kOpAllGather) {
+    mbar_arrive_expect_tx(bar, bytes * (uint32_t)p.R);
+    for (int r = 0; r < p.R; ++r)
+      bulk_load(stage + (size_t)r * slot_bytes, static_cast<const unsigned char *>(p.in[r]) + t0 * E, bytes, bar, pol);
+  } else {
+    mbar_arrive_expect_tx(bar, bytes);
+    const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
+    for (int c = c_lo; c <= c_hi; ++c) {
+      const unsigned long long off = (unsigned long long)c * p.base;
+      const unsigned long long end = chunk_end(c, p.base, p.L, p.count);
+      const unsigned long long s0 = t0 > off ? t0 : off, s1 = t1 < end ? t1 : end;
+      if (s1 > s0)
+        bulk_load(stage + (s0 - t0) * E, static_cast<const unsigned char *>(p.in[c]) + (s0 - off) * E,
+                  (uint32_t)((s1 - s0) * E), bar, pol);
+    }
+  }
+}
+
+// Write slot 0 of a stage (tile t).  AllReduce / AllGather: to every output.
+// ReduceScatter: each chunk's part to the output of that chunk.
+template <int OP, int DT>
+__device__ __forceinline__ void issue_stores(const RingParams &p, const unsigned char *stage, unsigned long long t,
+                                             uint64_t pol) {
+  constexpr int E = Fmt<DT>::bytes;
+  const unsigned long long t0 = tile_begin(p, t), t1 = tile_end(p, t);
+  const uint32_t bytes = (uint32_t)((t1 - t0) * E);
+  if (OP != kOpReduceScatter) {
+    for (int r = 0; r < p.R; ++r) bulk_store(static_cast<unsigned char *>(p.out[r]) + t0 * E, stage, bytes, pol);
+  } else {
+    const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
+    for (int c = c_lo; c <= c_hi; ++c) {
+      const unsigned long long off = (unsigned long long)c * p.base;
+      const unsigned long long end = chunk_end(c, p.base, p.L, p.count);
+      const unsigned long long s0 = t0 > off ? t0 : off, s1 = t1 < end ? t1 : end;
+      if (s1 > s0)
+        bulk_store(static_cast<unsigned char *>(p.out[c]) + (s0 - off) * E, stage + (s0 - t0) * E,
+                   (uint32_t)((s1 - s0) * E), pol);
+    }
+  }
+}
+
+template <int OP, int DT, int WT>
+__global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ RingParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int E = Fmt<DT>::bytes;
+  const int S = p.stages;
+  const uint32_t slot_bytes = (uint32_t)p.tile_elems * E;
+  const uint32_t stage_bytes = slot_bytes * (uint32_t)p.slots;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
+
+  // tiles of this CTA: first, first + step, first + 2 step, ...
+  const unsigned long long first = blockIdx.x, step = gridDim.x;
+  const long long n_local = first < p.n_tiles ? (long long)((p.n_tiles - 1 - first) / step + 1) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t pol = l2_evict_first_policy();
+  if (threadIdx.x == 0) {
+    const long long pro = n_local < S ? n_local : S;
+    for (long long j = 0; j < pro; ++j)
+      issue_loads<OP, DT>(p, smem + (size_t)j * stage_bytes, slot_bytes, &full[j], first + (unsigned long long)j * step,
+                          pol);
+  }
+
+  // The ragged end [n_bulk, count) (less than 16 bytes per rank) goes through
+  // plain loads and stores in the last CTA, while its first tiles load.
+  if (blockIdx.x == gridDim.x - 1)
+    for (unsigned long long i = p.n_bulk + threadIdx.x; i < p.count; i += blockDim.x) element_op<OP, DT, WT>(p, i);
+
+  long long j = 0;
+  bool ok = true;
+  for (; j < n_local; ++j) {
+    const int s = (int)(j % S);
+    const uint32_t parity = (uint32_t)((j / S) & 1);
+    unsigned char *stage = smem + (size_t)s * stage_bytes;
+    const unsigned long long t = first + (unsigned long long)j * step;
+    const bool got = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
+    if (OP != kOpAllGather && got) compute_tile<DT, WT>(p, stage, slot_bytes, t);
+    fence_proxy_async_smem();
+    if (!__syncthreads_and(got)) {
+      ok = false;
+      break;
+    }
+    if (threadIdx.x == 0) {
+      issue_stores<OP, DT>(p, stage, t, pol);
+      bulk_commit();
+      // refill the stage of tile j-1 once its stores have read shared memory
+      if (j >= 1 && j - 1 + S < n_local) {
+        bulk_wait_read<1>();
+        const int sp = (int)((j - 1) % S);
+        issue_loads<OP, DT>(p, smem + (size_t)sp * stage_bytes, slot_bytes, &full[sp],
+                            first + (unsigned long long)(j - 1 + S) * step, pol);
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (!ok) {
+      atomicOr(p.status, kStatusWaitTimeout);
+      // let the loads still in flight land before the shared memory is released
+      long long issued_end = (j >= 1 ? j - 1 : 0) + S;
+      if (issued_end > n_local) issued_end = n_local;
+      for (long long u = j; u < issued_end; ++u)
+        mbar_wait_bounded(&full[u % S], (uint32_t)((u / S) & 1), kWaitLimitNs);
+    }
+    bulk_wait_all();
+  }
+}
+
+// A single CTA waits on a barrier that nothing completes; the bounded wait
+// must give up and record it.
+__global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long limit_ns);
+
+// --------------------------------------------------------------------------
+// host side: one launch of (OP, DT, WT)
+// --------------------------------------------------------------------------
+
+template <int OP, int DT, int WT>
+cudaError_t launch_one(const RingParams &p, const Launch &l, cudaStream_t s) {
+  if (l.path == RR_PATH_BULK) {
+    static int smem_set[64] = {0};  // largest dynamic shared memory opted in, per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (l.smem > 48 * 1024 && (dev >= 64 || smem_set[dev] < (int)l.smem)) {
+      e = cudaFuncSetAttribute(rr_bulk_kernel<OP, DT, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) smem_set[dev] = (int)l.smem;
+    }
+    rr_bulk_kernel<OP, DT, WT><<<l.grid, l.threads, l.smem, s>>>(p);
+  } else {
+    rr_simple_kernel<OP, DT, WT><<<l.grid, l.threads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rr

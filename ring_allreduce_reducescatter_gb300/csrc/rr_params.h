@@ -1,0 +1,56 @@
+// rr_params.h -- the parameter block of every libringred kernel and the
+// internal launcher interface between the C ABI (rr_api.cu) and the kernel
+// translation units (rr_inst_*.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ringred.h"
+
+namespace rr {
+
+enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum : int { kOpAllReduce = 0, kOpReduceScatter = 1, kOpAllGather = 2 };
+
+// Device status bits (the word lives in rr_api.cu).
+enum : unsigned int { kStatusWaitTimeout = 1u };
+
+// Limit of one bounded wait inside a kernel.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Passed by value as a __grid_constant__ kernel parameter (about 1.1 KB).
+struct RingParams {
+  const void *in[RR_MAX_RANKS];
+  void *out[RR_MAX_RANKS];
+  unsigned long long count;       // N, elements per rank vector
+  unsigned long long base;        // floor(N / L): length of every chunk but the last
+  unsigned long long n_bulk;      // bulk path: elements [0, n_bulk) go through tiles
+  unsigned long long n_tiles;     // bulk path: ceil(n_bulk / tile_elems)
+  unsigned int *status;           // device status word
+  int R;                          // ranks
+  int L;                          // ranks per group (chunk table of (N, L))
+  int G;                          // groups, R / L
+  int tile_elems;                 // bulk path: elements per rank per tile
+  int stages;                     // bulk path: pipeline depth
+  int slots;                      // bulk path: tiles of one stage (R, or 1 for AllGather)
+};
+
+// One launch, fully resolved by the planner.
+struct Launch {
+  int path;         // RR_PATH_BULK or RR_PATH_SIMPLE
+  int grid;
+  int threads;
+  size_t smem;      // dynamic shared memory bytes
+  int ctas_per_sm;
+};
+
+// Defined in rr_inst_<storage>.cu: launch the kernel of (op, storage dtype,
+// wire) on `stream`; returns the launch error.
+cudaError_t launch_f32(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+cudaError_t launch_f16(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+cudaError_t launch_bf16(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+// Defined in rr_inst_f32.cu: the bounded-wait self test kernel.
+cudaError_t launch_wait_probe(unsigned int *status, unsigned long long limit_ns, cudaStream_t s);
+
+}  // namespace rr

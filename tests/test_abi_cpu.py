@@ -1,0 +1,201 @@
+"""Host-side tests of the C ABI: no GPU needed, no kernel launched.
+
+The library must load, export every function include/ringred.h declares, and
+reject bad arguments before it makes any CUDA call (the validation runs on the
+host), so fake device addresses are enough here.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ringred.h")
+
+OK, EINVAL, EUNSUP, EALIAS, ECUDA, ETIMEOUT = range(6)
+AR, RS, AG = 0, 1, 2
+F32, F16, BF16 = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    from ring_allreduce_reducescatter_gb300 import _build
+
+    _build.build()
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    return rr.lib()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:rr_status|size_t|const char|int)\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_collectives():
+    names = declared_functions()
+    for want in ("ring_allreduce", "ring_reduce_scatter", "ring_allgather", "ring_allreduce_ex",
+                 "ring_reduce_scatter_ex", "ring_collective", "ring_plan", "ring_chunk_count",
+                 "ring_chunk_offset", "ring_status_string", "ring_device_status",
+                 "ring_selftest_bounded_wait", "ring_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_abi_version(L):
+    assert L.ring_abi_version() == 1
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert L.ring_status_string(s)
+    assert b"unknown" in L.ring_status_string(77)
+
+
+def test_chunk_table_agrees_with_oracle(L):
+    for R in range(1, 17):
+        for N in list(range(0, 70)) + [1_048_576, 50_000_017, 16_777_216, 2 ** 33 + 7]:
+            for c in range(R):
+                assert L.ring_chunk_count(N, R, c) == oracle.chunk_len(N, R, c)
+                assert L.ring_chunk_offset(N, R, c) == oracle.chunk_off(N, R, c)
+    assert L.ring_chunk_count(10, 0, 0) == 0
+    assert L.ring_chunk_count(10, 4, 4) == 0
+    assert L.ring_chunk_offset(10, 4, -1) == 0
+
+
+def ptrs(vals):
+    arr = (ctypes.c_void_p * len(vals))()
+    for k, v in enumerate(vals):
+        arr[k] = v
+    return arr
+
+
+BASE = 0x7F0000000000  # fake, never dereferenced
+
+
+def fake(R, count, E, gap=1 << 24):
+    ins = [BASE + r * gap for r in range(R)]
+    outs = [BASE + (R + r) * gap for r in range(R)]
+    return ins, outs
+
+
+def call(L, op, ins, outs, R, count, dtype, wire=None, group=0, cfg=None):
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    wire = dtype if wire is None else wire
+    c = None
+    if cfg is not None:
+        c = ctypes.byref(rr.LaunchCfg(*cfg))
+    return L.ring_collective(op, ptrs(ins) if ins is not None else None,
+                             ptrs(outs) if outs is not None else None, R, count, dtype, wire, group, c, None)
+
+
+def test_bad_rank_counts(L):
+    ins, outs = fake(64, 100, 4)
+    assert call(L, AR, ins[:0], outs[:0], 0, 100, F32) == EINVAL
+    assert call(L, AR, ins + [BASE], outs + [BASE], 65, 100, F32) == EINVAL
+
+
+def test_bad_dtypes_and_pairs(L):
+    ins, outs = fake(4, 100, 4)
+    assert call(L, AR, ins, outs, 4, 100, 3) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F16, F32) == EUNSUP
+    assert call(L, AR, ins, outs, 4, 100, F16, BF16) == EUNSUP
+    assert call(L, AR, ins, outs, 4, 100, BF16, F16) == EUNSUP
+    assert call(L, AG, ins, outs, 4, 100, F32, BF16) == EUNSUP
+
+
+def test_bad_group_sizes(L):
+    ins, outs = fake(8, 100, 4)
+    assert call(L, AR, ins, outs, 8, 100, F32, group=3) == EINVAL
+    assert call(L, AR, ins, outs, 8, 100, F32, group=16) == EINVAL
+    assert call(L, AR, ins, outs, 8, 100, F32, group=-1) == EINVAL
+    assert call(L, RS, ins, outs, 8, 100, F32, group=4) == EINVAL
+    assert call(L, AG, ins, outs, 8, 100, F32, group=2) == EINVAL
+
+
+def test_null_and_misaligned_pointers(L):
+    ins, outs = fake(4, 100, 4)
+    assert call(L, AR, None, outs, 4, 100, F32) == EINVAL
+    assert call(L, AR, ins, None, 4, 100, F32) == EINVAL
+    assert call(L, AR, [0] + ins[1:], outs, 4, 100, F32) == EINVAL
+    assert call(L, AR, ins, outs[:3] + [0], 4, 100, F32) == EINVAL
+    assert call(L, AR, [ins[0] + 2] + ins[1:], outs, 4, 100, F32) == EINVAL  # not 4-byte aligned
+    assert call(L, AR, ins, [outs[0] + 1] + outs[1:], 4, 100, F16) == EINVAL
+    # zero-length buffers may be NULL: AllGather with N < R has empty chunks 0..R-2
+    r = call(L, AG, [0, 0, 0, ins[3]], outs, 4, 3, F32)
+    assert r not in (EINVAL, EALIAS, EUNSUP)
+
+
+def test_count_zero_is_a_no_op(L):
+    assert call(L, AR, [0] * 4, [0] * 4, 4, 0, F32) == OK
+    assert call(L, RS, [0] * 4, [0] * 4, 4, 0, F16) == OK
+    assert call(L, AG, [0] * 4, [0] * 4, 4, 0, BF16) == OK
+
+
+def test_huge_count_and_address_wrap(L):
+    ins, outs = fake(2, 100, 4)
+    assert call(L, AR, ins, outs, 2, 2 ** 62, F32) == EINVAL
+    top = (1 << 64) - 64
+    assert call(L, AR, [top, ins[1]], outs, 2, 100, F32) == EINVAL
+
+
+def test_aliasing(L):
+    R, N, E = 4, 1000, 4
+    ins, outs = fake(R, N, E)
+    # outputs overlapping each other
+    assert call(L, AR, ins, [outs[0], outs[0] + 400] + outs[2:], R, N, F32) == EALIAS
+    # an output overlapping another rank's input
+    assert call(L, AR, ins, [ins[1] + 16] + outs[1:], R, N, F32) == EALIAS
+    # partial overlap with its own input
+    assert call(L, AR, ins, [ins[0] + 16] + outs[1:], R, N, F32) == EALIAS
+    # in place is allowed for AllReduce (validation passes; the call then needs a device)
+    assert call(L, AR, ins, list(ins), R, N, F32) not in (EALIAS, EINVAL, EUNSUP)
+    # ... but not for ReduceScatter / AllGather
+    assert call(L, RS, ins, list(ins), R, N, F32) == EALIAS
+    assert call(L, AG, ins, list(ins), R, N, F32) == EALIAS
+    # inputs may overlap one another (they are only read)
+    assert call(L, AR, [ins[0]] * R, outs, R, N, F32) not in (EALIAS, EINVAL, EUNSUP)
+    # ReduceScatter outputs are chunk-sized: back to back is fine, one byte more is not
+    rs_len = N // R * E
+    packed = [outs[0] + k * rs_len for k in range(R)]
+    assert call(L, RS, ins, packed, R, N, F32) not in (EALIAS, EINVAL, EUNSUP)
+    assert call(L, RS, ins, [packed[0], packed[1] - 4] + packed[2:], R, N, F32) == EALIAS
+
+
+def test_bad_launch_cfg(L):
+    ins, outs = fake(4, 100, 4)
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(3, 0, 0, 0, 0)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 24, 0, 0, 0)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 9, 0, 0)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 1, 0, 0)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 0, 5, 0)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 0, 0, 1000)) == EINVAL
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    monkeypatch.setattr(rr, "_lib", None)
+    monkeypatch.setattr(rr, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        rr.lib()
+
+
+def test_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "ring_allreduce_reducescatter_gb300")
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle|#\s*include\s*[<\"].*oracle)", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                with open(os.path.join(dirpath, fn)) as f:
+                    assert not pat.search(f.read()), fn

@@ -1,0 +1,95 @@
+"""Host logic of bench.py at N > 1, on CPU: two gloo ranks.
+
+The benchmark runs independent replicas (the ring collective on one GPU has no
+exchange between GPUs); the job time is the slowest replica's, and the value
+is the sum of every replica's work over that time.
+"""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local = [10.0 + 5 * rank, 1.0 + rank]  # the second rank is slower
+    got = bench.combine_ranks(dist, local)
+    value = bench.job_throughput(world, 1 << 20, got[0])
+    # only rank 0 of the reference arm does work and prints
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        if rank != 0:
+            bench.run_reference(type("A", (), dict(warmup=3, steps=1, msg_mib=512, ref_sample_mib=1))())
+    q.put((rank, got, value, buf.getvalue()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_and_aggregate():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, got, value, out in results:
+        assert got == [15.0, 2.0]  # max over ranks, element-wise
+        assert value == pytest.approx(2 * (1 << 20) / 15e-3 / 1e9)
+        if rank != 0:
+            assert out == ""
+
+
+def test_single_process_combine_is_identity():
+    assert bench.combine_ranks(None, [3.0, 4.0]) == [3.0, 4.0]
+    assert bench.job_throughput(1, 512 << 20, 1.0) == pytest.approx((512 << 20) / 1e-3 / 1e9)
+
+
+def test_reference_arm_prints_one_json_line(monkeypatch):
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    args = type("A", (), dict(warmup=3, steps=2, msg_mib=512, ref_sample_mib=1))()
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(args)
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_clock_summary_flags_throttling():
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.samples = [(1.0, ["1900", "2070", "900", "0x0", "Not Active", "Not Active", "Not Active", "Active"]),
+                 (1.2, ["1950", "2070", "950", "0x0", "Not Active", "Active", "Not Active", "Not Active"]),
+                 (5.0, ["300", "2070", "100", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"])]
+    c = s.summary(0.9, 1.3)
+    assert c["samples"] == 2 and c["sm_mhz"] == 1925.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]

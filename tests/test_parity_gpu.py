@@ -1,0 +1,359 @@
+"""GPU parity: libringred's CUDA kernels against the CPU oracle, bit for bit.
+
+Every case runs through the C ABI (the Python binding only marshals) and is
+compared element by element with the oracle's literal ring simulation, or, at
+the full workload sizes, on sampled elements with the oracle's closed form
+plus size-independent properties.  The bar is bit-exact for every format:
+both sides follow the same accumulation order and rounding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+PAIRS = [(torch.float32, None), (torch.float16, None), (torch.bfloat16, None), (torch.float32, "bf16"),
+         (torch.float32, "f16")]
+
+
+@pytest.fixture(scope="module")
+def rr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import ring_allreduce_reducescatter_gb300 as mod
+
+    torch.cuda.set_device(0)
+    return mod
+
+
+@pytest.fixture(scope="module")
+def wl():
+    from ring_allreduce_reducescatter_gb300 import workloads
+
+    return workloads
+
+
+def host(t):
+    """Tensor -> numpy array in the oracle's element convention."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits(a):
+    a = np.asarray(a)
+    return a.view(np.uint32) if a.dtype == np.float32 else a.view(np.uint16)
+
+
+def assert_same(got, want, what):
+    g, w = bits(got), bits(want)
+    assert g.shape == w.shape, (what, g.shape, w.shape)
+    if not np.array_equal(g, w):
+        bad = np.flatnonzero(g != w)
+        raise AssertionError(f"{what}: {bad.size} of {g.size} elements differ, first at {int(bad[0])}: "
+                             f"got {int(g[bad[0]]):#x} want {int(w[bad[0]]):#x}")
+
+
+def gen(R, N, dtype, seed, dev="cuda", scale=1.0, lengths=None):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    xs = []
+    for r in range(R):
+        n = N if lengths is None else lengths[r]
+        x = torch.randn(n, generator=g, device=dev, dtype=torch.float32) * scale
+        # sprinkle exact ties and cancellations
+        if n:
+            k = torch.randint(0, n, (max(1, n // 8),), generator=g, device=dev)
+            v = torch.tensor([1.0, -1.0, 2.0 ** -11, 2.0 ** -24, 2.0 ** -8, 0.0], device=dev)
+            x[k] = v[torch.randint(0, v.numel(), (k.numel(),), generator=g, device=dev)]
+        xs.append(x.to(dtype))
+    return xs
+
+
+def cfg_of(rr, path=0, tile=0, stages=0, ctas=0, threads=0):
+    return rr.LaunchCfg(path, tile, stages, ctas, threads)
+
+
+def run_ar(rr, xs, wire=None, group=0, cfg=None, inplace=False):
+    if inplace:
+        outs = [x.clone() for x in xs]
+        rr.collective(rr.OP_ALLREDUCE, outs, outs, xs[0].numel(), wire, group, None, cfg)
+        return outs
+    outs = [torch.empty_like(x) for x in xs]
+    rr.collective(rr.OP_ALLREDUCE, xs, outs, xs[0].numel(), wire, group, None, cfg)
+    return outs
+
+
+def check_ar(rr, xs, wire=None, group=0, cfg=None, inplace=False, what=""):
+    outs = run_ar(rr, xs, wire, group, cfg, inplace)
+    torch.cuda.synchronize()
+    dt = NAME[xs[0].dtype]
+    ref = oracle.allreduce([host(x) for x in xs], dt, wire, group)
+    assert ref.status == oracle.OK
+    for r in range(len(xs)):
+        assert_same(host(outs[r]), ref.outs[r], f"{what} rank {r}")
+
+
+def check_rs(rr, xs, wire=None, cfg=None, what=""):
+    R, N = len(xs), xs[0].numel()
+    outs = [torch.empty(rr.chunk_count(N, R, r), dtype=xs[0].dtype, device=xs[0].device) for r in range(R)]
+    rr.collective(rr.OP_REDUCE_SCATTER, xs, outs, N, wire, 0, None, cfg)
+    torch.cuda.synchronize()
+    ref = oracle.reduce_scatter([host(x) for x in xs], NAME[xs[0].dtype], wire)
+    assert ref.status == oracle.OK
+    for r in range(R):
+        assert_same(host(outs[r]), ref.outs[r], f"{what} rank {r}")
+
+
+def check_ag(rr, chunks, N, cfg=None, what=""):
+    R = len(chunks)
+    outs = [torch.empty(N, dtype=chunks[0].dtype, device="cuda") for _ in range(R)]
+    rr.collective(rr.OP_ALLGATHER, chunks, outs, N, None, 0, None, cfg)
+    torch.cuda.synchronize()
+    ref = oracle.allgather([host(c) for c in chunks], N, NAME[chunks[0].dtype])
+    assert ref.status == oracle.OK
+    for r in range(R):
+        assert_same(host(outs[r]), ref.outs[r], f"{what} rank {r}")
+
+
+def counts_for(R):
+    c = {0, 1, 2, R - 1, R, R + 1, 2 * R + 3, 255, 4095, 4096, 4097, 65535, 65536, 65537, 100_003}
+    return sorted(x for x in c if x >= 0)
+
+
+# --------------------------------------------------------------------------
+# edge grid: ranks x counts x formats x launch paths
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 7, 8, 16])
+def test_allreduce_edge_grid(rr, dtype, wire, R):
+    seed = 100 * R + 7
+    for N in counts_for(R):
+        xs = gen(R, N, dtype, seed + N)
+        tag = f"AR {NAME[dtype]}/{wire} R={R} N={N}"
+        check_ar(rr, xs, wire, what=tag + " auto")
+        check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+        if N * xs[0].element_size() >= 16:
+            # tiny tiles: tiles straddle many chunks, vectors straddle chunk boundaries
+            check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=64, stages=3), what=tag + " bulk64")
+            check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=1024, stages=8, ctas=1,
+                                               threads=128), what=tag + " bulk1k")
+    xs = gen(R, 65537, dtype, seed)
+    check_ar(rr, xs, wire, inplace=True, what=f"AR in place R={R}")
+
+
+@pytest.mark.parametrize("G,L", [(2, 8), (2, 2), (3, 4), (4, 1), (2, 4), (8, 2)])
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_two_level_grid(rr, G, L, dtype, wire):
+    R = G * L
+    for N in (1, L - 1, L + 1, 4095, 65537, 100_003):
+        if N < 1:
+            continue
+        xs = gen(R, N, dtype, 31 * R + N)
+        tag = f"2lvl {G}x{L} {NAME[dtype]}/{wire} N={N}"
+        check_ar(rr, xs, wire, group=L, what=tag)
+        check_ar(rr, xs, wire, group=L, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+        if N * xs[0].element_size() >= 16:
+            check_ar(rr, xs, wire, group=L, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=128), what=tag + " bulk128")
+
+
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+def test_reduce_scatter_grid(rr, dtype, wire, R):
+    for N in counts_for(R) + [R * 1024, R * 4096 + 8 * R]:
+        xs = gen(R, N, dtype, 17 * R + N)
+        tag = f"RS {NAME[dtype]}/{wire} R={R} N={N}"
+        check_rs(rr, xs, wire, what=tag)
+        check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16], ids=str)
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+def test_allgather_grid(rr, dtype, R):
+    for N in counts_for(R) + [R * 1024, R * 4096 + 8 * R]:
+        lens = [oracle.chunk_len(N, R, c) for c in range(R)]
+        chunks = gen(R, 0, dtype, 23 * R + N, lengths=lens)
+        tag = f"AG {NAME[dtype]} R={R} N={N}"
+        check_ag(rr, chunks, N, what=tag)
+        check_ag(rr, chunks, N, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+
+
+def test_bulk_path_is_chosen_when_aligned(rr):
+    xs = gen(8, 1 << 20, torch.float16, 5)
+    outs = [torch.empty_like(x) for x in xs]
+    assert rr.plan(rr.OP_ALLREDUCE, xs, outs, 1 << 20)["path"] == rr.PATH_BULK
+    # chunk boundaries off the 16-byte grid: ReduceScatter takes the simple path
+    N = 8 * 1001
+    xs = gen(8, N, torch.float16, 5)
+    rs = [torch.empty(N // 8, dtype=torch.float16, device="cuda") for _ in range(8)]
+    assert rr.plan(rr.OP_REDUCE_SCATTER, xs, rs, N)["path"] == rr.PATH_SIMPLE
+    with pytest.raises(rr.RingError) as e:
+        rr.collective(rr.OP_REDUCE_SCATTER, xs, rs, N, cfg=cfg_of(rr, path=rr.PATH_BULK))
+    assert e.value.status == rr.ERR_UNSUPPORTED
+
+
+def test_misaligned_buffers(rr):
+    # element-aligned but not 16-byte aligned views: the simple path, same bits
+    for dtype, wire in PAIRS:
+        R, N = 5, 70_001
+        bufs = gen(R, N + 3, dtype, 77)
+        xs = [b[1 + (r % 3): 1 + (r % 3) + N] for r, b in enumerate(bufs)]
+        check_ar(rr, xs, wire, what=f"misaligned {NAME[dtype]}/{wire}")
+
+
+def test_outputs_do_not_write_outside(rr):
+    # guard bands around every output stay untouched (both paths, all ops)
+    R, N = 8, 100_003
+    for dtype in (torch.float32, torch.float16):
+        xs = gen(R, N, dtype, 9)
+        pad = 64
+        for path in (rr.PATH_AUTO, rr.PATH_SIMPLE):
+            big = [torch.full((N + 2 * pad,), 7.0, dtype=dtype, device="cuda") for _ in range(R)]
+            outs = [b[pad:pad + N] for b in big]
+            rr.collective(rr.OP_ALLREDUCE, xs, outs, N, cfg=cfg_of(rr, path=path))
+            torch.cuda.synchronize()
+            for b in big:
+                assert torch.all(b[:pad] == 7.0) and torch.all(b[pad + N:] == 7.0)
+        M = 8 * 4096
+        xs = gen(R, M, dtype, 10)
+        big = [torch.full((M // 8 + 2 * pad,), 7.0, dtype=dtype, device="cuda") for _ in range(R)]
+        outs = [b[pad:pad + M // 8] for b in big]
+        rr.collective(rr.OP_REDUCE_SCATTER, xs, outs, M)
+        torch.cuda.synchronize()
+        for b in big:
+            assert torch.all(b[:pad] == 7.0) and torch.all(b[pad + M // 8:] == 7.0)
+
+
+def test_alias_rejected_on_device_buffers(rr):
+    xs = gen(4, 1024, torch.float32, 1)
+    big = torch.empty(4096 + 16, device="cuda")
+    outs = [big[0:1024], big[512:1536], big[2048:3072], big[3072:4096]]
+    with pytest.raises(rr.RingError) as e:
+        rr.allreduce(xs, outs=outs)
+    assert e.value.status == rr.ERR_ALIAS
+
+
+def test_bounded_wait_gives_up_and_context_survives(rr):
+    import time
+
+    t = time.time()
+    st = rr.selftest_bounded_wait(50_000_000)  # 50 ms
+    dt = time.time() - t
+    assert st == rr.ERR_TIMEOUT
+    assert dt >= 0.04
+    assert rr.device_status() == 0  # the self test cleared its bit
+    xs = gen(4, 4099, torch.float32, 3)
+    check_ar(rr, xs, what="after bounded-wait self test")
+
+
+def test_streams_and_ordering(rr):
+    # the call enqueues on the given stream: back-to-back dependent calls on a side stream
+    s = torch.cuda.Stream()
+    xs = gen(4, 1 << 16, torch.float32, 4)
+    with torch.cuda.stream(s):
+        a = rr.allreduce(xs, stream=s)
+        b = rr.allreduce(a, stream=s)
+    s.synchronize()
+    ref_a = oracle.allreduce([host(x) for x in xs], "f32")
+    ref_b = oracle.allreduce(ref_a.outs, "f32")
+    for r in range(4):
+        assert_same(host(b[r]), ref_b.outs[r], f"chained rank {r}")
+
+
+# --------------------------------------------------------------------------
+# the workloads, at full size, in the launch configuration the benchmark uses
+# --------------------------------------------------------------------------
+
+def sample_indices(N, L, k=1 << 19, seed=0):
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, N, size=k)]
+    base = N // L
+    for c in range(1, L):
+        b = c * base
+        idx.append(np.arange(max(0, b - 24), min(N, b + 24)))
+    idx.append(np.arange(0, min(N, 64)))
+    idx.append(np.arange(max(0, N - 64), N))
+    return np.unique(np.concatenate(idx)).astype(np.int64)
+
+
+def check_sampled(rr, xs, outs, wire=None, group=0, what=""):
+    R, N = len(xs), xs[0].numel()
+    L = group or R
+    idx = sample_indices(N, L)
+    ti = torch.from_numpy(idx).cuda()
+    vals = [host(x[ti]) for x in xs]
+    want = oracle.fold_gathered(vals, idx.astype(np.uint64), N, NAME[xs[0].dtype], wire, group)
+    for r in range(R):
+        assert_same(host(outs[r][ti]), want, f"{what} sampled rank {r}")
+        if r:
+            assert torch.equal(outs[r].view(torch.int16 if outs[r].element_size() == 2 else torch.int32),
+                               outs[0].view(torch.int16 if outs[0].element_size() == 2 else torch.int32)), \
+                f"{what}: output {r} differs from output 0"
+
+
+def test_workload1_full(rr, wl):
+    w = wl.config1()
+    xs = wl.inputs(w, "cuda")
+    check_ar(rr, xs, what="workload 1 AR")
+    check_rs(rr, xs, what="workload 1 RS")
+    lens = [rr.chunk_count(w.count, w.R, c) for c in range(w.R)]
+    chunks = wl.inputs(wl.config1("allgather"), "cuda", lengths=lens)
+    check_ag(rr, chunks, w.count, what="workload 1 AG")
+
+
+@pytest.mark.parametrize("mib", [1, 16])
+def test_workload2_full_oracle(rr, wl, mib):
+    xs = wl.inputs(wl.config2(mib), "cuda")
+    check_ar(rr, xs, what=f"workload 2 {mib} MiB")
+
+
+@pytest.mark.parametrize("mib", [128, 512])
+def test_workload2_sampled(rr, wl, mib):
+    xs = wl.inputs(wl.config2(mib), "cuda")
+    outs = rr.allreduce(xs)
+    torch.cuda.synchronize()
+    check_sampled(rr, xs, outs, what=f"workload 2 {mib} MiB")
+    del outs, xs
+    torch.cuda.empty_cache()
+
+
+def test_workload3_sampled_full_size(rr, wl):
+    w = wl.config3()
+    xs = wl.inputs(w, "cuda")
+    outs = rr.allreduce(xs, wire="bf16")
+    torch.cuda.synchronize()
+    check_sampled(rr, xs, outs, wire="bf16", what="workload 3")
+
+
+def test_workload3_shape_full_oracle(rr):
+    # the same formats and an uneven prime-like count, small enough for the literal oracle
+    N = 5_000_011
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3000)
+    xs = [torch.randn(N, generator=g, device="cuda") for _ in range(8)]
+    check_ar(rr, xs, "bf16", what="workload 3 shape")
+
+
+def test_workload4_full_oracle(rr, wl):
+    w = wl.config4()
+    xs = wl.inputs(w, "cuda")
+    check_ar(rr, xs, group=w.group_size, what="workload 4")
+
+
+@pytest.mark.parametrize("bucket", [0, 48])
+def test_workload5_bucket_sampled(rr, wl, bucket):
+    w = wl.config5(bucket)
+    xs = wl.inputs(w, "cuda", bucket=bucket)
+    outs = rr.allreduce(xs)
+    torch.cuda.synchronize()
+    check_sampled(rr, xs, outs, what=f"workload 5 bucket {bucket}")
+    del outs, xs
+    torch.cuda.empty_cache()
