@@ -159,6 +159,19 @@ rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs,
                     size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
                     const rr_launch_cfg *cfg, rr_launch_cfg *chosen);
 
+/*
+ * ring_plan_device -- the planner of ring_collective for a described device
+ * instead of the current one: sm_count SMs, smem_per_sm bytes of shared
+ * memory per SM, smem_per_block_optin bytes per CTA at most, and buffers that
+ * are (buffers_16b_aligned != 0) or are not all 16-byte aligned.  Pure host
+ * computation, no CUDA call.  *chosen as for ring_plan; *grid receives the
+ * CTA count and *smem_bytes the dynamic shared memory of one CTA.  count must
+ * be positive.
+ */
+rr_status ring_plan_device(rr_op op, int R, size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
+                           int buffers_16b_aligned, int sm_count, int smem_per_sm, int smem_per_block_optin,
+                           const rr_launch_cfg *cfg, rr_launch_cfg *chosen, int *grid, size_t *smem_bytes);
+
 /* [p2] chunk table: length and offset of chunk c of `count` elements split
  * over R ranks (0 when R < 1 or c is out of range). */
 size_t ring_chunk_count(size_t count, int R, int c);

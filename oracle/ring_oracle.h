@@ -36,6 +36,10 @@
  *     sums of a chunk are folded in group order 0..G-1 by a chain of sends
  *     between the chunk's owners, and the total is sent back along the chain.
  *
+ * Parity unpinned: the group order of the two-level fold when there are more
+ * than two groups (the pages fix nothing there; with two groups every order
+ * gives the same bits, which the tests check).
+ *
  * Element storage: ORC_F32 elements are IEEE binary32; ORC_F16 and ORC_BF16
  * elements are 16-bit encodings held in uint16_t.
  */

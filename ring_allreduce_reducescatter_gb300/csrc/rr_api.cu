@@ -71,8 +71,9 @@ struct Checked {
   bool all_16b_aligned;
 };
 
-rr_status check_args(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
-                     int group_size, const rr_launch_cfg *cfg, Checked *ck) {
+// Checks of everything but the buffers.
+rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int group_size, const rr_launch_cfg *cfg,
+                        Checked *ck) {
   if (op != RR_OP_ALLREDUCE && op != RR_OP_REDUCE_SCATTER && op != RR_OP_ALLGATHER) return RR_ERR_INVALID_ARG;
   if (R < 1 || R > RR_MAX_RANKS) return RR_ERR_INVALID_ARG;
   if (!valid_type(dtype) || !valid_type(wire)) return RR_ERR_INVALID_ARG;
@@ -81,7 +82,6 @@ rr_status check_args(int op, const void *const *in, void *const *out, int R, siz
   const int L = group_size == 0 ? R : group_size;
   if (L < 1 || L > R || R % L != 0) return RR_ERR_INVALID_ARG;
   if (op != RR_OP_ALLREDUCE && L != R) return RR_ERR_INVALID_ARG;
-  if (!in || !out) return RR_ERR_INVALID_ARG;
   if (cfg) {
     if (cfg->path < RR_PATH_AUTO || cfg->path > RR_PATH_SIMPLE) return RR_ERR_INVALID_ARG;
     if (cfg->tile_bytes != 0 && (cfg->tile_bytes < 16 || cfg->tile_bytes % 16 != 0 || cfg->tile_bytes > (1 << 20)))
@@ -99,9 +99,17 @@ rr_status check_args(int op, const void *const *in, void *const *out, int R, siz
   ck->count = count;
   ck->E = elem_bytes(dtype);
   ck->all_16b_aligned = true;
+  if (count > (SIZE_MAX / 4) / ck->E) return RR_ERR_INVALID_ARG;
+  return RR_OK;
+}
+
+rr_status check_args(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
+                     int group_size, const rr_launch_cfg *cfg, Checked *ck) {
+  rr_status st = check_scalars(op, R, count, dtype, wire, group_size, cfg, ck);
+  if (st != RR_OK) return st;
+  if (!in || !out) return RR_ERR_INVALID_ARG;
   if (count == 0) return RR_OK;
   const size_t E = ck->E;
-  if (count > (SIZE_MAX / 4) / E) return RR_ERR_INVALID_ARG;
 
   // sizes, pointers, alignment
   Buf bufs[2 * RR_MAX_RANKS];
@@ -136,25 +144,25 @@ rr_status check_args(int op, const void *const *in, void *const *out, int R, siz
 
 int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
-// Resolve the launch and fill the kernel parameters.
-rr_status plan(const Checked &ck, const void *const *in, void *const *out, const rr_launch_cfg *cfg,
-               const DeviceInfo &dev, rr::RingParams *p, rr::Launch *l) {
+unsigned round16_down(unsigned long long x) { return (unsigned)(x & ~15ull); }
+
+// Resolve the launch: path, tiles, stages, grid.  Fills every field of *p
+// except the buffer pointers and the status word.  Every tile size it picks is
+// a multiple of 16 bytes (the bulk copies and the 16-byte shared-memory
+// vectors need it) and every shared-memory size fits the device.
+rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int smem_per_sm, int smem_optin,
+                      rr::RingParams *p, rr::Launch *l) {
   const rr_launch_cfg zero = {0, 0, 0, 0, 0};
   const rr_launch_cfg &c = cfg ? *cfg : zero;
   const size_t E = ck.E;
   const unsigned long long N = ck.count;
+  if (sms < 1 || smem_per_sm < 1 || smem_optin < 1) return RR_ERR_INVALID_ARG;
 
-  *p = rr::RingParams{};
-  for (int r = 0; r < ck.R; ++r) {
-    p->in[r] = in[r];
-    p->out[r] = out[r];
-  }
   p->count = N;
   p->R = ck.R;
   p->L = ck.L;
   p->G = ck.R / ck.L;
   p->base = N / (unsigned long long)ck.L;
-  p->status = dev.status;
 
   // bulk path: 16-byte aligned buffers, and for ReduceScatter / AllGather
   // chunk boundaries on 16-byte multiples (segments are copied per chunk)
@@ -169,48 +177,74 @@ rr_status plan(const Checked &ck, const void *const *in, void *const *out, const
   l->threads = c.threads ? c.threads : 256;
   if (path == RR_PATH_SIMPLE) {
     const unsigned long long blocks = (N + l->threads - 1) / l->threads;
-    const unsigned long long cap = (unsigned long long)dev.sms * 8;
-    l->grid = (int)(blocks < cap ? blocks : cap);
+    const unsigned long long cap = (unsigned long long)sms * 8;
+    l->grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
     l->smem = 0;
     l->ctas_per_sm = 0;
     p->n_bulk = 0;
     p->n_tiles = 0;
+    p->tile_elems = 0;
+    p->stages = 0;
+    p->slots = 0;
     return RR_OK;
   }
 
   const int slots = ck.op == RR_OP_ALLGATHER ? 1 : ck.R;
   const int ctas = c.ctas_per_sm ? c.ctas_per_sm : 2;
   // shared memory of one CTA: its share of the SM, less 1 KB the runtime keeps per CTA
-  int budget = dev.smem_per_sm / ctas - 1024;
-  if (budget > dev.smem_optin) budget = dev.smem_optin;
+  long long budget = (long long)smem_per_sm / ctas - 1024;
+  if (budget > smem_optin) budget = smem_optin;
+  if (budget < 64) return RR_ERR_UNSUPPORTED;
   const unsigned long long total_bytes = n_bulk * E;
 
-  int tile = c.tile_bytes;
+  unsigned long long tile = (unsigned long long)c.tile_bytes;
   if (tile == 0) {
-    tile = clamp_int((32768 / slots) & ~15, 512, 16384);
-    // keep at least two tiles per CTA slot when the message is small
-    const unsigned long long want = 2ull * dev.sms * ctas;
-    while (tile > 1024 && (total_bytes + tile - 1) / tile < want) tile /= 2;
+    tile = round16_down(32768 / slots);
+    if (tile < 512) tile = 512;
+    if (tile > 16384) tile = 16384;
+    // keep at least two tiles per CTA when the message is small
+    const unsigned long long want = 2ull * (unsigned long long)sms * ctas;
+    while (tile > 1024 && (total_bytes + tile - 1) / tile < want) tile = round16_down(tile / 2);
     // keep two stages within the shared-memory budget
-    while (tile > 16 && 2ull * ((unsigned long long)tile * slots + 8) > (unsigned long long)budget) tile = (tile / 2) & ~15;
+    while (tile > 16 && 2ull * (tile * slots + 8) > (unsigned long long)budget) tile = round16_down(tile / 2);
   }
-  if (tile % (int)E != 0 || tile < 16) return RR_ERR_INVALID_ARG;
-  const unsigned long long stage_bytes = (unsigned long long)tile * slots;
+  if (tile < 16 || tile % 16 != 0 || tile % E != 0) return RR_ERR_INVALID_ARG;
+  const unsigned long long stage_bytes = tile * slots;
   int stages = c.stages;
   if (stages == 0) stages = clamp_int((int)((unsigned long long)budget / (stage_bytes + 8)), 2, 8);
   const unsigned long long smem = (unsigned long long)stages * (stage_bytes + 8);
   if (smem > (unsigned long long)budget) return RR_ERR_UNSUPPORTED;
 
-  p->tile_elems = (int)(tile / (int)E);
+  p->tile_elems = (int)(tile / E);
   p->n_bulk = n_bulk;
   p->n_tiles = (n_bulk + p->tile_elems - 1) / p->tile_elems;
   p->stages = stages;
   p->slots = slots;
-  const unsigned long long cap = (unsigned long long)dev.sms * ctas;
+  const unsigned long long cap = (unsigned long long)sms * ctas;
   l->grid = (int)(p->n_tiles < cap ? p->n_tiles : cap);
   l->smem = (size_t)smem;
   l->ctas_per_sm = ctas;
   return RR_OK;
+}
+
+// Plan for the current device and fill the buffer pointers.
+rr_status plan(const Checked &ck, const void *const *in, void *const *out, const rr_launch_cfg *cfg,
+               const DeviceInfo &dev, rr::RingParams *p, rr::Launch *l) {
+  *p = rr::RingParams{};
+  for (int r = 0; r < ck.R; ++r) {
+    p->in[r] = in[r];
+    p->out[r] = out[r];
+  }
+  p->status = dev.status;
+  return plan_launch(ck, cfg, dev.sms, dev.smem_per_sm, dev.smem_optin, p, l);
+}
+
+void export_plan(const rr::RingParams &p, const rr::Launch &l, size_t E, rr_launch_cfg *chosen) {
+  chosen->path = l.path;
+  chosen->tile_bytes = l.path == RR_PATH_BULK ? p.tile_elems * (int)E : 0;
+  chosen->stages = l.path == RR_PATH_BULK ? p.stages : 0;
+  chosen->ctas_per_sm = l.ctas_per_sm;
+  chosen->threads = l.threads;
 }
 
 rr_status run(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
@@ -286,11 +320,26 @@ rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs,
   rr::Launch l;
   st = plan(ck, in_bufs, out_bufs, cfg, dev, &p, &l);
   if (st != RR_OK) return st;
-  chosen->path = l.path;
-  chosen->tile_bytes = l.path == RR_PATH_BULK ? p.tile_elems * (int)ck.E : 0;
-  chosen->stages = l.path == RR_PATH_BULK ? p.stages : 0;
-  chosen->ctas_per_sm = l.ctas_per_sm;
-  chosen->threads = l.threads;
+  export_plan(p, l, ck.E, chosen);
+  return RR_OK;
+}
+
+rr_status ring_plan_device(rr_op op, int R, size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
+                           int buffers_16b_aligned, int sm_count, int smem_per_sm, int smem_per_block_optin,
+                           const rr_launch_cfg *cfg, rr_launch_cfg *chosen, int *grid, size_t *smem_bytes) {
+  if (!chosen || !grid || !smem_bytes) return RR_ERR_INVALID_ARG;
+  Checked ck;
+  rr_status st = check_scalars(op, R, count, dtype, wire, group_size, cfg, &ck);
+  if (st != RR_OK) return st;
+  if (count == 0) return RR_ERR_INVALID_ARG;
+  ck.all_16b_aligned = buffers_16b_aligned != 0;
+  rr::RingParams p = rr::RingParams{};
+  rr::Launch l;
+  st = plan_launch(ck, cfg, sm_count, smem_per_sm, smem_per_block_optin, &p, &l);
+  if (st != RR_OK) return st;
+  export_plan(p, l, ck.E, chosen);
+  *grid = l.grid;
+  *smem_bytes = l.smem;
   return RR_OK;
 }
 

@@ -199,3 +199,73 @@ def test_package_never_imports_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 with open(os.path.join(dirpath, fn)) as f:
                     assert not pat.search(f.read()), fn
+
+
+# --------------------------------------------------------------------------
+# the launch planner, for a described GB300 (152 SMs, 228 KB / SM, 227 KB / CTA)
+# --------------------------------------------------------------------------
+
+GB300 = dict(sms=152, smem_per_sm=233472, optin=232448)
+
+
+def plan_dev(L, op, R, count, dtype, wire=None, group=0, aligned=1, cfg=None, dev=GB300):
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    chosen = rr.LaunchCfg()
+    grid = ctypes.c_int(0)
+    smem = ctypes.c_size_t(0)
+    L.ring_plan_device.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.POINTER(rr.LaunchCfg), ctypes.POINTER(rr.LaunchCfg),
+                                   ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]
+    L.ring_plan_device.restype = ctypes.c_int
+    st = L.ring_plan_device(op, R, count, dtype, dtype if wire is None else wire, group, aligned, dev["sms"],
+                            dev["smem_per_sm"], dev["optin"],
+                            ctypes.byref(rr.LaunchCfg(*cfg)) if cfg else None, ctypes.byref(chosen),
+                            ctypes.byref(grid), ctypes.byref(smem))
+    return st, chosen.as_dict(), grid.value, smem.value
+
+
+def test_planner_invariants_every_rank_count(L):
+    """Every plan keeps tiles on 16-byte multiples and within shared memory."""
+    counts = [1, 7, 8, 100, 4096, 65537, 524_288, 1_048_576, 8_388_608, 50_000_017, 268_435_456]
+    for R in range(1, 65):
+        for op in (AR, RS, AG):
+            for dtype, E in ((F32, 4), (F16, 2), (BF16, 2)):
+                for N in counts:
+                    for ctas in (0, 1, 2, 3, 4):
+                        cfg = (0, 0, 0, ctas, 0) if ctas else None
+                        st, ch, grid, smem = plan_dev(L, op, R, N, dtype, cfg=cfg)
+                        assert st == OK, (R, op, dtype, N, ctas, st)
+                        assert grid >= 1
+                        if ch["path"] == 1:
+                            slots = 1 if op == AG else R
+                            tile = ch["tile_bytes"]
+                            assert tile >= 16 and tile % 16 == 0 and tile % E == 0, (R, N, tile)
+                            assert 2 <= ch["stages"] <= 8
+                            assert smem == ch["stages"] * (tile * slots + 8)
+                            assert smem <= min(GB300["optin"], GB300["smem_per_sm"] // ch["ctas_per_sm"] - 1024)
+                            assert grid <= GB300["sms"] * ch["ctas_per_sm"]
+                            assert (N * E) // 16 > 0
+                            if op != AR:
+                                assert (N // R * E) % 16 == 0
+                        else:
+                            assert 64 <= ch["threads"] <= 1024
+
+
+def test_planner_paths(L):
+    # unaligned buffers or sub-16-byte messages take the simple path
+    assert plan_dev(L, AR, 8, 1 << 20, F16, aligned=0)[1]["path"] == 2
+    assert plan_dev(L, AR, 8, 7, F16)[1]["path"] == 2
+    assert plan_dev(L, AR, 8, 1 << 20, F16)[1]["path"] == 1
+    # ReduceScatter / AllGather need chunk boundaries on 16 bytes for the bulk path
+    assert plan_dev(L, RS, 8, 8 * 1001, F16)[1]["path"] == 2
+    assert plan_dev(L, RS, 8, 8 * 1024, F16)[1]["path"] == 1
+    assert plan_dev(L, AG, 8, 8 * 1024, F32)[1]["path"] == 1
+    # a forced bulk path the buffers do not allow is refused
+    assert plan_dev(L, RS, 8, 8 * 1001, F16, cfg=(1, 0, 0, 0, 0))[0] == EUNSUP
+    # a forced configuration that does not fit shared memory is refused
+    assert plan_dev(L, AR, 64, 1 << 20, F32, cfg=(1, 4096, 8, 1, 0))[0] == EUNSUP
+    # the two-level ring plans like the flat ring of all its ranks
+    st, ch, _, _ = plan_dev(L, AR, 16, 1 << 24, F32, group=8)
+    assert st == OK and ch["path"] == 1
