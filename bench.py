@@ -13,7 +13,10 @@ own full workload; the path has no exchange between GPUs).
 
 Also reported: the roofline of the kernel (2 R msg bytes per launch over its
 CUDA-event time against the measured HBM copy bandwidth), the sweep over 1,
-16, 128 and 512 MiB with an L2 flush before every timed launch, an end-to-end
+16, 128 and 512 MiB and a table of the other workloads (AllReduce /
+ReduceScatter / AllGather at R = 4, the bfloat16 wire, the two-level ring, a
+fusion bucket), each timed by CUDA-graph replay over rotating buffer sets of
+at least 3x the L2 size so no launch finds its inputs in L2, an end-to-end
 figure through the same C ABI with pinned host buffers (host-to-device copies
 of the inputs and device-to-host copies of all outputs inside the timed
 region), the CPU oracle's throughput on a bounded sample, and the SM clocks
@@ -189,6 +192,57 @@ def time_oracle(msg_mib, seed0=2000):
     return n * 2 / dt / 1e9, dt, n
 
 
+def graph_row(rr, wl, w, dev, l2_bytes, peak, launches):
+    """Time workload w: CUDA-graph replay of `launches` back-to-back calls over
+    rotating buffer sets (>= 3x L2 in total).  Returns one table row."""
+    import torch
+
+    op = {"allreduce": rr.OP_ALLREDUCE, "reduce_scatter": rr.OP_REDUCE_SCATTER, "allgather": rr.OP_ALLGATHER}[w.op]
+    E = torch.tensor([], dtype=w.dtype).element_size()
+    N, R_ = w.count, w.R
+    msg = N * E
+    lens = [rr.chunk_count(N, R_, c) for c in range(R_)]
+    in_lens = lens if op == rr.OP_ALLGATHER else [N] * R_
+    out_lens = lens if op == rr.OP_REDUCE_SCATTER else [N] * R_
+    set_bytes = (sum(in_lens) + sum(out_lens)) * E
+    nsets = max(1, min(16, -(-3 * l2_bytes // set_bytes)))
+    sets = []
+    for k in range(nsets):
+        ins = wl.inputs(w, dev, lengths=in_lens) if k == 0 else [t.clone() for t in sets[0][0]]
+        outs = [torch.empty(n, dtype=w.dtype, device=dev) for n in out_lens]
+        sets.append((ins, outs))
+    for ins, outs in sets:  # warm up outside capture
+        rr.collective(op, ins, outs, N, w.wire, w.group_size)
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for k in range(launches):
+                ins, outs = sets[k % nsets]
+                rr.collective(op, ins, outs, N, w.wire, w.group_size, s)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b) / launches)
+    t_ms = min(times)
+    alg = (2 * R_ if op == rr.OP_ALLREDUCE else R_ + 1) * msg
+    busbw = msg / t_ms / 1e6 * ((2 if op == rr.OP_ALLREDUCE else 1) * (R_ - 1) / R_)
+    row = {"workload": w.name, "op": w.op, "R": R_, "group_size": w.group_size or R_, "count": N,
+           "msg_bytes": msg, "ms": round(t_ms, 5), "algbw_gbs": round(msg / t_ms / 1e6, 2),
+           "busbw_gbs": round(busbw, 2), "hbm_gbs": round(alg / t_ms / 1e6, 1),
+           "roofline_frac": round(alg / t_ms / 1e6 / peak, 4), "buffer_sets": nsets,
+           "plan": rr.plan(op, sets[0][0], sets[0][1], N, w.wire, w.group_size)}
+    del g, sets
+    return row
+
+
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
@@ -273,40 +327,21 @@ def run_ours(args):
     traffic = recorded_traffic(digest)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
 
-    # sweep with an L2 flush before every timed launch
-    sweep = []
+    # the size sweep and the other workloads: CUDA-graph replay of back-to-back
+    # launches over rotating buffer sets at least 3x the L2 size, so every
+    # launch reads inputs that are not in L2 and no host time is included
+    sweep, table = [], []
     if not args.no_sweep:
-        flush = torch.empty(2 * l2_bytes // 4 + 1024, dtype=torch.float32, device=dev)
         del outs
-        for mib in SWEEP_MIB:
-            if mib == args.msg_mib:
-                sx, so = xs, [torch.empty_like(x) for x in xs]
-            else:
-                sw = wl.config2(mib)
-                sx = wl.inputs(sw, dev)
-                so = [torch.empty_like(x) for x in sx]
-            times = []
-            for it in range(args.sweep_iters + 2):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                rr.allreduce(sx, outs=so)
-                b.record(stream)
-                torch.cuda.synchronize(dev)
-                if it >= 2:
-                    times.append(a.elapsed_time(b))
-            t_ms = statistics.median(times)
-            m = sx[0].numel() * 2
-            sweep.append({"msg_mib": mib, "ms": round(t_ms, 5), "algbw_gbs": round(m / t_ms / 1e6, 2),
-                          "busbw_gbs": round(m / t_ms / 1e6 * 2 * (R - 1) / R, 2),
-                          "hbm_gbs": round(2 * R * m / t_ms / 1e6, 1),
-                          "roofline_frac": round(2 * R * m / t_ms / 1e6 / peak, 4),
-                          "plan": rr.plan(rr.OP_ALLREDUCE, sx, so, sx[0].numel())})
-            del so
-            if sx is not xs:
-                del sx
-        del flush
         torch.cuda.empty_cache()
+        for mib in SWEEP_MIB:
+            sweep.append(graph_row(rr, wl, wl.config2(mib), dev, l2_bytes, peak, args.sweep_iters))
+        torch.cuda.empty_cache()
+        if not args.no_workloads:
+            for w in (wl.config1("allreduce"), wl.config1("reduce_scatter"), wl.config1("allgather"), wl.config3(),
+                      wl.config4(), wl.config5(0)):
+                table.append(graph_row(rr, wl, w, dev, l2_bytes, peak, args.sweep_iters))
+                torch.cuda.empty_cache()
         outs = [torch.empty_like(x) for x in xs]
 
     # end to end through the same C ABI, with pinned host buffers
@@ -365,7 +400,7 @@ def run_ours(args):
                          "kernel_ms": round(kern_ms, 5), "algorithmic_bytes_per_launch": 2 * R * msg},
             "busbw_gbs": round(value / world * 2 * (R - 1) / R, 3),
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
-            "sweep": sweep, "kernel_sources": digest,
+            "sweep": sweep, "workloads": table, "kernel_sources": digest,
         }
         print(json.dumps(line), flush=True)
     if pg:
@@ -418,11 +453,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--msg-mib", type=int, default=MSG_MIB)
-    ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--sweep-iters", type=int, default=40)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-sample-mib", type=int, default=CPU_SAMPLE_MIB)
     ap.add_argument("--ref-sample-mib", type=int, default=REF_SAMPLE_MIB)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

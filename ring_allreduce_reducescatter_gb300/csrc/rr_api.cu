@@ -190,28 +190,49 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   }
 
   const int slots = ck.op == RR_OP_ALLGATHER ? 1 : ck.R;
-  const int ctas = c.ctas_per_sm ? c.ctas_per_sm : 2;
-  // shared memory of one CTA: its share of the SM, less 1 KB the runtime keeps per CTA
-  long long budget = (long long)smem_per_sm / ctas - 1024;
-  if (budget > smem_optin) budget = smem_optin;
-  if (budget < 64) return RR_ERR_UNSUPPORTED;
   const unsigned long long total_bytes = n_bulk * E;
+  // shared memory one CTA may use when `ctas` CTAs share an SM (the runtime keeps 1 KB per CTA)
+  auto budget_for = [&](int ctas) {
+    long long b = (long long)smem_per_sm / ctas - 1024;
+    return b > smem_optin ? (long long)smem_optin : b;
+  };
 
+  // Tile: 16 KB per stage across the slots, at least 2 KB per rank (smaller
+  // bulk copies lose bandwidth), shrunk only when two stages do not fit one CTA.
   unsigned long long tile = (unsigned long long)c.tile_bytes;
   if (tile == 0) {
-    tile = round16_down(32768 / slots);
-    if (tile < 512) tile = 512;
+    tile = round16_down(16384 / slots);
+    if (tile < 2048) tile = 2048;
     if (tile > 16384) tile = 16384;
-    // keep at least two tiles per CTA when the message is small
-    const unsigned long long want = 2ull * (unsigned long long)sms * ctas;
-    while (tile > 1024 && (total_bytes + tile - 1) / tile < want) tile = round16_down(tile / 2);
-    // keep two stages within the shared-memory budget
-    while (tile > 16 && 2ull * (tile * slots + 8) > (unsigned long long)budget) tile = round16_down(tile / 2);
+    const long long fit = budget_for(c.ctas_per_sm ? c.ctas_per_sm : 1);
+    while (tile > 16 && 2ull * (tile * slots + 8) > (unsigned long long)fit) tile = round16_down(tile / 2);
   }
   if (tile < 16 || tile % 16 != 0 || tile % E != 0) return RR_ERR_INVALID_ARG;
   const unsigned long long stage_bytes = tile * slots;
-  int stages = c.stages;
-  if (stages == 0) stages = clamp_int((int)((unsigned long long)budget / (stage_bytes + 8)), 2, 8);
+  const unsigned long long n_tiles = (total_bytes + tile - 1) / tile;
+
+  // CTAs per SM and stages.  Several independent CTA pipelines per SM keep
+  // more bulk copies in flight than one deep pipeline: prefer 3 CTAs of 3
+  // stages.  A message with at most 4 tiles per SM gets one CTA per tile.
+  int ctas = c.ctas_per_sm, stages = c.stages;
+  if (ctas == 0 && stages == 0 && n_tiles <= 4ull * (unsigned long long)sms) {
+    ctas = (int)((n_tiles + sms - 1) / sms);
+    if (ctas < 1) ctas = 1;
+    while (ctas > 1 && 2ull * (stage_bytes + 8) > (unsigned long long)budget_for(ctas)) --ctas;
+    stages = 2;
+  }
+  if (ctas == 0) {
+    const int want_stages = stages ? stages : 3;
+    ctas = 1;
+    for (int cand = 3; cand >= 1; --cand)
+      if ((unsigned long long)want_stages * (stage_bytes + 8) <= (unsigned long long)budget_for(cand)) {
+        ctas = cand;
+        break;
+      }
+  }
+  const long long budget = budget_for(ctas);
+  if (budget < 64) return RR_ERR_UNSUPPORTED;
+  if (stages == 0) stages = clamp_int((int)((unsigned long long)budget / (stage_bytes + 8)), 2, 3);
   const unsigned long long smem = (unsigned long long)stages * (stage_bytes + 8);
   if (smem > (unsigned long long)budget) return RR_ERR_UNSUPPORTED;
 
