@@ -17,9 +17,9 @@ CUDA-event time against the measured HBM copy bandwidth), the sweep over 1,
 ReduceScatter / AllGather at R = 4, the bfloat16 wire, the two-level ring, a
 fusion bucket), each timed by CUDA-graph replay over rotating buffer sets of
 at least 3x the L2 size so no launch finds its inputs in L2, an end-to-end
-figure through the same C ABI with pinned host buffers (host-to-device copies
-of the inputs and device-to-host copies of all outputs inside the timed
-region), the CPU oracle's throughput on a bounded sample, and the SM clocks
+figure through the C ABI's host-buffer entry point (ring_allreduce_host:
+page-locked inputs copied in and all R outputs copied back inside the timed
+region, pipelined in pieces), the CPU oracle's throughput on a bounded sample, and the SM clocks
 sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -344,20 +344,23 @@ def run_ours(args):
                 torch.cuda.empty_cache()
         outs = [torch.empty_like(x) for x in xs]
 
-    # end to end through the same C ABI, with pinned host buffers
+    # end to end through the C ABI's host-buffer entry point (ring_allreduce_host):
+    # inputs in page-locked host memory, every output copied back to the host,
+    # all inside the timed region; the copies of piece k+1 and k-1 overlap the
+    # fold of piece k
     e2e = None
     if not args.no_e2e:
+        del outs
+        torch.cuda.empty_cache()
         host_in = [torch.empty(N, dtype=torch.float16, pin_memory=True) for _ in range(R)]
         host_out = [torch.empty(N, dtype=torch.float16, pin_memory=True) for _ in range(R)]
         for r in range(R):
             host_in[r].copy_(xs[r])
+        piece = args.e2e_piece_mib * MIB // 2
+        ws = torch.empty(rr.host_workspace_bytes(R, piece, torch.float16), dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            for r in range(R):
-                xs[r].copy_(host_in[r], non_blocking=True)
-            rr.allreduce(xs, outs=outs)
-            for r in range(R):
-                host_out[r].copy_(outs[r], non_blocking=True)
+            rr.allreduce_host(host_in, host_outs=host_out, workspace=ws)
 
         for _ in range(2):
             e2e_step()
@@ -373,8 +376,10 @@ def run_ours(args):
         e_ms = combine_ranks(pg, [a.elapsed_time(b) / args.e2e_steps], dev)[0]
         e2e = {"value": round(job_throughput(world, msg, e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": R * msg, "d2h_bytes_per_step": R * msg, "ms_per_step": round(e_ms, 4),
-               "steps": args.e2e_steps}
-        del host_in, host_out
+               "steps": args.e2e_steps, "api": "ring_allreduce_host",
+               "piece_mib_per_rank": args.e2e_piece_mib}
+        del host_in, host_out, ws
+        outs = [torch.empty_like(x) for x in xs]
 
     if sampler:
         sampler.stop()
@@ -455,6 +460,7 @@ def main():
     ap.add_argument("--msg-mib", type=int, default=MSG_MIB)
     ap.add_argument("--sweep-iters", type=int, default=40)
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-piece-mib", type=int, default=32)
     ap.add_argument("--cpu-sample-mib", type=int, default=CPU_SAMPLE_MIB)
     ap.add_argument("--ref-sample-mib", type=int, default=REF_SAMPLE_MIB)
     ap.add_argument("--no-sweep", action="store_true")

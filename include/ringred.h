@@ -37,7 +37,9 @@
  *   - in_bufs and out_bufs are HOST arrays of R DEVICE pointers (current
  *     device).  The library reads the arrays during the call only.
  *   - The caller owns every buffer and the stream.  The library allocates no
- *     memory and keeps no pointer after the call returns.
+ *     memory and keeps no pointer after the call returns (ring_allreduce_host
+ *     creates two streams and ten events per device on first use and keeps
+ *     them until exit).
  *   - The call is asynchronous: it validates its arguments, enqueues work on
  *     `stream` and returns.  Errors of the enqueued work surface when the
  *     caller synchronizes the stream; a bounded wait inside a kernel that gave
@@ -149,6 +151,50 @@ typedef struct {
 rr_status ring_collective(rr_op op, const void *const *in_bufs, void *const *out_bufs, int R,
                           size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
                           const rr_launch_cfg *cfg, cudaStream_t stream);
+
+/*
+ * ring_allreduce_range -- elements [first, first + n) of the AllReduce of
+ * count-element rank vectors: the building block of a chunked AllReduce that
+ * overlaps compute (page bjdmk.com.cn/news/5966809, sections 4.2-4.3: the big
+ * tensor is cut into pieces and each piece is reduced on a communication
+ * stream as soon as it is ready).
+ * in_bufs[r], out_bufs[r]: n elements each, holding elements first .. first+n-1
+ * of rank r's vector (out_bufs[r] == in_bufs[r] allowed).  Every element is
+ * reduced exactly as ring_allreduce_ex would reduce it: its chunk (hence its
+ * start rank) comes from its global index in the count-element vector, so
+ * any split of [0, count) into ranges gives the same bits as one call.
+ * Requires first + n <= count.  group_size, wire and cfg as for
+ * ring_collective.
+ */
+rr_status ring_allreduce_range(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                               size_t first, size_t n, rr_dtype dtype, rr_dtype wire, int group_size,
+                               const rr_launch_cfg *cfg, cudaStream_t stream);
+
+/*
+ * ring_allreduce_host -- the AllReduce of vectors held in HOST memory
+ * (host_in[r], host_out[r]: `count` elements each; host_out[r] == host_in[r]
+ * allowed; page-locked memory lets the copies overlap).  The vectors stream
+ * through the caller's device workspace in pieces: while piece k is reduced
+ * on `stream`, piece k+1 is copied in and piece k-1 copied out on two
+ * internal streams (created once per device, with their events), the
+ * pipelining of page bjdmk.com.cn/news/5966809, section 4.3.
+ * dev_workspace: device memory, 16-byte aligned, workspace_bytes long, used
+ * by this call until `stream` reaches the point where the call returns; the
+ * piece length is the largest multiple of 256 elements whose three slots of R
+ * pieces fit (ring_allreduce_host_workspace gives the size for a piece
+ * length).  The result equals ring_allreduce_ex on device copies, bit for
+ * bit.  Work enqueued on `stream` after the call sees host_out complete.
+ * Calls from several host threads on one device are serialised.
+ * Errors: as above; RR_ERR_INVALID_ARG if the workspace cannot hold 256
+ * elements per slot; RR_ERR_ALIAS if it overlaps a host buffer.
+ */
+rr_status ring_allreduce_host(const void *const *host_in, void *const *host_out, int R, size_t count,
+                              rr_dtype dtype, rr_dtype wire, int group_size, void *dev_workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes ring_allreduce_host needs for pieces of piece_count
+ * elements (rounded up to 256); 0 for invalid arguments. */
+size_t ring_allreduce_host_workspace(int R, size_t piece_count, rr_dtype dtype);
 
 /*
  * ring_plan -- the launch configuration ring_collective would use for these

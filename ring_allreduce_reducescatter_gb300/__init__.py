@@ -16,6 +16,7 @@ import torch
 
 __all__ = [
     "RingError", "lib", "allreduce", "reduce_scatter", "allgather", "collective", "plan",
+    "allreduce_range", "allreduce_host", "host_workspace_bytes",
     "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
     "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE",
@@ -75,6 +76,12 @@ def lib() -> ctypes.CDLL:
                   "ring_reduce_scatter", "ring_reduce_scatter_ex", "ring_allgather",
                   "ring_device_status", "ring_selftest_bounded_wait"):
             getattr(L, f).restype = i
+        L.ring_allreduce_range.argtypes = [vpp, vpp, i, sz, sz, sz, i, i, i, ctypes.POINTER(LaunchCfg), vp]
+        L.ring_allreduce_range.restype = i
+        L.ring_allreduce_host.argtypes = [vpp, vpp, i, sz, i, i, i, vp, sz, vp]
+        L.ring_allreduce_host.restype = i
+        L.ring_allreduce_host_workspace.argtypes = [i, sz, i]
+        L.ring_allreduce_host_workspace.restype = sz
         L.ring_chunk_count.argtypes = [sz, i, i]
         L.ring_chunk_count.restype = sz
         L.ring_chunk_offset.argtypes = [sz, i, i]
@@ -201,6 +208,53 @@ def allgather(ins: Sequence[torch.Tensor], count: Optional[int] = None,
         outs = [torch.empty(count, dtype=ref.dtype, device=ref.device) for _ in ins]
     collective(OP_ALLGATHER, ins, list(outs), count, None, 0, stream, cfg)
     return outs
+
+
+def allreduce_range(ins, outs, count: int, first: int, wire=None, group_size: int = 0, stream=None,
+                    cfg: Optional[LaunchCfg] = None) -> None:
+    """ring_allreduce_range: ins[r] / outs[r] hold elements [first, first + n) of
+    rank r's count-element vector; outs receive those elements of the AllReduce."""
+    ins, outs = list(ins), list(outs)
+    dtype = ins[0].dtype
+    _check_tensors(ins, dtype, "ins")
+    _check_tensors(outs, dtype, "outs")
+    dt = _code(dtype)
+    wt = dt if wire is None else _code(wire)
+    st = lib().ring_allreduce_range(_ptr_array(ins), _ptr_array(outs), len(ins), count, first, ins[0].numel(), dt,
+                                    wt, group_size, ctypes.byref(cfg) if cfg is not None else None,
+                                    _stream_handle(stream))
+    if st != OK:
+        raise RingError(st, "ring_allreduce_range")
+
+
+def host_workspace_bytes(R: int, piece_count: int, dtype) -> int:
+    return int(lib().ring_allreduce_host_workspace(R, piece_count, _code(dtype)))
+
+
+def allreduce_host(host_ins, host_outs=None, workspace: Optional[torch.Tensor] = None, wire=None,
+                   group_size: int = 0, stream=None, piece_count: int = 1 << 24):
+    """ring_allreduce_host: CPU tensors in and out (page-locked for overlap),
+    pipelined through a device workspace (allocated here if not given)."""
+    host_ins = list(host_ins)
+    dtype = host_ins[0].dtype
+    for t in host_ins:
+        if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != dtype:
+            raise ValueError("host_ins: contiguous CPU tensors of one dtype")
+    if host_outs is None:
+        host_outs = [torch.empty_like(t, pin_memory=t.is_pinned()) for t in host_ins]
+    R, N = len(host_ins), host_ins[0].numel()
+    if workspace is None:
+        nbytes = host_workspace_bytes(R, min(piece_count, max(N, 1)), dtype)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=torch.cuda.current_device())
+    dt = _code(dtype)
+    wt = dt if wire is None else _code(wire)
+    hin = (ctypes.c_void_p * R)(*[t.data_ptr() for t in host_ins])
+    hout = (ctypes.c_void_p * R)(*[t.data_ptr() for t in host_outs])
+    st = lib().ring_allreduce_host(hin, hout, R, N, dt, wt, group_size, workspace.data_ptr(), workspace.numel(),
+                                   _stream_handle(stream))
+    if st != OK:
+        raise RingError(st, "ring_allreduce_host")
+    return host_outs
 
 
 def device_status() -> int:

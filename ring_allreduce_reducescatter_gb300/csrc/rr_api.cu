@@ -66,7 +66,9 @@ struct Buf {
 // Everything that can be checked without the device.
 struct Checked {
   int op, R, L, dtype, wire;
-  size_t count;
+  size_t count;  // N, elements of the whole rank vector
+  size_t first;  // AllReduce ranges: the buffers hold elements [first, first + n)
+  size_t n;
   size_t E;
   bool all_16b_aligned;
 };
@@ -97,26 +99,37 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
   ck->dtype = dtype;
   ck->wire = wire;
   ck->count = count;
+  ck->first = 0;
+  ck->n = count;
   ck->E = elem_bytes(dtype);
   ck->all_16b_aligned = true;
   if (count > (SIZE_MAX / 4) / ck->E) return RR_ERR_INVALID_ARG;
   return RR_OK;
 }
 
+// Buffer checks: sizes, NULL, element alignment, address wrap, aliasing.
+rr_status check_buffers(const void *const *in, void *const *out, Checked *ck);
+
 rr_status check_args(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
                      int group_size, const rr_launch_cfg *cfg, Checked *ck) {
   rr_status st = check_scalars(op, R, count, dtype, wire, group_size, cfg, ck);
   if (st != RR_OK) return st;
+  return check_buffers(in, out, ck);
+}
+
+rr_status check_buffers(const void *const *in, void *const *out, Checked *ck) {
   if (!in || !out) return RR_ERR_INVALID_ARG;
-  if (count == 0) return RR_OK;
+  if (ck->n == 0) return RR_OK;
   const size_t E = ck->E;
+  const int R = ck->R, op = ck->op;
+  const size_t count = ck->count;
 
   // sizes, pointers, alignment
   Buf bufs[2 * RR_MAX_RANKS];
   int nb = 0;
   for (int r = 0; r < R; ++r) {
-    const size_t n_in = (op == RR_OP_ALLGATHER) ? chunk_len(count, R, r) : count;
-    const size_t n_out = (op == RR_OP_REDUCE_SCATTER) ? chunk_len(count, R, r) : count;
+    const size_t n_in = (op == RR_OP_ALLGATHER) ? chunk_len(count, R, r) : ck->n;
+    const size_t n_out = (op == RR_OP_REDUCE_SCATTER) ? chunk_len(count, R, r) : ck->n;
     for (int side = 0; side < 2; ++side) {
       const void *ptr = side == 0 ? in[r] : out[r];
       const size_t bytes = (side == 0 ? n_in : n_out) * E;
@@ -155,14 +168,16 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   const rr_launch_cfg zero = {0, 0, 0, 0, 0};
   const rr_launch_cfg &c = cfg ? *cfg : zero;
   const size_t E = ck.E;
-  const unsigned long long N = ck.count;
+  const unsigned long long N = ck.n;  // elements of this launch
   if (sms < 1 || smem_per_sm < 1 || smem_optin < 1) return RR_ERR_INVALID_ARG;
 
   p->count = N;
+  p->first = ck.first;
+  p->total = ck.count;
   p->R = ck.R;
   p->L = ck.L;
   p->G = ck.R / ck.L;
-  p->base = N / (unsigned long long)ck.L;
+  p->base = (unsigned long long)ck.count / (unsigned long long)ck.L;
 
   // bulk path: 16-byte aligned buffers, and for ReduceScatter / AllGather
   // chunk boundaries on 16-byte multiples (segments are copied per chunk)
@@ -268,26 +283,138 @@ void export_plan(const rr::RingParams &p, const rr::Launch &l, size_t E, rr_laun
   chosen->threads = l.threads;
 }
 
-rr_status run(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
-              int group_size, const rr_launch_cfg *cfg, cudaStream_t stream) {
-  Checked ck;
-  rr_status st = check_args(op, in, out, R, count, dtype, wire, group_size, cfg, &ck);
-  if (st != RR_OK || count == 0) return st;
+// Plan and launch a validated collective on the current device.
+rr_status launch_checked(const Checked &ck, const void *const *in, void *const *out, const rr_launch_cfg *cfg,
+                         cudaStream_t stream) {
   DeviceInfo dev;
-  st = current_device(&dev);
+  rr_status st = current_device(&dev);
   if (st != RR_OK) return st;
   rr::RingParams p;
   rr::Launch l;
   st = plan(ck, in, out, cfg, dev, &p, &l);
   if (st != RR_OK) return st;
   cudaError_t e;
-  if (dtype == RR_FP32)
-    e = rr::launch_f32(op, wire, p, l, stream);
-  else if (dtype == RR_FP16)
-    e = rr::launch_f16(op, wire, p, l, stream);
+  if (ck.dtype == RR_FP32)
+    e = rr::launch_f32(ck.op, ck.wire, p, l, stream);
+  else if (ck.dtype == RR_FP16)
+    e = rr::launch_f16(ck.op, ck.wire, p, l, stream);
   else
-    e = rr::launch_bf16(op, wire, p, l, stream);
+    e = rr::launch_bf16(ck.op, ck.wire, p, l, stream);
   return e == cudaSuccess ? RR_OK : RR_ERR_CUDA;
+}
+
+rr_status run(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
+              int group_size, const rr_launch_cfg *cfg, cudaStream_t stream) {
+  Checked ck;
+  rr_status st = check_args(op, in, out, R, count, dtype, wire, group_size, cfg, &ck);
+  if (st != RR_OK || count == 0) return st;
+  return launch_checked(ck, in, out, cfg, stream);
+}
+
+// --------------------------------------------------------------------------
+// AllReduce of host buffers through a device workspace, pipelined in pieces
+// --------------------------------------------------------------------------
+
+constexpr int kHostSlots = 3;           // workspace slots: copy-in, fold, copy-out overlap
+constexpr size_t kPieceAlign = 256;     // piece length granularity (elements)
+
+struct Pipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t copied_in[kHostSlots] = {}, folded[kHostSlots] = {}, copied_out[kHostSlots] = {};
+  bool valid = false;
+  std::mutex mu;
+};
+Pipe g_pipes[kMaxDevices];
+
+rr_status pipe_for_current_device(Pipe **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
+  Pipe &pp = g_pipes[dev];
+  std::lock_guard<std::mutex> lock(g_devices_mu);
+  if (!pp.valid) {
+    if (cudaStreamCreateWithFlags(&pp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&pp.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&pp.start, cudaEventDisableTiming) != cudaSuccess)
+      return RR_ERR_CUDA;
+    for (int k = 0; k < kHostSlots; ++k)
+      if (cudaEventCreateWithFlags(&pp.copied_in[k], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&pp.folded[k], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&pp.copied_out[k], cudaEventDisableTiming) != cudaSuccess)
+        return RR_ERR_CUDA;
+    pp.valid = true;
+  }
+  *out = &pp;
+  return RR_OK;
+}
+
+rr_status host_pipeline(const void *const *host_in, void *const *host_out, int R, size_t count, int dtype, int wire,
+                        int group_size, void *ws, size_t ws_bytes, cudaStream_t stream) {
+  Checked ck;
+  rr_status st = check_scalars(RR_OP_ALLREDUCE, R, count, dtype, wire, group_size, nullptr, &ck);
+  if (st != RR_OK) return st;
+  st = check_buffers(host_in, host_out, &ck);  // the host buffers: sizes, NULL, aliasing
+  if (st != RR_OK || count == 0) return st;
+  const size_t E = ck.E;
+  const uintptr_t wsa = reinterpret_cast<uintptr_t>(ws);
+  if (!ws || wsa % 16 != 0) return RR_ERR_INVALID_ARG;
+  size_t piece = ws_bytes / ((size_t)kHostSlots * R * E) / kPieceAlign * kPieceAlign;
+  if (piece == 0) return RR_ERR_INVALID_ARG;
+  if (piece > count) piece = (count + kPieceAlign - 1) / kPieceAlign * kPieceAlign;
+  const size_t slot_bytes = (size_t)R * piece * E;
+  // the workspace must not overlap the host buffers (they may be device-visible)
+  for (int r = 0; r < R; ++r) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(host_in[r]), b = reinterpret_cast<uintptr_t>(host_out[r]);
+    const uintptr_t lo = wsa, hi = wsa + (size_t)kHostSlots * slot_bytes;
+    if ((a < hi && lo < a + count * E) || (b < hi && lo < b + count * E)) return RR_ERR_ALIAS;
+  }
+
+  Pipe *pp = nullptr;
+  st = pipe_for_current_device(&pp);
+  if (st != RR_OK) return st;
+  std::lock_guard<std::mutex> lock(pp->mu);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // the copies start after the work already enqueued on `stream`
+  if (!ok(cudaEventRecord(pp->start, stream)) || !ok(cudaStreamWaitEvent(pp->h2d, pp->start, 0))) return RR_ERR_CUDA;
+  const size_t pieces = (count + piece - 1) / piece;
+  for (size_t k = 0; k < pieces; ++k) {
+    const int sl = (int)(k % kHostSlots);
+    const size_t first = k * piece, n = (count - first < piece) ? count - first : piece;
+    unsigned char *slot = static_cast<unsigned char *>(ws) + (size_t)sl * slot_bytes;
+    const void *dev_in[RR_MAX_RANKS];
+    void *dev_out[RR_MAX_RANKS];
+    // copy in once the slot's previous copy-out has finished
+    if (!ok(cudaStreamWaitEvent(pp->h2d, pp->copied_out[sl], 0))) return RR_ERR_CUDA;
+    for (int r = 0; r < R; ++r) {
+      unsigned char *d = slot + (size_t)r * piece * E;
+      dev_in[r] = d;
+      dev_out[r] = d;
+      if (!ok(cudaMemcpyAsync(d, static_cast<const unsigned char *>(host_in[r]) + first * E, n * E,
+                              cudaMemcpyHostToDevice, pp->h2d)))
+        return RR_ERR_CUDA;
+    }
+    if (!ok(cudaEventRecord(pp->copied_in[sl], pp->h2d)) || !ok(cudaStreamWaitEvent(stream, pp->copied_in[sl], 0)))
+      return RR_ERR_CUDA;
+    // fold the piece in place: elements [first, first + n) of the count-element AllReduce
+    Checked pk = ck;
+    pk.first = first;
+    pk.n = n;
+    pk.all_16b_aligned = true;  // slot buffers start on 512-byte multiples of a 16-byte aligned workspace
+    st = launch_checked(pk, dev_in, dev_out, nullptr, stream);
+    if (st != RR_OK) return st;
+    if (!ok(cudaEventRecord(pp->folded[sl], stream)) || !ok(cudaStreamWaitEvent(pp->d2h, pp->folded[sl], 0)))
+      return RR_ERR_CUDA;
+    for (int r = 0; r < R; ++r)
+      if (!ok(cudaMemcpyAsync(static_cast<unsigned char *>(host_out[r]) + first * E, slot + (size_t)r * piece * E,
+                              n * E, cudaMemcpyDeviceToHost, pp->d2h)))
+        return RR_ERR_CUDA;
+    if (!ok(cudaEventRecord(pp->copied_out[sl], pp->d2h))) return RR_ERR_CUDA;
+  }
+  // work enqueued on `stream` after this call sees every output copied
+  const int used = pieces < (size_t)kHostSlots ? (int)pieces : kHostSlots;
+  for (int sl = 0; sl < used; ++sl)
+    if (!ok(cudaStreamWaitEvent(stream, pp->copied_out[sl], 0))) return RR_ERR_CUDA;
+  return RR_OK;
 }
 
 }  // namespace
@@ -419,5 +546,31 @@ rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t s
 }
 
 int ring_abi_version(void) { return RR_ABI_VERSION; }
+
+rr_status ring_allreduce_range(const void *const *in_bufs, void *const *out_bufs, int R, size_t count, size_t first,
+                               size_t n, rr_dtype dtype, rr_dtype wire, int group_size, const rr_launch_cfg *cfg,
+                               cudaStream_t stream) {
+  Checked ck;
+  rr_status st = check_scalars(RR_OP_ALLREDUCE, R, count, dtype, wire, group_size, cfg, &ck);
+  if (st != RR_OK) return st;
+  if (first > count || n > count - first) return RR_ERR_INVALID_ARG;
+  ck.first = first;
+  ck.n = n;
+  st = check_buffers(in_bufs, out_bufs, &ck);
+  if (st != RR_OK || n == 0) return st;
+  return launch_checked(ck, in_bufs, out_bufs, cfg, stream);
+}
+
+size_t ring_allreduce_host_workspace(int R, size_t piece_count, rr_dtype dtype) {
+  if (R < 1 || R > RR_MAX_RANKS || !valid_type(dtype) || piece_count == 0) return 0;
+  const size_t piece = (piece_count + kPieceAlign - 1) / kPieceAlign * kPieceAlign;
+  return (size_t)kHostSlots * (size_t)R * piece * elem_bytes(dtype);
+}
+
+rr_status ring_allreduce_host(const void *const *host_in, void *const *host_out, int R, size_t count,
+                              rr_dtype dtype, rr_dtype wire, int group_size, void *dev_workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, dev_workspace, workspace_bytes, stream);
+}
 
 }  // extern "C"

@@ -62,10 +62,11 @@ __device__ __forceinline__ typename Fmt<DT>::type fold_elem_global(const RingPar
 }
 
 // The whole collective at element i (every input read, then every output written).
+// i is the buffers' (local) index; its chunk is that of the global index first + i.
 template <int OP, int DT, int WT>
 __device__ __forceinline__ void element_op(const RingParams &p, unsigned long long i) {
   using S = typename Fmt<DT>::type;
-  const int c = chunk_of(i, p.base, p.L);
+  const int c = chunk_of(p.first + i, p.base, p.L);
   if (OP == kOpAllReduce) {
     const S v = fold_elem_global<DT, WT>(p, i, c);
     for (int r = 0; r < p.R; ++r) static_cast<S *>(p.out[r])[i] = v;
@@ -111,7 +112,7 @@ __device__ __forceinline__ uint4 fold_vec_smem(const unsigned char *stage, uint3
   return VT::out(total);
 }
 
-// 16 bytes that straddle a chunk boundary: element by element.
+// 16 bytes that straddle a chunk boundary, element by element (i0: global index).
 template <int DT, int WT>
 __device__ __noinline__ uint4 fold_ragged_smem(const RingParams &p, const unsigned char *stage, uint32_t slot_bytes,
                                                unsigned long long i0, uint32_t off) {
@@ -159,12 +160,13 @@ __device__ __forceinline__ void compute_tile(const RingParams &p, unsigned char 
   const unsigned long long t0 = tile_begin(p, t), t1 = tile_end(p, t);
   const uint32_t nvec = (uint32_t)((t1 - t0) / V);
   const int L = p.L, G = p.G;
-  const int c_first = chunk_of(t0, p.base, L), c_last = chunk_of(t1 - 1, p.base, L);
+  const unsigned long long g0 = p.first + t0;  // global index of the tile's first element
+  const int c_first = chunk_of(g0, p.base, L), c_last = chunk_of(g0 + (t1 - t0) - 1, p.base, L);
   for (uint32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
     const uint32_t off = v * 16u;
     int c = c_first, c1 = c_last;
     if (c != c1) {
-      const unsigned long long i0 = t0 + (unsigned long long)v * V;
+      const unsigned long long i0 = g0 + (unsigned long long)v * V;
       c = chunk_of(i0, p.base, L);
       c1 = chunk_of(i0 + V - 1, p.base, L);
     }
@@ -172,7 +174,7 @@ __device__ __forceinline__ void compute_tile(const RingParams &p, unsigned char 
     if (c == c1)
       res = fold_vec_smem<VT>(stage, slot_bytes, L, G, c, off);
     else
-      res = fold_ragged_smem<DT, WT>(p, stage, slot_bytes, t0 + (unsigned long long)v * V, off);
+      res = fold_ragged_smem<DT, WT>(p, stage, slot_bytes, g0 + (unsigned long long)v * V, off);
     *reinterpret_cast<uint4 *>(stage + off) = res;
   }
 }
@@ -195,7 +197,7 @@ __device__ __forceinline__ void issue_loads(const RingParams &p, unsigned char *
     const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
     for (int c = c_lo; c <= c_hi; ++c) {
       const unsigned long long off = (unsigned long long)c * p.base;
-      const unsigned long long end = chunk_end(c, p.base, p.L, p.count);
+      const unsigned long long end = chunk_end(c, p.base, p.L, p.total);
       const unsigned long long s0 = t0 > off ? t0 : off, s1 = t1 < end ? t1 : end;
       if (s1 > s0)
         bulk_load(stage + (s0 - t0) * E, static_cast<const unsigned char *>(p.in[c]) + (s0 - off) * E,
@@ -218,7 +220,7 @@ __device__ __forceinline__ void issue_stores(const RingParams &p, const unsigned
     const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
     for (int c = c_lo; c <= c_hi; ++c) {
       const unsigned long long off = (unsigned long long)c * p.base;
-      const unsigned long long end = chunk_end(c, p.base, p.L, p.count);
+      const unsigned long long end = chunk_end(c, p.base, p.L, p.total);
       const unsigned long long s0 = t0 > off ? t0 : off, s1 = t1 < end ? t1 : end;
       if (s1 > s0)
         bulk_store(static_cast<unsigned char *>(p.out[c]) + (s0 - off) * E, stage + (s0 - t0) * E,

@@ -23,7 +23,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 struct RingParams {
   const void *in[RR_MAX_RANKS];
   void *out[RR_MAX_RANKS];
-  unsigned long long count;       // N, elements per rank vector
+  unsigned long long count;       // elements this launch covers (per rank)
+  unsigned long long first;       // global index of element 0 of the buffers (AllReduce ranges)
+  unsigned long long total;       // N, elements of the whole rank vector (the chunk table's N)
   unsigned long long base;        // floor(N / L): length of every chunk but the last
   unsigned long long n_bulk;      // bulk path: elements [0, n_bulk) go through tiles
   unsigned long long n_tiles;     // bulk path: ceil(n_bulk / tile_elems)

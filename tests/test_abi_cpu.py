@@ -269,3 +269,58 @@ def test_planner_paths(L):
     # the two-level ring plans like the flat ring of all its ranks
     st, ch, _, _ = plan_dev(L, AR, 16, 1 << 24, F32, group=8)
     assert st == OK and ch["path"] == 1
+
+
+# --------------------------------------------------------------------------
+# ranges and the host-buffer pipeline: argument checks
+# --------------------------------------------------------------------------
+
+def call_range(L, ins, outs, R, count, first, n, dtype, wire=None, group=0):
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    rr.lib()
+    return L.ring_allreduce_range(ptrs(ins), ptrs(outs), R, count, first, n, dtype,
+                                  dtype if wire is None else wire, group, None, None)
+
+
+def test_range_arguments(L):
+    ins, outs = fake(4, 100, 4)
+    assert call_range(L, ins, outs, 4, 100, 90, 11, F32) == EINVAL   # past the end
+    assert call_range(L, ins, outs, 4, 100, 101, 0, F32) == EINVAL
+    assert call_range(L, ins, outs, 4, 100, 100, 0, F32) == OK       # empty range at the end
+    assert call_range(L, ins, outs, 4, 100, 0, 0, F32) == OK
+    assert call_range(L, ins, outs, 0, 100, 0, 10, F32) == EINVAL
+    assert call_range(L, ins, outs, 4, 100, 0, 10, F16, F32) == EUNSUP
+    assert call_range(L, ins, outs, 4, 100, 0, 10, F32, group=3) == EINVAL
+    assert call_range(L, ins, [ins[1]] + outs[1:], 4, 100, 0, 10, F32) == EALIAS
+    assert call_range(L, ins, list(ins), 4, 100, 50, 10, F32) not in (EINVAL, EALIAS, EUNSUP)
+
+
+def call_host(L, hin, hout, R, count, dtype, ws, ws_bytes, wire=None, group=0):
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    rr.lib()
+    return L.ring_allreduce_host(ptrs(hin), ptrs(hout), R, count, dtype, dtype if wire is None else wire, group,
+                                 ws, ws_bytes, None)
+
+
+def test_host_pipeline_arguments(L):
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    rr.lib()
+    R, N = 4, 10_000
+    hin, hout = fake(R, N, 4)
+    ws = BASE + (1 << 40)
+    need = L.ring_allreduce_host_workspace(R, 256, F32)
+    assert need == 3 * R * 256 * 4
+    assert L.ring_allreduce_host_workspace(R, 1, F16) == 3 * R * 256 * 2
+    assert L.ring_allreduce_host_workspace(0, 256, F32) == 0
+    assert L.ring_allreduce_host_workspace(R, 0, F32) == 0
+    assert call_host(L, hin, hout, R, N, F32, None, need) == EINVAL          # no workspace
+    assert call_host(L, hin, hout, R, N, F32, ws + 8, need) == EINVAL        # not 16-byte aligned
+    assert call_host(L, hin, hout, R, N, F32, ws, need - 1) == EINVAL        # no room for 256 elements
+    assert call_host(L, hin, hout, R, N, F32, hin[2] + 64, need) == EALIAS   # overlaps a host buffer
+    assert call_host(L, hin, [hin[1]] + hout[1:], R, N, F32, ws, need) == EALIAS   # output 0 on input 1
+    assert call_host(L, hin, hout, R, N, F16, ws, need, wire=F32) == EUNSUP
+    assert call_host(L, hin, hout, R, 0, F32, ws, need) == OK                # nothing to do
+    assert call_host(L, hin, list(hin), R, N, F32, ws, need) not in (EINVAL, EALIAS, EUNSUP)  # in place

@@ -357,3 +357,88 @@ def test_workload5_bucket_sampled(rr, wl, bucket):
     check_sampled(rr, xs, outs, what=f"workload 5 bucket {bucket}")
     del outs, xs
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------
+# ranges (chunked AllReduce) and the host-buffer pipeline
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,wire,R,L", [(torch.float16, None, 8, 0), (torch.float32, "bf16", 8, 0),
+                                            (torch.float32, None, 16, 8), (torch.bfloat16, None, 3, 0),
+                                            (torch.float32, "f16", 5, 0)])
+def test_ranges_concatenate_to_the_allreduce(rr, dtype, wire, R, L):
+    N = 200_003
+    xs = gen(R, N, dtype, 41 + R)
+    Lc = L or R
+    base = N // Lc
+    rng = np.random.default_rng(R)
+    # split points: chunk boundaries and their neighbours, 16-byte multiples, odd places
+    cuts = {0, N, 1, N - 1, 4096, 65536, 12_345}
+    for c in range(1, Lc):
+        cuts |= {c * base - 1, c * base, c * base + 3}
+    cuts |= set(int(v) for v in rng.integers(0, N, 12))
+    cuts = sorted(v for v in cuts if 0 <= v <= N)
+    outs = [torch.full_like(x, 0) for x in xs]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        if b > a:
+            rr.allreduce_range([x[a:b] for x in xs], [o[a:b] for o in outs], N, a, wire, L)
+    torch.cuda.synchronize()
+    ref = oracle.allreduce([host(x) for x in xs], NAME[dtype], wire, L)
+    for r in range(R):
+        assert_same(host(outs[r]), ref.outs[r], f"ranges {NAME[dtype]}/{wire} R={R} L={L} rank {r}")
+    # in place, a range at a time
+    ys = [x.clone() for x in xs]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        if b > a:
+            rr.allreduce_range([y[a:b] for y in ys], [y[a:b] for y in ys], N, a, wire, L)
+    torch.cuda.synchronize()
+    for r in range(R):
+        assert_same(host(ys[r]), ref.outs[r], f"ranges in place rank {r}")
+
+
+@pytest.mark.parametrize("dtype,wire,R,L,N,piece", [
+    (torch.float16, None, 8, 0, 1_000_003, 4096),      # 245 pieces, ragged last piece
+    (torch.float32, "bf16", 8, 0, 300_001, 65536),
+    (torch.float32, None, 16, 8, 100_000, 1000),       # piece rounds up to 1024
+    (torch.bfloat16, None, 4, 0, 4_097, 1 << 20),      # one piece
+    (torch.float32, None, 1, 0, 12_345, 256),
+])
+def test_host_pipeline_parity(rr, dtype, wire, R, L, N, piece):
+    g = torch.Generator()
+    g.manual_seed(N + R)
+    for pinned in (True, False):
+        hin = [torch.randn(N, generator=g).to(dtype) for _ in range(R)]
+        if pinned:
+            hin = [t.pin_memory() for t in hin]
+        ws = torch.empty(rr.host_workspace_bytes(R, piece, dtype), dtype=torch.uint8, device="cuda")
+        hout = rr.allreduce_host(hin, workspace=ws, wire=wire, group_size=L)
+        torch.cuda.current_stream().synchronize()
+        ref = oracle.allreduce([host(t) for t in hin], NAME[dtype], wire, L)
+        for r in range(R):
+            assert_same(host(hout[r]), ref.outs[r], f"host pipeline pinned={pinned} rank {r}")
+        # a second call on the same workspace, in place on the host buffers
+        hin2 = [t * 0.5 for t in hin]
+        ref2 = oracle.allreduce([host(t) for t in hin2], NAME[dtype], wire, L)
+        if pinned:
+            hin2 = [t.pin_memory() for t in hin2]
+        rr.allreduce_host(hin2, host_outs=hin2, workspace=ws, wire=wire, group_size=L)
+        torch.cuda.current_stream().synchronize()
+        for r in range(R):
+            assert_same(host(hin2[r]), ref2.outs[r], f"host pipeline second call rank {r}")
+
+
+def test_host_pipeline_orders_after_prior_stream_work(rr):
+    # the copies must wait for work already enqueued on the stream (here: a
+    # device-to-host copy that fills the host inputs)
+    R, N = 4, 1 << 20
+    dev_src = gen(R, N, torch.float32, 5)
+    hin = [torch.empty(N, dtype=torch.float32).pin_memory() for _ in range(R)]
+    s = torch.cuda.current_stream()
+    torch.cuda._sleep(20_000_000)  # keep the stream busy so the copies below are still queued
+    for r in range(R):
+        hin[r].copy_(dev_src[r], non_blocking=True)
+    hout = rr.allreduce_host(hin, piece_count=65536)
+    s.synchronize()
+    ref = oracle.allreduce([host(x) for x in dev_src], "f32")
+    for r in range(R):
+        assert_same(host(hout[r]), ref.outs[r], f"ordered host pipeline rank {r}")
