@@ -196,6 +196,39 @@ rr_status ring_allreduce_host(const void *const *host_in, void *const *host_out,
  * elements (rounded up to 256); 0 for invalid arguments. */
 size_t ring_allreduce_host_workspace(int R, size_t piece_count, rr_dtype dtype);
 
+/* Size of the staging array that ring_allreduce_host_static uses instead of a
+ * caller workspace: 32 MiB, held on every GPU that loads the library until the
+ * process exits. */
+#define RR_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * ring_allreduce_host_static -- ring_allreduce_host without a workspace
+ * argument, for callers that cannot hand the library device memory: plugin
+ * code whose host program's allocator owns all device memory and offers no
+ * raw buffer, or a path that must not risk an allocation failing or blocking
+ * at run time.  The pages have no counterpart; it exists for such callers.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  The pieces go through RR_STATIC_SCRATCH_BYTES of device memory
+ * compiled into the library.  The first call on a device looks up that
+ * memory's device address (cudaGetSymbolAddress, with the device current) and
+ * creates the two internal streams and ten events of the pipelined copies;
+ * make that first call before any stream capture.
+ * host_in, host_out, R, count, dtype, wire, group_size, stream: as for
+ * ring_allreduce_host, with the same result bit for bit.  piece_count:
+ * elements per rank per piece, rounded up to 256; 0 picks the largest that
+ * fits.  A piece whose three slots of R pieces would exceed
+ * RR_STATIC_SCRATCH_BYTES is rejected with RR_ERR_INVALID_ARG before any CUDA
+ * call; the message length itself is not limited.
+ * Every call on a device shares the one array and leaves its last contents in
+ * it; nothing in it needs to start at zero, since a slot is always filled
+ * before it is read.  The library chains its own calls through per-device
+ * events and a lock so their pieces take turns in the array; GPU work that
+ * overlapped one of these calls while using the array would race with it.
+ */
+rr_status ring_allreduce_host_static(const void *const *host_in, void *const *host_out, int R, size_t count,
+                                     rr_dtype dtype, rr_dtype wire, int group_size, size_t piece_count,
+                                     cudaStream_t stream);
+
 /*
  * ring_plan -- the launch configuration ring_collective would use for these
  * arguments (after validation; nothing is enqueued).  *chosen receives the

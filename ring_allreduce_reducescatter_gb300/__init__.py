@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "RingError", "lib", "allreduce", "reduce_scatter", "allgather", "collective", "plan",
-    "allreduce_range", "allreduce_host", "host_workspace_bytes",
+    "allreduce_range", "allreduce_host", "allreduce_host_static", "host_workspace_bytes",
     "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
     "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE",
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.ring_allreduce_range.restype = i
         L.ring_allreduce_host.argtypes = [vpp, vpp, i, sz, i, i, i, vp, sz, vp]
         L.ring_allreduce_host.restype = i
+        L.ring_allreduce_host_static.argtypes = [vpp, vpp, i, sz, i, i, i, sz, vp]
+        L.ring_allreduce_host_static.restype = i
         L.ring_allreduce_host_workspace.argtypes = [i, sz, i]
         L.ring_allreduce_host_workspace.restype = sz
         L.ring_chunk_count.argtypes = [sz, i, i]
@@ -255,6 +257,27 @@ def allreduce_host(host_ins, host_outs=None, workspace: Optional[torch.Tensor] =
     if st != OK:
         raise RingError(st, "ring_allreduce_host")
     return host_outs
+
+
+def allreduce_host_static(host_ins, host_outs, wire=None, group_size: int = 0, piece_count: int = 0,
+                          stream=None) -> None:
+    """ring_allreduce_host_static: like allreduce_host, but the pieces go through
+    staging memory built into the library, so nothing is allocated (host_outs
+    must be given; it may be host_ins for in place)."""
+    host_ins, host_outs = list(host_ins), list(host_outs)
+    dtype = host_ins[0].dtype
+    for t in host_ins + host_outs:
+        if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != dtype:
+            raise ValueError("host buffers: contiguous CPU tensors of one dtype")
+    R, N = len(host_ins), host_ins[0].numel()
+    dt = _code(dtype)
+    wt = dt if wire is None else _code(wire)
+    hin = (ctypes.c_void_p * R)(*[t.data_ptr() for t in host_ins])
+    hout = (ctypes.c_void_p * R)(*[t.data_ptr() for t in host_outs])
+    st = lib().ring_allreduce_host_static(hin, hout, R, N, dt, wt, group_size, piece_count,
+                                          _stream_handle(stream))
+    if st != OK:
+        raise RingError(st, "ring_allreduce_host_static")
 
 
 def device_status() -> int:

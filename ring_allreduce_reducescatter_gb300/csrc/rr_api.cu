@@ -417,6 +417,32 @@ rr_status host_pipeline(const void *const *host_in, void *const *host_out, int R
   return RR_OK;
 }
 
+// --------------------------------------------------------------------------
+// Staging memory for callers that cannot allocate: a fixed array in the
+// library's own device image.  Host code only ever holds its address as
+// returned by cudaGetSymbolAddress for the current device; the symbol itself
+// is a host-side stand-in, not a device address.
+// --------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_rr_static_scratch[RR_STATIC_SCRATCH_BYTES];
+
+unsigned char *g_static_scratch_addr[kMaxDevices];
+std::mutex g_static_scratch_mu;
+
+// Once per device, with that device current: look up the array's device address.
+rr_status static_scratch_for_current_device(unsigned char **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_rr_static_scratch) != cudaSuccess || !addr) return RR_ERR_CUDA;
+    g_static_scratch_addr[dev] = static_cast<unsigned char *>(addr);
+  }
+  *out = g_static_scratch_addr[dev];
+  return RR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -571,6 +597,22 @@ rr_status ring_allreduce_host(const void *const *host_in, void *const *host_out,
                               rr_dtype dtype, rr_dtype wire, int group_size, void *dev_workspace,
                               size_t workspace_bytes, cudaStream_t stream) {
   return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, dev_workspace, workspace_bytes, stream);
+}
+
+rr_status ring_allreduce_host_static(const void *const *host_in, void *const *host_out, int R, size_t count,
+                                     rr_dtype dtype, rr_dtype wire, int group_size, size_t piece_count,
+                                     cudaStream_t stream) {
+  // size checks first: nothing is touched when the request does not fit
+  if (R < 1 || R > RR_MAX_RANKS || !valid_type(dtype)) return RR_ERR_INVALID_ARG;
+  const size_t per_slot_elem = (size_t)kHostSlots * (size_t)R * elem_bytes(dtype);
+  const size_t largest = RR_STATIC_SCRATCH_BYTES / per_slot_elem / kPieceAlign * kPieceAlign;
+  if (largest == 0 || piece_count > largest) return RR_ERR_INVALID_ARG;
+  const size_t piece = piece_count == 0 ? largest : (piece_count + kPieceAlign - 1) / kPieceAlign * kPieceAlign;
+  unsigned char *scratch = nullptr;
+  rr_status st = static_scratch_for_current_device(&scratch);
+  if (st != RR_OK) return st;
+  // the pipeline never reads a slot it has not first filled, so nothing needs clearing
+  return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, scratch, piece * per_slot_elem, stream);
 }
 
 }  // extern "C"
