@@ -137,11 +137,12 @@ static size_t elem_size(int t) { return t == ORC_F32 ? 4 : 2; }
 
 static int valid_type(int t) { return t == ORC_F32 || t == ORC_F16 || t == ORC_BF16; }
 
-/* Supported (storage, wire) pairs: the same type, or binary32 storage carried
- * on a 16-bit wire. */
+/* Supported (storage, wire) pairs: the same type; binary32 storage carried on
+ * a 16-bit wire; or 16-bit storage accumulated in binary32 (exact widening on
+ * ingress, binary32 hops, one rounding to the storage format at the end). */
 static int supported_pair(int dtype, int wire) {
   if (!valid_type(dtype) || !valid_type(wire)) return 0;
-  return dtype == wire || dtype == ORC_F32;
+  return dtype == wire || dtype == ORC_F32 || wire == ORC_F32;
 }
 
 /* Encoding at j (binary32 bits for ORC_F32). */
@@ -182,13 +183,15 @@ uint32_t orc_wire_add(int wire, uint32_t a, uint32_t b) {
   return value_to_bits(wire, s);                             /* identity for binary32 */
 }
 
-/* Storage element -> wire encoding (ingress cast, round to nearest even). */
+/* Storage element -> wire encoding (ingress cast: round to nearest even, or
+ * exact when the wire is wider). */
 static uint32_t ingress(int dtype, int wire, uint32_t v) {
   if (dtype == wire) return v;
   return value_to_bits(wire, bits_to_value(dtype, v));
 }
 
-/* Wire encoding -> storage element (egress widening, exact). */
+/* Wire encoding -> storage element (egress: exact widening, or one rounding to
+ * nearest even when the storage is narrower). */
 static uint32_t egress(int dtype, int wire, uint32_t v) {
   if (dtype == wire) return v;
   return value_to_bits(dtype, bits_to_value(wire, v));

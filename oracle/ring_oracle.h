@@ -20,7 +20,9 @@
  *        2(N-1)*S/N per card.
  *   [p2] ai6s.net/6a157e6510ee7a33f27553e9.html, "自定义通信模式" -- the chunk
  *        partition: floor(count/ranks) per chunk, the last chunk takes the rest.
- *   [p5] "大模型训练中的通信优化" -- gradients communicated in FP16.
+ *   [p5] "大模型训练中的通信优化" -- gradients communicated in FP16; mixed
+ *        FP16 / FP32 precision (read here both ways: binary32 values on a
+ *        16-bit wire, and 16-bit values accumulated in binary32).
  *   [p5] "通信拓扑与带宽利用率" -- across nodes, one inter-node exchange per
  *        AllReduce (the two-level ring).
  *

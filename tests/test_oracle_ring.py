@@ -16,7 +16,8 @@ import torch
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-PAIRS = [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"), ("f32", "bf16"), ("f32", "f16")]
+PAIRS = [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"), ("f32", "bf16"), ("f32", "f16"), ("f16", "f32"),
+         ("bf16", "f32")]
 EB = {"f32": 4, "f16": 2, "bf16": 2}
 
 
@@ -304,6 +305,8 @@ def test_r2_is_one_rounded_add():
 
 
 @pytest.mark.parametrize("dtype,wire,R,L,dist", [
+    ("f16", "f32", 8, 0, "grad"),
+    ("bf16", "f32", 8, 0, "grad2"),
     ("f32", "f32", 4, 0, "uniform"),
     ("f16", "f16", 8, 0, "grad"),
     ("f32", "bf16", 8, 0, "normal"),
@@ -336,7 +339,10 @@ def test_error_bound_against_fp64(dtype, wire, R, L, dist):
     exact = np.sum(x64, axis=0)
     mag = np.sum(np.abs(x64), axis=0)
     tol = {"f32": 1e-6, "f16": R * 2.0 ** -10, "bf16": R * 2.0 ** -7}[wire]
-    floor = (R - 1) * 2.0 ** -25 if wire == "f16" else 0.0
+    if wire == "f32" and dtype != "f32":
+        # binary32 accumulation: (R-1) binary32 roundings, then one rounding to storage
+        tol = (R - 1) * 2.0 ** -24 + {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}[dtype]
+    floor = (R - 1) * 2.0 ** -25 if wire == "f16" else (2.0 ** -25 if dtype == "f16" else 0.0)
     out = to_f64(oracle.allreduce(xs, dtype, wire, group_size=L).outs[0], dtype)
     err = np.abs(out - exact)
     assert np.all(err <= tol * mag + floor), float(np.max(err / (mag + 1e-300)))
@@ -439,10 +445,10 @@ def test_faults_are_detected():
 def test_bad_arguments():
     x = [np.ones(4, np.float32)] * 3
     assert oracle.allreduce(x, "f32", group_size=2).status == oracle.EINVAL
-    assert oracle.allreduce([x[0].astype(np.float16).view(np.uint16)] * 3, "f16", "f32").status == \
-        oracle.EUNSUPPORTED
-    assert oracle.allreduce([x[0].astype(np.float16).view(np.uint16)] * 3, "f16", "bf16").status == \
-        oracle.EUNSUPPORTED
+    h = [x[0].astype(np.float16).view(np.uint16)] * 3
+    assert oracle.allreduce(h, "f16", "bf16").status == oracle.EUNSUPPORTED
+    assert oracle.allreduce(h, "bf16", "f16").status == oracle.EUNSUPPORTED
+    assert oracle.allreduce(h, "f16", "f32").status == oracle.OK
 
 
 # --------------------------------------------------------------------------
@@ -513,3 +519,27 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
         except (AssertionError, RuntimeError):  # a failed check or an oracle error status
             caught.append(pin.__name__)
     assert caught, f"planted mistake {name!r} passed every pin"
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_binary32_accumulation_is_more_accurate(dtype):
+    """Ablation of the per-hop rounding: on gradient-like data, accumulating in
+    binary32 and rounding once leaves a smaller error than rounding every hop,
+    and never a larger one than half a unit of the storage format per element
+    beyond the binary32 part."""
+    rng = np.random.default_rng(21)
+    R, N = 8, 50_000
+    x32 = [(rng.standard_normal(N) * 1e-3).astype(np.float32) for _ in range(R)]
+    if dtype == "f16":
+        xs = [x.astype(np.float16).view(np.uint16) for x in x32]
+    else:
+        xs = [torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for x in x32]
+    exact = np.sum([to_f64(x, dtype) for x in xs], axis=0)
+    hop = to_f64(oracle.allreduce(xs, dtype).outs[0], dtype)
+    acc = to_f64(oracle.allreduce(xs, dtype, "f32").outs[0], dtype)
+    e_hop, e_acc = np.abs(hop - exact), np.abs(acc - exact)
+    assert e_acc.mean() < 0.5 * e_hop.mean()
+    # one final rounding of a value within (R-1) binary32 roundings of the exact sum
+    ulp_half = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}[dtype]
+    assert np.all(e_acc <= ulp_half * np.abs(exact) * 1.0001 + (R - 1) * 2.0 ** -24 * np.sum(
+        [np.abs(to_f64(x, dtype)) for x in xs], axis=0) + 2.0 ** -25)
