@@ -339,7 +339,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         if not args.no_workloads:
             for w in (wl.config1("allreduce"), wl.config1("reduce_scatter"), wl.config1("allgather"), wl.config3(),
-                      wl.config4(), wl.config5(0)):
+                      wl.config4(), wl.config5(0), wl.config2(512, wire="f32")):
                 table.append(graph_row(rr, wl, w, dev, l2_bytes, peak, args.sweep_iters))
                 torch.cuda.empty_cache()
         outs = [torch.empty_like(x) for x in xs]

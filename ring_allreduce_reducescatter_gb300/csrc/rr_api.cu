@@ -79,7 +79,7 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
   if (op != RR_OP_ALLREDUCE && op != RR_OP_REDUCE_SCATTER && op != RR_OP_ALLGATHER) return RR_ERR_INVALID_ARG;
   if (R < 1 || R > RR_MAX_RANKS) return RR_ERR_INVALID_ARG;
   if (!valid_type(dtype) || !valid_type(wire)) return RR_ERR_INVALID_ARG;
-  if (!(dtype == wire || dtype == RR_FP32)) return RR_ERR_UNSUPPORTED;
+  if (!(dtype == wire || dtype == RR_FP32 || wire == RR_FP32)) return RR_ERR_UNSUPPORTED;
   if (op == RR_OP_ALLGATHER && wire != dtype) return RR_ERR_UNSUPPORTED;
   const int L = group_size == 0 ? R : group_size;
   if (L < 1 || L > R || R % L != 0) return RR_ERR_INVALID_ARG;

@@ -6,7 +6,9 @@
 //    bfloat16 hops use the hardware's correctly rounded 16-bit adds: because
 //    binary32 carries at least 2p+2 significand bits for p = 11 and p = 8, one
 //    correctly rounded 16-bit add equals the binary32 sum rounded once.
-//  * 16-byte vector forms of ingress (storage -> wire), hop and egress.
+//  * 16-byte vector forms of ingress (storage -> wire), hop and egress, for
+//    every supported (storage, wire) pair, including 16-bit storage summed in
+//    binary32 (the same section's FP16 / FP32 mixed precision).
 //  * chunk lookup of the partition of N elements into L chunks (page
 //    ai6s.net/6a157e65..., section "自定义通信模式": floor(N/L) per chunk, the
 //    last chunk takes the rest).
@@ -77,6 +79,15 @@ template <>
 __device__ __forceinline__ __half Scalar<kF32, kF16>::in(float x) { return __float2half_rn(x); }
 template <>
 __device__ __forceinline__ float Scalar<kF32, kF16>::out(__half w) { return __half2float(w); }
+// 16-bit storage accumulated in binary32: exact widening, one rounding at the end
+template <>
+__device__ __forceinline__ float Scalar<kF16, kF32>::in(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ __half Scalar<kF16, kF32>::out(float w) { return __float2half_rn(w); }
+template <>
+__device__ __forceinline__ float Scalar<kBF16, kF32>::in(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 Scalar<kBF16, kF32>::out(float w) { return __float2bfloat16_rn(w); }
 
 // --------------------------------------------------------------------------
 // 16-byte vectors: V storage elements, held in the wire format as W
@@ -172,6 +183,52 @@ struct Vec<kF32, kF16> {
   static __device__ __forceinline__ uint4 out(W w) {
     float2 lo = __half22float2(as_h2(w.x)), hi = __half22float2(as_h2(w.y));
     return make_uint4(__float_as_uint(lo.x), __float_as_uint(lo.y), __float_as_uint(hi.x), __float_as_uint(hi.y));
+  }
+};
+
+// Eight binary32 lanes: 16 bytes of 16-bit storage accumulated in binary32.
+struct F8 {
+  float4 lo, hi;
+};
+
+__device__ __forceinline__ F8 add_f8(const F8 &a, const F8 &b) {
+  F8 r;
+  r.lo = make_float4(__fadd_rn(a.lo.x, b.lo.x), __fadd_rn(a.lo.y, b.lo.y), __fadd_rn(a.lo.z, b.lo.z),
+                     __fadd_rn(a.lo.w, b.lo.w));
+  r.hi = make_float4(__fadd_rn(a.hi.x, b.hi.x), __fadd_rn(a.hi.y, b.hi.y), __fadd_rn(a.hi.z, b.hi.z),
+                     __fadd_rn(a.hi.w, b.hi.w));
+  return r;
+}
+
+template <>
+struct Vec<kF16, kF32> {
+  static constexpr int V = 8;
+  using W = F8;
+  static __device__ __forceinline__ W in(uint4 r) {
+    float2 a = __half22float2(as_h2(r.x)), b = __half22float2(as_h2(r.y)), c = __half22float2(as_h2(r.z)),
+           d = __half22float2(as_h2(r.w));
+    return F8{make_float4(a.x, a.y, b.x, b.y), make_float4(c.x, c.y, d.x, d.y)};
+  }
+  static __device__ __forceinline__ W hop(W a, W b) { return add_f8(a, b); }
+  static __device__ __forceinline__ uint4 out(W w) {
+    return make_uint4(as_u32(__floats2half2_rn(w.lo.x, w.lo.y)), as_u32(__floats2half2_rn(w.lo.z, w.lo.w)),
+                      as_u32(__floats2half2_rn(w.hi.x, w.hi.y)), as_u32(__floats2half2_rn(w.hi.z, w.hi.w)));
+  }
+};
+
+template <>
+struct Vec<kBF16, kF32> {
+  static constexpr int V = 8;
+  using W = F8;
+  static __device__ __forceinline__ W in(uint4 r) {
+    float2 a = __bfloat1622float2(as_b2(r.x)), b = __bfloat1622float2(as_b2(r.y)),
+           c = __bfloat1622float2(as_b2(r.z)), d = __bfloat1622float2(as_b2(r.w));
+    return F8{make_float4(a.x, a.y, b.x, b.y), make_float4(c.x, c.y, d.x, d.y)};
+  }
+  static __device__ __forceinline__ W hop(W a, W b) { return add_f8(a, b); }
+  static __device__ __forceinline__ uint4 out(W w) {
+    return make_uint4(as_u32(__floats2bfloat162_rn(w.lo.x, w.lo.y)), as_u32(__floats2bfloat162_rn(w.lo.z, w.lo.w)),
+                      as_u32(__floats2bfloat162_rn(w.hi.x, w.hi.y)), as_u32(__floats2bfloat162_rn(w.hi.z, w.hi.w)));
   }
 };
 

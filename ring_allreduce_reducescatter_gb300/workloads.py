@@ -51,10 +51,12 @@ def config1(op: str = "allreduce") -> Workload:
     return Workload(1, f"{op} R=4 fp32 N=1048576", op, 4, torch.float32, None, 1_048_576, "uniform")
 
 
-def config2(msg_mib: int = 512) -> Workload:
+def config2(msg_mib: int = 512, wire: Optional[str] = None) -> Workload:
+    """Workload 2; wire="f32" is its binary32-accumulation variant (same inputs)."""
     count = msg_mib * MIB // 2
-    return Workload(2, f"allreduce R=8 fp16 per-hop fp16 msg={msg_mib}MiB", "allreduce", 8,
-                    torch.float16, None, count, "grad1e-3")
+    how = "per-hop fp16" if wire is None else f"{wire} accumulation"
+    return Workload(2, f"allreduce R=8 fp16 {how} msg={msg_mib}MiB", "allreduce", 8,
+                    torch.float16, wire, count, "grad1e-3")
 
 
 CONFIG2_SIZES_MIB = (1, 16, 128, 512)

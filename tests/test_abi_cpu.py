@@ -108,7 +108,7 @@ def test_bad_rank_counts(L):
 def test_bad_dtypes_and_pairs(L):
     ins, outs = fake(4, 100, 4)
     assert call(L, AR, ins, outs, 4, 100, 3) == EINVAL
-    assert call(L, AR, ins, outs, 4, 100, F16, F32) == EUNSUP
+    assert call(L, AR, ins, outs, 4, 100, F16, F32) not in (EINVAL, EUNSUP, EALIAS)  # binary32 accumulation
     assert call(L, AR, ins, outs, 4, 100, F16, BF16) == EUNSUP
     assert call(L, AR, ins, outs, 4, 100, BF16, F16) == EUNSUP
     assert call(L, AG, ins, outs, 4, 100, F32, BF16) == EUNSUP
@@ -290,7 +290,7 @@ def test_range_arguments(L):
     assert call_range(L, ins, outs, 4, 100, 100, 0, F32) == OK       # empty range at the end
     assert call_range(L, ins, outs, 4, 100, 0, 0, F32) == OK
     assert call_range(L, ins, outs, 0, 100, 0, 10, F32) == EINVAL
-    assert call_range(L, ins, outs, 4, 100, 0, 10, F16, F32) == EUNSUP
+    assert call_range(L, ins, outs, 4, 100, 0, 10, F16, BF16) == EUNSUP
     assert call_range(L, ins, outs, 4, 100, 0, 10, F32, group=3) == EINVAL
     assert call_range(L, ins, [ins[1]] + outs[1:], 4, 100, 0, 10, F32) == EALIAS
     assert call_range(L, ins, list(ins), 4, 100, 50, 10, F32) not in (EINVAL, EALIAS, EUNSUP)
@@ -321,6 +321,6 @@ def test_host_pipeline_arguments(L):
     assert call_host(L, hin, hout, R, N, F32, ws, need - 1) == EINVAL        # no room for 256 elements
     assert call_host(L, hin, hout, R, N, F32, hin[2] + 64, need) == EALIAS   # overlaps a host buffer
     assert call_host(L, hin, [hin[1]] + hout[1:], R, N, F32, ws, need) == EALIAS   # output 0 on input 1
-    assert call_host(L, hin, hout, R, N, F16, ws, need, wire=F32) == EUNSUP
+    assert call_host(L, hin, hout, R, N, F16, ws, need, wire=BF16) == EUNSUP
     assert call_host(L, hin, hout, R, 0, F32, ws, need) == OK                # nothing to do
     assert call_host(L, hin, list(hin), R, N, F32, ws, need) not in (EINVAL, EALIAS, EUNSUP)  # in place

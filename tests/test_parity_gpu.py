@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
 PAIRS = [(torch.float32, None), (torch.float16, None), (torch.bfloat16, None), (torch.float32, "bf16"),
-         (torch.float32, "f16")]
+         (torch.float32, "f16"), (torch.float16, "f32"), (torch.bfloat16, "f32")]
 
 
 @pytest.fixture(scope="module")
