@@ -28,7 +28,10 @@ NP_STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16}
 ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
 
 OK, EINVAL, EUNSUPPORTED, ENOMEM, EPROTO, ETIMEOUT = 0, 1, 2, 3, 4, 5
-PHASE_RS, PHASE_XCHG, PHASE_XBCAST, PHASE_AG = 0, 1, 2, 3
+PHASE_RS, PHASE_XCHG, PHASE_XBCAST, PHASE_AG, PHASE_PRE, PHASE_POST = 0, 1, 2, 3, 4, 5
+ALGO_RING, ALGO_HALVING_DOUBLING, ALGO_NAIVE = 0, 1, 2
+ALGOS = {"ring": ALGO_RING, "hd": ALGO_HALVING_DOUBLING, "halving_doubling": ALGO_HALVING_DOUBLING,
+         "naive": ALGO_NAIVE}
 FAULT_NONE, FAULT_DROP, FAULT_DUP, FAULT_SILENT = 0, 1, 2, 3
 
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
@@ -82,6 +85,12 @@ def load(path: str):
                                     ctypes.c_int, ctypes.c_void_p]
     for f in ("orc_allreduce", "orc_reduce_scatter", "orc_allgather", "orc_fold_gathered"):
         getattr(L, f).restype = ctypes.c_int
+    L.orc_allreduce_algo.argtypes = [vpp, vpp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.POINTER(Opts)]
+    L.orc_allreduce_algo.restype = ctypes.c_int
+    L.orc_fold_gathered_algo.argtypes = [vpp, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    L.orc_fold_gathered_algo.restype = ctypes.c_int
     L.orc_chunk_len.argtypes = [ctypes.c_size_t, ctypes.c_int, ctypes.c_int]
     L.orc_chunk_len.restype = ctypes.c_size_t
     L.orc_chunk_off.argtypes = [ctypes.c_size_t, ctypes.c_int, ctypes.c_int]
@@ -210,6 +219,35 @@ def allgather(ins, count, dtype="f32", trace_cap=0, fault=None, poll_limit=0):
     o, sent, tr = _opts(R, trace_cap, fault, poll_limit)
     st = lib().orc_allgather(_ptrs(ins), _ptrs(outs), R, count, DTYPES[dtype], ctypes.byref(o))
     return _finish(st, outs, o, sent, tr, R)
+
+
+def allreduce_algo(ins, dtype="f32", wire=None, algo="ring", trace_cap=0, fault=None, poll_limit=0):
+    """Literal AllReduce by algorithm ("ring", "hd" = halving-doubling, "naive")."""
+    wire = wire or dtype
+    R = len(ins)
+    N = ins[0].size if R else 0
+    _check(ins, dtype)
+    outs = [np.empty(N, dtype=NP_STORAGE[dtype]) for _ in range(R)]
+    o, sent, tr = _opts(R, trace_cap, fault, poll_limit)
+    st = lib().orc_allreduce_algo(_ptrs(ins), _ptrs(outs), R, N, DTYPES[dtype], DTYPES[wire], ALGOS[algo],
+                                  ctypes.byref(o))
+    return _finish(st, outs, o, sent, tr, R)
+
+
+def fold_gathered_algo(vals, idx, count, dtype="f32", wire=None, algo="ring"):
+    """Closed form of allreduce_algo at global indices ``idx``."""
+    wire = wire or dtype
+    R = len(vals)
+    idx = np.ascontiguousarray(idx, dtype=np.uint64)
+    vals = [np.ascontiguousarray(v) for v in vals]
+    _check(vals, dtype)
+    out = np.empty(idx.size, dtype=NP_STORAGE[dtype])
+    st = lib().orc_fold_gathered_algo(_ptrs(vals), idx.ctypes.data if idx.size else None, idx.size, R, count,
+                                      DTYPES[dtype], DTYPES[wire], ALGOS[algo],
+                                      out.ctypes.data if out.size else None)
+    if st != OK:
+        raise RuntimeError(f"orc_fold_gathered_algo failed with status {st}")
+    return out
 
 
 def fold_gathered(vals, idx, count, dtype="f32", wire=None, group_size=0):

@@ -576,3 +576,152 @@ int orc_fold_gathered(const void *const *vals, const uint64_t *idx, size_t n, in
   }
   return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Halving-doubling and naive AllReduce.                                     */
+/* ------------------------------------------------------------------------ */
+
+static int floor_pow2(int R) {
+  int P = 1;
+  while (P * 2 <= R) P *= 2;
+  return P;
+}
+
+static int log2_exact(int P) {
+  int l = 0;
+  while ((1 << l) < P) l++;
+  return l;
+}
+
+/* rank of virtual rank v in halving-doubling (E extra ranks folded in pairs) */
+static int hd_rank(int v, int E) { return v < E ? 2 * v + 1 : v + E; }
+
+/* element offset of block b of the (count, P) table; block P is the end */
+static size_t block_start(size_t count, int P, int b) {
+  return b >= P ? count : orc_chunk_off(count, P, b);
+}
+
+static void halving_doubling(ring_sim *s, int R, size_t count) {
+  const int P = floor_pow2(R), E = R - P, steps = log2_exact(P);
+  /* fold the extra ranks into their odd neighbours */
+  for (int k = 0; k < E; k++) sim_send(s, ORC_PHASE_PRE, 0, 2 * k, 2 * k + 1, -1, 0, count);
+  for (int k = 0; k < E && s->status == ORC_OK; k++) recv_add(s, 2 * k + 1, 2 * k, -1, 0, count);
+  /* recursive halving: every virtual rank owns the block range [lo[v], hi[v]) */
+  int lo[64], hi[64];
+  for (int v = 0; v < P; v++) {
+    lo[v] = 0;
+    hi[v] = P;
+  }
+  for (int t = 0; t < steps && s->status == ORC_OK; t++) {
+    const int d = P >> (t + 1);
+    int keep_lo[64], keep_hi[64];
+    for (int v = 0; v < P; v++) { /* send the half the partner keeps */
+      const int mid = (lo[v] + hi[v]) / 2, u = v ^ d;
+      const int give_lo = (v & d) ? lo[v] : mid, give_hi = (v & d) ? mid : hi[v];
+      keep_lo[v] = (v & d) ? mid : lo[v];
+      keep_hi[v] = (v & d) ? hi[v] : mid;
+      const size_t a = block_start(count, P, give_lo), b = block_start(count, P, give_hi);
+      sim_send(s, ORC_PHASE_RS, t, hd_rank(v, E), hd_rank(u, E), give_lo, a, b - a);
+    }
+    for (int v = 0; v < P && s->status == ORC_OK; v++) { /* add the partner's copy of the half I keep */
+      const size_t a = block_start(count, P, keep_lo[v]), b = block_start(count, P, keep_hi[v]);
+      recv_add(s, hd_rank(v, E), hd_rank(v ^ d, E), keep_lo[v], a, b - a);
+    }
+    for (int v = 0; v < P; v++) {
+      lo[v] = keep_lo[v];
+      hi[v] = keep_hi[v];
+    }
+  }
+  /* recursive doubling: swap ranges with the partner, nearest partner first */
+  for (int t = steps - 1; t >= 0 && s->status == ORC_OK; t--) {
+    const int d = P >> (t + 1);
+    for (int v = 0; v < P; v++) {
+      const size_t a = block_start(count, P, lo[v]), b = block_start(count, P, hi[v]);
+      sim_send(s, ORC_PHASE_AG, steps - 1 - t, hd_rank(v, E), hd_rank(v ^ d, E), lo[v], a, b - a);
+    }
+    int new_lo[64], new_hi[64];
+    for (int v = 0; v < P && s->status == ORC_OK; v++) {
+      const int u = v ^ d;
+      const size_t a = block_start(count, P, lo[u]), b = block_start(count, P, hi[u]);
+      recv_copy(s, hd_rank(v, E), hd_rank(u, E), lo[u], a, b - a);
+      new_lo[v] = lo[v] < lo[u] ? lo[v] : lo[u];
+      new_hi[v] = hi[v] > hi[u] ? hi[v] : hi[u];
+    }
+    for (int v = 0; v < P; v++) {
+      lo[v] = new_lo[v];
+      hi[v] = new_hi[v];
+    }
+  }
+  /* hand the result back to the folded ranks */
+  for (int k = 0; k < E && s->status == ORC_OK; k++) sim_send(s, ORC_PHASE_POST, 0, 2 * k + 1, 2 * k, -1, 0, count);
+  for (int k = 0; k < E && s->status == ORC_OK; k++) recv_copy(s, 2 * k, 2 * k + 1, -1, 0, count);
+}
+
+static void naive_reduce_broadcast(ring_sim *s, int R, size_t count) {
+  for (int k = 1; k < R && s->status == ORC_OK; k++) { /* the collector adds rank k's vector */
+    sim_send(s, ORC_PHASE_RS, k - 1, k, 0, -1, 0, count);
+    recv_add(s, 0, k, -1, 0, count);
+  }
+  for (int k = 1; k < R && s->status == ORC_OK; k++) { /* and sends the sum back */
+    sim_send(s, ORC_PHASE_AG, k - 1, 0, k, -1, 0, count);
+    recv_copy(s, k, 0, -1, 0, count);
+  }
+}
+
+int orc_allreduce_algo(const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
+                       int algo, orc_opts *opts) {
+  if (algo == ORC_ALGO_RING) return orc_allreduce(in, out, R, count, dtype, wire, 0, opts);
+  if (algo != ORC_ALGO_HALVING_DOUBLING && algo != ORC_ALGO_NAIVE) return ORC_EINVAL;
+  if (R < 1 || R > 64 || !in || !out) return ORC_EINVAL;
+  if (!supported_pair(dtype, wire)) return ORC_EUNSUPPORTED;
+  for (int r = 0; r < R; r++)
+    if (count > 0 && (!in[r] || !out[r])) return ORC_EINVAL;
+  ring_sim s;
+  int st = sim_init(&s, R, wire, count, count, opts);
+  if (st != ORC_OK) {
+    sim_free(&s);
+    return st;
+  }
+  for (int r = 0; r < R; r++)
+    for (size_t j = 0; j < count; j++) put_bits(s.W[r], wire, j, ingress(dtype, wire, get_bits(in[r], dtype, j)));
+  if (algo == ORC_ALGO_NAIVE)
+    naive_reduce_broadcast(&s, R, count);
+  else
+    halving_doubling(&s, R, count);
+  if (s.status == ORC_OK)
+    for (int r = 0; r < R; r++)
+      for (size_t j = 0; j < count; j++) put_bits(out[r], dtype, j, egress(dtype, wire, get_bits(s.W[r], wire, j)));
+  st = s.status;
+  sim_free(&s);
+  return st;
+}
+
+/* Closed forms.  Naive: x_0 (+) x_1 (+) ... (+) x_{R-1}.  Halving-doubling:
+ * leaves L_v = x_{2v} (+) x_{2v+1} for v < E, x_{v+E} otherwise; then for
+ * d = P/2, P/4, ..., 1: L_v = L_v (+) L_{v+d} for v < d; the result is L_0. */
+int orc_fold_gathered_algo(const void *const *vals, const uint64_t *idx, size_t n, int R, size_t count,
+                           int dtype, int wire, int algo, void *out) {
+  if (algo == ORC_ALGO_RING) return orc_fold_gathered(vals, idx, n, R, count, dtype, wire, 0, out);
+  if (algo != ORC_ALGO_HALVING_DOUBLING && algo != ORC_ALGO_NAIVE) return ORC_EINVAL;
+  if (R < 1 || R > 64 || !vals || (n > 0 && (!idx || !out))) return ORC_EINVAL;
+  if (!supported_pair(dtype, wire)) return ORC_EUNSUPPORTED;
+  for (size_t k = 0; k < n; k++) {
+    if ((size_t)idx[k] >= count) return ORC_EINVAL;
+    uint32_t x[64];
+    for (int r = 0; r < R; r++) x[r] = ingress(dtype, wire, get_bits(vals[r], dtype, k));
+    uint32_t y;
+    if (algo == ORC_ALGO_NAIVE) {
+      y = x[0];
+      for (int r = 1; r < R; r++) y = orc_wire_add(wire, y, x[r]);
+    } else {
+      const int P = floor_pow2(R), E = R - P;
+      uint32_t leaf[64];
+      for (int v = 0; v < P; v++) leaf[v] = v < E ? orc_wire_add(wire, x[2 * v], x[2 * v + 1]) : x[v + E];
+      for (int d = P / 2; d >= 1; d /= 2)
+        for (int v = 0; v < d; v++) leaf[v] = orc_wire_add(wire, leaf[v], leaf[v + d]);
+      y = leaf[0];
+    }
+    put_bits(out, dtype, k, egress(dtype, wire, y));
+  }
+  return ORC_OK;
+}

@@ -40,7 +40,10 @@
  *
  * Parity unpinned: the group order of the two-level fold when there are more
  * than two groups (the pages fix nothing there; with two groups every order
- * gives the same bits, which the tests check).
+ * gives the same bits, which the tests check); the steps of halving-doubling
+ * and the collector's order in the naive AllReduce (the pages name both
+ * algorithms but give no steps; the readings are stated at
+ * orc_allreduce_algo).
  *
  * Element storage: ORC_F32 elements are IEEE binary32; ORC_F16 and ORC_BF16
  * elements are 16-bit encodings held in uint16_t.
@@ -66,8 +69,25 @@ enum {
   ORC_ETIMEOUT = 5      /* a receive found no message within its poll limit */
 };
 
-/* Phases of a message in the trace. */
-enum { ORC_PHASE_RS = 0, ORC_PHASE_XCHG = 1, ORC_PHASE_XBCAST = 2, ORC_PHASE_AG = 3 };
+/* Phases of a message in the trace.  ORC_PHASE_RS / ORC_PHASE_AG are the
+ * reduce and distribute halves of every algorithm; PRE / POST are the folding
+ * of the extra ranks of halving-doubling when R is not a power of two. */
+enum {
+  ORC_PHASE_RS = 0,
+  ORC_PHASE_XCHG = 1,
+  ORC_PHASE_XBCAST = 2,
+  ORC_PHASE_AG = 3,
+  ORC_PHASE_PRE = 4,
+  ORC_PHASE_POST = 5
+};
+
+/* AllReduce algorithms (page ai6s.net/6a0dd5b5662f9a54cb75ef90.html, the
+ * topology switch of TpAllReduceOp::Execute: ring for a ring topology,
+ * halving-doubling with logarithmic steps for a full mesh, naive Reduce +
+ * Broadcast otherwise; page hwcomputing.csdn.net/6a0dc11a..., section
+ * "为什么大模型训练离不开通信": without a library every card sends its
+ * gradients to a collector, which adds them and sends the sum back). */
+enum { ORC_ALGO_RING = 0, ORC_ALGO_HALVING_DOUBLING = 1, ORC_ALGO_NAIVE = 2 };
 
 /* One simulated message. */
 typedef struct {
@@ -129,6 +149,29 @@ int orc_reduce_scatter(const void *const *in, void *const *out, int R, size_t co
  * out[r] receives all `count` elements. */
 int orc_allgather(const void *const *in, void *const *out, int R, size_t count, int dtype,
                   orc_opts *opts);
+
+/*
+ * AllReduce by algorithm (flat: one group).  ORC_ALGO_RING is orc_allreduce.
+ * ORC_ALGO_NAIVE: ranks 1..R-1 send their vectors to rank 0 in rank order,
+ * rank 0 adds each as it arrives (((x0 + x1) + x2) + ...), then sends the sum
+ * to ranks 1..R-1.
+ * ORC_ALGO_HALVING_DOUBLING (reading: the textbook recursive-halving
+ * reduce-scatter and recursive-doubling allgather, the pages give no steps):
+ * with P the largest power of two <= R and E = R - P, rank 2k (k < E) first
+ * sends its vector to rank 2k+1, which adds it; the remaining P ranks (virtual
+ * rank v is rank 2v+1 for v < E, rank v+E otherwise) split the vector into P
+ * blocks (the chunk table of (count, P)); at step t = 0..log2(P)-1, virtual
+ * ranks v and v ^ (P >> (t+1)) swap halves of their current block range, the
+ * lower rank keeping the lower half, and each adds the half it keeps; the
+ * allgather reverses the steps with copies; rank 2k+1 finally sends the result
+ * to rank 2k.
+ */
+int orc_allreduce_algo(const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
+                       int algo, orc_opts *opts);
+
+/* Closed form of orc_allreduce_algo at sampled elements (as orc_fold_gathered). */
+int orc_fold_gathered_algo(const void *const *vals, const uint64_t *idx, size_t n, int R, size_t count,
+                           int dtype, int wire, int algo, void *out);
 
 /*
  * Closed form of the AllReduce result, one element at a time, for sampled
