@@ -192,7 +192,7 @@ def time_oracle(msg_mib, seed0=2000):
     return n * 2 / dt / 1e9, dt, n
 
 
-def graph_row(rr, wl, w, dev, l2_bytes, peak, launches):
+def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring"):
     """Time workload w: CUDA-graph replay of `launches` back-to-back calls over
     rotating buffer sets (>= 3x L2 in total).  Returns one table row."""
     import torch
@@ -211,8 +211,14 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches):
         ins = wl.inputs(w, dev, lengths=in_lens) if k == 0 else [t.clone() for t in sets[0][0]]
         outs = [torch.empty(n, dtype=w.dtype, device=dev) for n in out_lens]
         sets.append((ins, outs))
+    def call(ins, outs, stream=None):
+        if algo == "ring":
+            rr.collective(op, ins, outs, N, w.wire, w.group_size, stream)
+        else:
+            rr.allreduce_algo(ins, outs, w.wire, algo, stream)
+
     for ins, outs in sets:  # warm up outside capture
-        rr.collective(op, ins, outs, N, w.wire, w.group_size)
+        call(ins, outs)
     torch.cuda.synchronize(dev)
     s = torch.cuda.Stream(dev)
     g = torch.cuda.CUDAGraph()
@@ -220,7 +226,7 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches):
         with torch.cuda.graph(g, stream=s):
             for k in range(launches):
                 ins, outs = sets[k % nsets]
-                rr.collective(op, ins, outs, N, w.wire, w.group_size, s)
+                call(ins, outs, s)
     g.replay()
     torch.cuda.synchronize(dev)
     times = []
@@ -234,7 +240,8 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches):
     t_ms = min(times)
     alg = (2 * R_ if op == rr.OP_ALLREDUCE else R_ + 1) * msg
     busbw = msg / t_ms / 1e6 * ((2 if op == rr.OP_ALLREDUCE else 1) * (R_ - 1) / R_)
-    row = {"workload": w.name, "op": w.op, "R": R_, "group_size": w.group_size or R_, "count": N,
+    row = {"workload": w.name if algo == "ring" else f"{w.name}, {algo} order", "op": w.op, "algo": algo,
+           "R": R_, "group_size": w.group_size or R_, "count": N,
            "msg_bytes": msg, "ms": round(t_ms, 5), "algbw_gbs": round(msg / t_ms / 1e6, 2),
            "busbw_gbs": round(busbw, 2), "hbm_gbs": round(alg / t_ms / 1e6, 1),
            "roofline_frac": round(alg / t_ms / 1e6 / peak, 4), "buffer_sets": nsets,
@@ -341,6 +348,9 @@ def run_ours(args):
             for w in (wl.config1("allreduce"), wl.config1("reduce_scatter"), wl.config1("allgather"), wl.config3(),
                       wl.config4(), wl.config5(0), wl.config2(512, wire="f32")):
                 table.append(graph_row(rr, wl, w, dev, l2_bytes, peak, args.sweep_iters))
+                torch.cuda.empty_cache()
+            for algo in ("hd", "naive"):
+                table.append(graph_row(rr, wl, wl.config2(512), dev, l2_bytes, peak, args.sweep_iters, algo=algo))
                 torch.cuda.empty_cache()
         outs = [torch.empty_like(x) for x in xs]
 

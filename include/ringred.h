@@ -152,6 +152,30 @@ rr_status ring_collective(rr_op op, const void *const *in_bufs, void *const *out
                           size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
                           const rr_launch_cfg *cfg, cudaStream_t stream);
 
+/* AllReduce algorithms: the summation order of the result. */
+typedef enum { RR_ALGO_RING = 0, RR_ALGO_HALVING_DOUBLING = 1, RR_ALGO_NAIVE = 2 } rr_algo;
+
+/*
+ * ring_allreduce_algo -- the AllReduce of another algorithm on the topology
+ * switch of the page ai6s.net/6a0dd5b5662f9a54cb75ef90.html
+ * (TpAllReduceOp::Execute): same buffers, same bytes moved, a different
+ * summation order and so different bits.
+ *   RR_ALGO_RING: ring_allreduce_ex with group_size 0.
+ *   RR_ALGO_NAIVE (Reduce + Broadcast; the collector of the page
+ *     hwcomputing.csdn.net/6a0dc11a10ee7a33f273f7fd.html, section
+ *     "为什么大模型训练离不开通信"): y = ((x_0 (+) x_1) (+) x_2) ... (+) x_{R-1}.
+ *   RR_ALGO_HALVING_DOUBLING (full mesh, logarithmic steps; the pages give
+ *     no steps, the textbook recursive-halving / recursive-doubling algorithm
+ *     is taken): with P the largest power of two <= R and E = R - P, leaves
+ *     L_v = x_{2v} (+) x_{2v+1} for v < E and x_{v+E} otherwise, then
+ *     L_v = L_v (+) L_{v+d} for d = P/2, P/4, ..., 1; y = L_0.
+ * Arguments as for ring_allreduce_ex without group_size (flat ranks only);
+ * cfg as for ring_collective.
+ */
+rr_status ring_allreduce_algo(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
+                              rr_dtype dtype, rr_dtype wire, rr_algo algo, const rr_launch_cfg *cfg,
+                              cudaStream_t stream);
+
 /*
  * ring_allreduce_range -- elements [first, first + n) of the AllReduce of
  * count-element rank vectors: the building block of a chunked AllReduce that

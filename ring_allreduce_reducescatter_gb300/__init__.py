@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "RingError", "lib", "allreduce", "reduce_scatter", "allgather", "collective", "plan",
-    "allreduce_range", "allreduce_host", "allreduce_host_static", "host_workspace_bytes",
+    "allreduce_range", "allreduce_host", "allreduce_host_static", "host_workspace_bytes", "allreduce_algo",
     "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
     "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE",
@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
                   "ring_reduce_scatter", "ring_reduce_scatter_ex", "ring_allgather",
                   "ring_device_status", "ring_selftest_bounded_wait"):
             getattr(L, f).restype = i
+        L.ring_allreduce_algo.argtypes = [vpp, vpp, i, sz, i, i, i, ctypes.POINTER(LaunchCfg), vp]
+        L.ring_allreduce_algo.restype = i
         L.ring_allreduce_range.argtypes = [vpp, vpp, i, sz, sz, sz, i, i, i, ctypes.POINTER(LaunchCfg), vp]
         L.ring_allreduce_range.restype = i
         L.ring_allreduce_host.argtypes = [vpp, vpp, i, sz, i, i, i, vp, sz, vp]
@@ -209,6 +211,31 @@ def allgather(ins: Sequence[torch.Tensor], count: Optional[int] = None,
     if outs is None:
         outs = [torch.empty(count, dtype=ref.dtype, device=ref.device) for _ in ins]
     collective(OP_ALLGATHER, ins, list(outs), count, None, 0, stream, cfg)
+    return outs
+
+
+ALGO_RING, ALGO_HALVING_DOUBLING, ALGO_NAIVE = 0, 1, 2
+_ALGO_CODE = {"ring": ALGO_RING, "hd": ALGO_HALVING_DOUBLING, "halving_doubling": ALGO_HALVING_DOUBLING,
+              "naive": ALGO_NAIVE}
+
+
+def allreduce_algo(ins, outs=None, wire=None, algo="ring", stream=None, cfg: Optional[LaunchCfg] = None):
+    """ring_allreduce_algo: the AllReduce summed in the order of another algorithm
+    ("ring", "hd" = halving-doubling, "naive" = Reduce + Broadcast)."""
+    ins = list(ins)
+    if outs is None:
+        outs = [torch.empty_like(t) for t in ins]
+    outs = list(outs)
+    dtype = ins[0].dtype
+    _check_tensors(ins, dtype, "ins")
+    _check_tensors(outs, dtype, "outs")
+    dt = _code(dtype)
+    wt = dt if wire is None else _code(wire)
+    code = _ALGO_CODE[algo] if isinstance(algo, str) else int(algo)
+    st = lib().ring_allreduce_algo(_ptr_array(ins), _ptr_array(outs), len(ins), ins[0].numel(), dt, wt, code,
+                                   ctypes.byref(cfg) if cfg is not None else None, _stream_handle(stream))
+    if st != OK:
+        raise RingError(st, "ring_allreduce_algo")
     return outs
 
 

@@ -71,6 +71,7 @@ struct Checked {
   size_t n;
   size_t E;
   bool all_16b_aligned;
+  int algo;  // AllReduce summation order (rr_algo)
 };
 
 // Checks of everything but the buffers.
@@ -101,6 +102,7 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
   ck->count = count;
   ck->first = 0;
   ck->n = count;
+  ck->algo = RR_ALGO_RING;
   ck->E = elem_bytes(dtype);
   ck->all_16b_aligned = true;
   if (count > (SIZE_MAX / 4) / ck->E) return RR_ERR_INVALID_ARG;
@@ -178,6 +180,14 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   p->L = ck.L;
   p->G = ck.R / ck.L;
   p->base = (unsigned long long)ck.count / (unsigned long long)ck.L;
+  p->algo = ck.algo;
+  int P = 1, log2p = 0;
+  while (P * 2 <= ck.R) {
+    P *= 2;
+    ++log2p;
+  }
+  p->hd_log2p = log2p;
+  p->hd_extra = ck.R - P;
 
   // bulk path: 16-byte aligned buffers, and for ReduceScatter / AllGather
   // chunk boundaries on 16-byte multiples (segments are copied per chunk)
@@ -572,6 +582,18 @@ rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t s
 }
 
 int ring_abi_version(void) { return RR_ABI_VERSION; }
+
+rr_status ring_allreduce_algo(const void *const *in_bufs, void *const *out_bufs, int R, size_t count, rr_dtype dtype,
+                              rr_dtype wire, rr_algo algo, const rr_launch_cfg *cfg, cudaStream_t stream) {
+  if (algo != RR_ALGO_RING && algo != RR_ALGO_HALVING_DOUBLING && algo != RR_ALGO_NAIVE) return RR_ERR_INVALID_ARG;
+  Checked ck;
+  rr_status st = check_scalars(RR_OP_ALLREDUCE, R, count, dtype, wire, 0, cfg, &ck);
+  if (st != RR_OK) return st;
+  ck.algo = algo;
+  st = check_buffers(in_bufs, out_bufs, &ck);
+  if (st != RR_OK || count == 0) return st;
+  return launch_checked(ck, in_bufs, out_bufs, cfg, stream);
+}
 
 rr_status ring_allreduce_range(const void *const *in_bufs, void *const *out_bufs, int R, size_t count, size_t first,
                                size_t n, rr_dtype dtype, rr_dtype wire, int group_size, const rr_launch_cfg *cfg,

@@ -36,6 +36,72 @@
 namespace rr {
 
 // --------------------------------------------------------------------------
+// summation orders of the other AllReduce algorithms (page
+// ai6s.net/6a0dd5b5662f9a54cb75ef90.html, TpAllReduceOp::Execute)
+// --------------------------------------------------------------------------
+
+// Naive (Reduce + Broadcast): the collector adds ranks 0, 1, ..., R-1 in order,
+// which is the ring fold started at rank 0 for every element.
+__device__ __forceinline__ int start_rank(const RingParams &p, unsigned long long global_index) {
+  return p.algo == kAlgoNaive ? 0 : chunk_of(global_index, p.base, p.L);
+}
+
+__host__ __device__ constexpr int bit_reverse(int u, int bits) {
+  int r = 0;
+  for (int i = 0; i < bits; ++i) r |= ((u >> i) & 1) << (bits - 1 - i);
+  return r;
+}
+__host__ __device__ constexpr int trailing_ones(int u) {
+  int k = 0;
+  while (u & 1) {
+    ++k;
+    u >>= 1;
+  }
+  return k;
+}
+
+// Halving-doubling: P = 2^LOG2P leaves L_v, combined by recursive halving
+// (partners at distance P/2 first): level 1 adds L_v and L_{v+P/2}, level 2
+// adds those pair sums at distance P/4, and so on.  Visiting the leaves in
+// bit-reversed order turns that tree into adjacent pairs, so a pairwise stack
+// of LOG2P + 1 entries, fully unrolled, evaluates it with static indices.
+template <int LOG2P, class W, class Leaf, class Add>
+__device__ __forceinline__ W hd_tree(const Leaf &leaf, const Add &add) {
+  constexpr int P = 1 << LOG2P;
+  W stk[LOG2P + 1];
+#pragma unroll
+  for (int u = 0; u < P; ++u) {
+    W val = leaf(bit_reverse(u, LOG2P));
+#pragma unroll
+    for (int t = 0; t < LOG2P; ++t)
+      if (t < trailing_ones(u)) val = add(stk[t], val);
+    stk[trailing_ones(u)] = val;
+  }
+  return stk[LOG2P];
+}
+
+// The tree for the runtime P (leaf(v) gives L_v).
+template <class W, class Leaf, class Add>
+__device__ __forceinline__ W hd_fold(int log2p, const Leaf &leaf, const Add &add) {
+  switch (log2p) {
+    case 0:
+      return hd_tree<0, W>(leaf, add);
+    case 1:
+      return hd_tree<1, W>(leaf, add);
+    case 2:
+      return hd_tree<2, W>(leaf, add);
+    case 3:
+      return hd_tree<3, W>(leaf, add);
+    case 4:
+      return hd_tree<4, W>(leaf, add);
+    case 5:
+      return hd_tree<5, W>(leaf, add);
+    default:
+      return hd_tree<6, W>(leaf, add);
+  }
+}
+
+// --------------------------------------------------------------------------
 // one element, global memory
 // --------------------------------------------------------------------------
 
@@ -63,12 +129,30 @@ __device__ __forceinline__ typename Fmt<DT>::type fold_elem_global(const RingPar
 
 // The whole collective at element i (every input read, then every output written).
 // i is the buffers' (local) index; its chunk is that of the global index first + i.
-template <int OP, int DT, int WT>
+template <int DT, int WT>
+__device__ __forceinline__ typename Fmt<DT>::type hd_elem_global(const RingParams &p, unsigned long long i) {
+  using S = typename Fmt<DT>::type;
+  using SC = Scalar<DT, WT>;
+  using W = typename SC::W;
+  const int E = p.hd_extra;
+  auto x = [&](int r) { return SC::in(static_cast<const S *>(p.in[r])[i]); };
+  auto leaf = [&](int v) { return v < E ? hop(x(2 * v), x(2 * v + 1)) : x(v + E); };
+  auto add = [](W a, W b) { return hop(a, b); };
+  return SC::out(hd_fold<W>(p.hd_log2p, leaf, add));
+}
+
+// HD: the halving-doubling tree instead of the ring / naive fold (a separate
+// instantiation, so the ring kernels carry none of its registers).
+template <int OP, int DT, int WT, bool HD = false>
 __device__ __forceinline__ void element_op(const RingParams &p, unsigned long long i) {
   using S = typename Fmt<DT>::type;
-  const int c = chunk_of(p.first + i, p.base, p.L);
+  const int c = start_rank(p, p.first + i);
   if (OP == kOpAllReduce) {
-    const S v = fold_elem_global<DT, WT>(p, i, c);
+    S v;
+    if constexpr (HD)
+      v = hd_elem_global<DT, WT>(p, i);
+    else
+      v = fold_elem_global<DT, WT>(p, i, c);
     for (int r = 0; r < p.R; ++r) static_cast<S *>(p.out[r])[i] = v;
   } else if (OP == kOpReduceScatter) {
     const S v = fold_elem_global<DT, WT>(p, i, c);
@@ -79,11 +163,11 @@ __device__ __forceinline__ void element_op(const RingParams &p, unsigned long lo
   }
 }
 
-template <int OP, int DT, int WT>
+template <int OP, int DT, int WT, bool HD>
 __global__ void __launch_bounds__(1024) rr_simple_kernel(const __grid_constant__ RingParams p) {
   const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
   for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count; i += stride)
-    element_op<OP, DT, WT>(p, i);
+    element_op<OP, DT, WT, HD>(p, i);
 }
 
 // --------------------------------------------------------------------------
@@ -152,7 +236,7 @@ __device__ __forceinline__ unsigned long long tile_end(const RingParams &p, unsi
 }
 
 // Fold tile t (AllReduce / ReduceScatter); the result replaces slot 0.
-template <int DT, int WT>
+template <int DT, int WT, bool HD>
 __device__ __forceinline__ void compute_tile(const RingParams &p, unsigned char *stage, uint32_t slot_bytes,
                                              unsigned long long t) {
   using VT = Vec<DT, WT>;
@@ -160,8 +244,21 @@ __device__ __forceinline__ void compute_tile(const RingParams &p, unsigned char 
   const unsigned long long t0 = tile_begin(p, t), t1 = tile_end(p, t);
   const uint32_t nvec = (uint32_t)((t1 - t0) / V);
   const int L = p.L, G = p.G;
+  if constexpr (HD) {  // the same tree for every element
+    using W = typename VT::W;
+    const int E = p.hd_extra;
+    for (uint32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const uint32_t off = v * 16u;
+      auto x = [&](int r) { return VT::in(*reinterpret_cast<const uint4 *>(stage + (size_t)r * slot_bytes + off)); };
+      auto leaf = [&](int u) { return u < E ? VT::hop(x(2 * u), x(2 * u + 1)) : x(u + E); };
+      auto add = [](W a, W b) { return VT::hop(a, b); };
+      const uint4 res = VT::out(hd_fold<W>(p.hd_log2p, leaf, add));
+      *reinterpret_cast<uint4 *>(stage + off) = res;
+    }
+    return;
+  }
   const unsigned long long g0 = p.first + t0;  // global index of the tile's first element
-  const int c_first = chunk_of(g0, p.base, L), c_last = chunk_of(g0 + (t1 - t0) - 1, p.base, L);
+  const int c_first = start_rank(p, g0), c_last = start_rank(p, g0 + (t1 - t0) - 1);
   for (uint32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
     const uint32_t off = v * 16u;
     int c = c_first, c1 = c_last;
@@ -229,7 +326,7 @@ __device__ __forceinline__ void issue_stores(const RingParams &p, const unsigned
   }
 }
 
-template <int OP, int DT, int WT>
+template <int OP, int DT, int WT, bool HD>
 __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ RingParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int E = Fmt<DT>::bytes;
@@ -258,7 +355,7 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
   // The ragged end [n_bulk, count) (less than 16 bytes per rank) goes through
   // plain loads and stores in the last CTA, while its first tiles load.
   if (blockIdx.x == gridDim.x - 1)
-    for (unsigned long long i = p.n_bulk + threadIdx.x; i < p.count; i += blockDim.x) element_op<OP, DT, WT>(p, i);
+    for (unsigned long long i = p.n_bulk + threadIdx.x; i < p.count; i += blockDim.x) element_op<OP, DT, WT, HD>(p, i);
 
   long long j = 0;
   bool ok = true;
@@ -268,7 +365,7 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
     unsigned char *stage = smem + (size_t)s * stage_bytes;
     const unsigned long long t = first + (unsigned long long)j * step;
     const bool got = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
-    if (OP != kOpAllGather && got) compute_tile<DT, WT>(p, stage, slot_bytes, t);
+    if (OP != kOpAllGather && got) compute_tile<DT, WT, HD>(p, stage, slot_bytes, t);
     fence_proxy_async_smem();
     if (!__syncthreads_and(got)) {
       ok = false;
@@ -307,23 +404,31 @@ __global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long li
 // host side: one launch of (OP, DT, WT)
 // --------------------------------------------------------------------------
 
-template <int OP, int DT, int WT>
-cudaError_t launch_one(const RingParams &p, const Launch &l, cudaStream_t s) {
+template <int OP, int DT, int WT, bool HD>
+cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s) {
   if (l.path == RR_PATH_BULK) {
     static int smem_set[64] = {0};  // largest dynamic shared memory opted in, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (l.smem > 48 * 1024 && (dev >= 64 || smem_set[dev] < (int)l.smem)) {
-      e = cudaFuncSetAttribute(rr_bulk_kernel<OP, DT, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem);
+      e = cudaFuncSetAttribute(rr_bulk_kernel<OP, DT, WT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)l.smem);
       if (e != cudaSuccess) return e;
       if (dev < 64) smem_set[dev] = (int)l.smem;
     }
-    rr_bulk_kernel<OP, DT, WT><<<l.grid, l.threads, l.smem, s>>>(p);
+    rr_bulk_kernel<OP, DT, WT, HD><<<l.grid, l.threads, l.smem, s>>>(p);
   } else {
-    rr_simple_kernel<OP, DT, WT><<<l.grid, l.threads, 0, s>>>(p);
+    rr_simple_kernel<OP, DT, WT, HD><<<l.grid, l.threads, 0, s>>>(p);
   }
   return cudaGetLastError();
+}
+
+template <int OP, int DT, int WT>
+cudaError_t launch_one(const RingParams &p, const Launch &l, cudaStream_t s) {
+  if constexpr (OP == kOpAllReduce)
+    if (p.algo == kAlgoHalvingDoubling) return launch_variant<OP, DT, WT, true>(p, l, s);
+  return launch_variant<OP, DT, WT, false>(p, l, s);
 }
 
 }  // namespace rr

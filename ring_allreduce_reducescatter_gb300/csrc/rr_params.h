@@ -12,6 +12,7 @@ namespace rr {
 
 enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 enum : int { kOpAllReduce = 0, kOpReduceScatter = 1, kOpAllGather = 2 };
+enum : int { kAlgoRing = 0, kAlgoHalvingDoubling = 1, kAlgoNaive = 2 };
 
 // Device status bits (the word lives in rr_api.cu).
 enum : unsigned int { kStatusWaitTimeout = 1u };
@@ -36,6 +37,9 @@ struct RingParams {
   int tile_elems;                 // bulk path: elements per rank per tile
   int stages;                     // bulk path: pipeline depth
   int slots;                      // bulk path: tiles of one stage (R, or 1 for AllGather)
+  int algo;                       // AllReduce summation order: kAlgo*
+  int hd_log2p;                   // halving-doubling: log2 of P, the largest power of two <= R
+  int hd_extra;                   // halving-doubling: R - P ranks folded in pairs first
 };
 
 // One launch, fully resolved by the planner.

@@ -324,3 +324,19 @@ def test_host_pipeline_arguments(L):
     assert call_host(L, hin, hout, R, N, F16, ws, need, wire=BF16) == EUNSUP
     assert call_host(L, hin, hout, R, 0, F32, ws, need) == OK                # nothing to do
     assert call_host(L, hin, list(hin), R, N, F32, ws, need) not in (EINVAL, EALIAS, EUNSUP)  # in place
+
+
+def test_algo_arguments(L):
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    rr.lib()
+    ins, outs = fake(8, 100, 4)
+    call_algo = lambda algo, R=8, dt=F32, wire=F32, o=outs: L.ring_allreduce_algo(  # noqa: E731
+        ptrs(ins[:R]), ptrs(o[:R]), R, 100, dt, wire, algo, None, None)
+    assert call_algo(3) == EINVAL
+    assert call_algo(-1) == EINVAL
+    assert call_algo(1, R=0) == EINVAL
+    assert call_algo(2, dt=F16, wire=BF16) == EUNSUP
+    assert call_algo(1, o=[ins[1]] + outs[1:]) == EALIAS
+    for algo in (0, 1, 2):  # valid: validation passes and the call then needs a device
+        assert call_algo(algo) not in (EINVAL, EALIAS, EUNSUP)

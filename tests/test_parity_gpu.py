@@ -442,3 +442,45 @@ def test_host_pipeline_orders_after_prior_stream_work(rr):
     ref = oracle.allreduce([host(x) for x in dev_src], "f32")
     for r in range(R):
         assert_same(host(hout[r]), ref.outs[r], f"ordered host pipeline rank {r}")
+
+
+# --------------------------------------------------------------------------
+# the other AllReduce algorithms: halving-doubling and naive
+# --------------------------------------------------------------------------
+
+def check_algo(rr, xs, wire, algo, cfg=None, what=""):
+    outs = rr.allreduce_algo(xs, wire=wire, algo=algo, cfg=cfg)
+    torch.cuda.synchronize()
+    ref = oracle.allreduce_algo([host(x) for x in xs], NAME[xs[0].dtype], wire, algo)
+    assert ref.status == oracle.OK
+    for r in range(len(xs)):
+        assert_same(host(outs[r]), ref.outs[r], f"{what} rank {r}")
+
+
+@pytest.mark.parametrize("algo", ["hd", "naive"])
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_algorithm_grid(rr, algo, dtype, wire):
+    for R in (1, 2, 3, 4, 5, 7, 8, 12, 16, 17, 33, 64):
+        for N in (1, R + 1, 4097, 65_537):
+            xs = gen(R, N, dtype, 7 * R + N)
+            tag = f"{algo} {NAME[dtype]}/{wire} R={R} N={N}"
+            check_algo(rr, xs, wire, algo, what=tag)
+            check_algo(rr, xs, wire, algo, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+            if N * xs[0].element_size() >= 16 and R <= 16:
+                check_algo(rr, xs, wire, algo, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=256), what=tag + " bulk256")
+
+
+@pytest.mark.parametrize("algo", ["hd", "naive"])
+def test_algorithm_full_size_sampled(rr, wl, algo):
+    xs = wl.inputs(wl.config2(512), "cuda")
+    outs = rr.allreduce_algo(xs, algo=algo)
+    torch.cuda.synchronize()
+    N = xs[0].numel()
+    idx = sample_indices(N, 8)
+    ti = torch.from_numpy(idx).cuda()
+    want = oracle.fold_gathered_algo([host(x[ti]) for x in xs], idx.astype(np.uint64), N, "f16", None, algo)
+    for r in range(8):
+        assert_same(host(outs[r][ti]), want, f"{algo} 512 MiB sampled rank {r}")
+        assert torch.equal(outs[r].view(torch.int16), outs[0].view(torch.int16))
+    del outs, xs
+    torch.cuda.empty_cache()
