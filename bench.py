@@ -67,10 +67,15 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+DEVICE_SOURCES = ("rr_kernels.cuh", "rr_device.cuh", "rr_params.h", "rr_inst_f32.cu", "rr_inst_f16.cu",
+                  "rr_inst_bf16.cu")
+
+
 def kernel_sources_digest():
+    """Digest of the device code (the kernels, not the host-side planner)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "ring_allreduce_reducescatter_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in DEVICE_SOURCES:
+        with open(os.path.join(ROOT, "ring_allreduce_reducescatter_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -158,6 +163,52 @@ def combine_ranks(pg, local_ms, device=None):
 def job_throughput(world, msg_bytes, ms_per_step):
     """Whole-job algbw (GB/s): every replica moves msg_bytes per rank per step."""
     return world * msg_bytes / (ms_per_step * 1e-3) / 1e9
+
+
+def parse_cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def bind_to_gpu_local_cpus(props, gpu_id):
+    """Run this process on the CPUs attached to the GPU's PCI root, so that
+    page-locked host buffers land in the memory next to the GPU's host link.
+    Returns a short description, or None when the topology is not readable."""
+    addr = None
+    if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+        addr = f"{props.pci_domain_id:04x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    else:
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(gpu_id), "--query-gpu=pci.bus_id",
+                                  "--format=csv,noheader"], capture_output=True, text=True, timeout=30).stdout
+            bus = out.strip().lower()
+            if bus:
+                dom, rest = bus.split(":", 1)
+                addr = f"{int(dom, 16) & 0xffff:04x}:{rest}"
+        except (OSError, ValueError, subprocess.SubprocessError):
+            return None
+    if not addr:
+        return None
+    base = f"/sys/bus/pci/devices/{addr}"
+    try:
+        with open(f"{base}/local_cpulist") as f:
+            cpus = parse_cpulist(f.read())
+        node = open(f"{base}/numa_node").read().strip() if os.path.exists(f"{base}/numa_node") else "?"
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return f"{len(cpus)} CPUs local to GPU {addr} (NUMA node {node})"
+    except (OSError, ValueError):
+        return None
 
 
 def dist_setup():
@@ -250,6 +301,126 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring"):
     return row
 
 
+def bucket_set_row(rr, wl, dev, peak):
+    """Workload 5 whole: the 49 gradient buckets of the decoder, all resident
+    (one flat in-place vector per rank, about 104 GB), reduced bucket by bucket
+    in place as data-parallel training does; timed over one pass."""
+    import torch
+
+    counts = wl.decoder_bucket_counts()
+    total = sum(counts)
+    R_ = 8
+    flat = [torch.empty(total, dtype=torch.bfloat16, device=dev) for _ in range(R_)]
+    for r in range(R_):  # seeded per rank and bucket (workload 5's recipe)
+        off = 0
+        for b, n in enumerate(counts):
+            wl.rank_values(5, r, n, torch.bfloat16, "grad1e-2", dev, bucket=b, out=flat[r][off:off + n])
+            off += n
+    views, off = [], 0
+    for n in counts:
+        views.append([f[off:off + n] for f in flat])
+        off += n
+
+    def one_pass():
+        for v in views:
+            rr.allreduce(v, outs=v)
+
+    one_pass()  # warm-up (and in place: the values grow, the timing does not care)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    one_pass()
+    b.record()
+    torch.cuda.synchronize(dev)
+    t_ms = a.elapsed_time(b)
+    msg = total * 2
+    row = {"workload": f"fusion buckets: {len(counts)} bf16 buckets of a 32-layer 4096-hidden decoder, "
+                       f"R=8, in place, all resident", "op": "allreduce", "R": R_, "count": total,
+           "buckets": len(counts), "msg_bytes": msg, "ms": round(t_ms, 3),
+           "algbw_gbs": round(msg / t_ms / 1e6, 2), "hbm_gbs": round(2 * R_ * msg / t_ms / 1e6, 1),
+           "roofline_frac": round(2 * R_ * msg / t_ms / 1e6 / peak, 4), "gpu_launches": len(counts)}
+    del views, flat
+    torch.cuda.empty_cache()
+    return row
+
+
+def overlap_row(rr, wl, dev, pieces=8, max_ctas=0):
+    """Chunked AllReduce overlapped with compute (the pattern of the page
+    bjdmk.com.cn/news/5966809, sections 4.2-4.3): `pieces` bf16 GEMMs run on the
+    compute stream; after each one an event releases one range of a 512 MiB
+    fp16 AllReduce (R = 8) on a communication stream.  Reports the two
+    streams alone and together."""
+    import torch
+
+    w = wl.config2(512)
+    xs = wl.inputs(w, dev)
+    outs = [torch.empty_like(x) for x in xs]
+    N = w.count
+    step = -(-N // pieces) // 256 * 256
+    n = 8192
+    A = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    B = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    C = torch.empty(n, n, device=dev, dtype=torch.bfloat16)
+    comp, comm = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    evs = [torch.cuda.Event() for _ in range(pieces)]
+
+    def ranges(k):
+        a = k * step
+        b = min(N, a + step)
+        return a, b
+
+    def compute_only():
+        with torch.cuda.stream(comp):
+            for _ in range(pieces):
+                torch.matmul(A, B, out=C)
+
+    cfg = rr.LaunchCfg(0, 0, 0, 0, 0, max_ctas)
+
+    def comm_only():
+        for k in range(pieces):
+            a, b = ranges(k)
+            rr.allreduce_range([x[a:b] for x in xs], [o[a:b] for o in outs], N, a, stream=comm, cfg=cfg)
+
+    def both():
+        for k in range(pieces):
+            with torch.cuda.stream(comp):
+                torch.matmul(A, B, out=C)
+                evs[k].record(comp)
+            comm.wait_event(evs[k])
+            a, b = ranges(k)
+            rr.allreduce_range([x[a:b] for x in xs], [o[a:b] for o in outs], N, a, stream=comm, cfg=cfg)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        best = None
+        for _ in range(3):
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            cur = torch.cuda.current_stream(dev)
+            t0.record(cur)
+            comp.wait_stream(cur)
+            comm.wait_stream(cur)
+            fn()
+            cur.wait_stream(comp)
+            cur.wait_stream(comm)
+            t1.record(cur)
+            torch.cuda.synchronize(dev)
+            ms = t0.elapsed_time(t1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    t_comp, t_comm, t_both = timed(compute_only), timed(comm_only), timed(both)
+    hidden = (t_comp + t_comm - t_both) / min(t_comp, t_comm)
+    del xs, outs, A, B, C
+    torch.cuda.empty_cache()
+    return {"what": f"{pieces} bf16 GEMMs {n}^3 on a compute stream; after each, one of {pieces} ranges of the "
+                    f"512 MiB R=8 fp16 AllReduce on a communication stream", "max_ctas": max_ctas,
+            "compute_ms": round(t_comp, 3),
+            "allreduce_ms": round(t_comm, 3), "together_ms": round(t_both, 3),
+            "serial_ms": round(t_comp + t_comm, 3), "fraction_of_shorter_hidden": round(hidden, 3)}
+
+
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
@@ -279,6 +450,9 @@ def run_ours(args):
 
     props = torch.cuda.get_device_properties(dev)
     l2_bytes = int(getattr(props, "L2_cache_size", 128 * MIB))
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (uuid or local)
+    affinity = bind_to_gpu_local_cpus(props, gpu_id)
     w = wl.config2(args.msg_mib)
     N = w.count
     msg = N * 2
@@ -295,8 +469,6 @@ def run_ours(args):
     if rr.device_status() != 0:
         raise RuntimeError("device status set during warm-up")
 
-    gpu_id = getattr(props, "uuid", None)
-    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else (gpu_id or local)
     sampler = ClockSampler(gpu_id) if local == 0 else None
     time.sleep(0.5 if sampler else 0)
 
@@ -337,7 +509,7 @@ def run_ours(args):
     # the size sweep and the other workloads: CUDA-graph replay of back-to-back
     # launches over rotating buffer sets at least 3x the L2 size, so every
     # launch reads inputs that are not in L2 and no host time is included
-    sweep, table = [], []
+    sweep, table, overlap = [], [], None
     if not args.no_sweep:
         del outs
         torch.cuda.empty_cache()
@@ -345,13 +517,18 @@ def run_ours(args):
             sweep.append(graph_row(rr, wl, wl.config2(mib), dev, l2_bytes, peak, args.sweep_iters))
         torch.cuda.empty_cache()
         if not args.no_workloads:
-            for w in (wl.config1("allreduce"), wl.config1("reduce_scatter"), wl.config1("allgather"), wl.config3(),
-                      wl.config4(), wl.config5(0), wl.config2(512, wire="f32")):
-                table.append(graph_row(rr, wl, w, dev, l2_bytes, peak, args.sweep_iters))
+            for wk in (wl.config1("allreduce"), wl.config1("reduce_scatter"), wl.config1("allgather"), wl.config3(),
+                       wl.config4(), wl.config5(0), wl.config2(512, wire="f32")):
+                table.append(graph_row(rr, wl, wk, dev, l2_bytes, peak, args.sweep_iters))
                 torch.cuda.empty_cache()
             for algo in ("hd", "naive"):
                 table.append(graph_row(rr, wl, wl.config2(512), dev, l2_bytes, peak, args.sweep_iters, algo=algo))
                 torch.cuda.empty_cache()
+            del xs
+            torch.cuda.empty_cache()
+            table.append(bucket_set_row(rr, wl, dev, peak))
+            overlap = [overlap_row(rr, wl, dev, max_ctas=m) for m in (0, 128, 96)]
+            xs = wl.inputs(w, dev)
         outs = [torch.empty_like(x) for x in xs]
 
     # end to end through the C ABI's host-buffer entry point (ring_allreduce_host):
@@ -387,7 +564,7 @@ def run_ours(args):
         e2e = {"value": round(job_throughput(world, msg, e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": R * msg, "d2h_bytes_per_step": R * msg, "ms_per_step": round(e_ms, 4),
                "steps": args.e2e_steps, "api": "ring_allreduce_host",
-               "piece_mib_per_rank": args.e2e_piece_mib}
+               "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity}
         del host_in, host_out, ws
         outs = [torch.empty_like(x) for x in xs]
 
@@ -415,7 +592,7 @@ def run_ours(args):
                          "kernel_ms": round(kern_ms, 5), "algorithmic_bytes_per_launch": 2 * R * msg},
             "busbw_gbs": round(value / world * 2 * (R - 1) / R, 3),
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
-            "sweep": sweep, "workloads": table, "kernel_sources": digest,
+            "sweep": sweep, "workloads": table, "overlap": overlap, "kernel_sources": digest,
         }
         print(json.dumps(line), flush=True)
     if pg:

@@ -134,9 +134,13 @@ typedef enum { RR_PATH_AUTO = 0, RR_PATH_BULK = 1, RR_PATH_SIMPLE = 2 } rr_path;
 typedef struct {
   int path;        /* rr_path */
   int tile_bytes;  /* bulk path: bytes per rank per tile, a multiple of 16 */
-  int stages;      /* bulk path: tiles in flight per CTA, 2..8 */
+  int stages;      /* bulk path: tiles in flight per CTA, 2..16 */
   int ctas_per_sm; /* bulk path: 1..4 */
   int threads;     /* threads per CTA: 64..1024, a multiple of 32 */
+  int max_ctas;    /* at most this many CTAs (0: no limit); a chunked AllReduce
+                      that runs beside compute kernels can leave them SMs.
+                      With fewer CTAs than 3 per SM and no stages / CTAs-per-SM
+                      given, each CTA takes a whole SM with larger tiles. */
 } rr_launch_cfg;
 
 /*

@@ -48,6 +48,8 @@ rr_status current_device(DeviceInfo *out) {
   return RR_OK;
 }
 
+constexpr int kMaxStages = 16;  // pipeline depth limit of the bulk path
+
 size_t elem_bytes(int t) { return t == RR_FP32 ? 4 : 2; }
 bool valid_type(int t) { return t == RR_FP32 || t == RR_FP16 || t == RR_BF16; }
 
@@ -89,10 +91,11 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
     if (cfg->path < RR_PATH_AUTO || cfg->path > RR_PATH_SIMPLE) return RR_ERR_INVALID_ARG;
     if (cfg->tile_bytes != 0 && (cfg->tile_bytes < 16 || cfg->tile_bytes % 16 != 0 || cfg->tile_bytes > (1 << 20)))
       return RR_ERR_INVALID_ARG;
-    if (cfg->stages != 0 && (cfg->stages < 2 || cfg->stages > 8)) return RR_ERR_INVALID_ARG;
+    if (cfg->stages != 0 && (cfg->stages < 2 || cfg->stages > kMaxStages)) return RR_ERR_INVALID_ARG;
     if (cfg->ctas_per_sm != 0 && (cfg->ctas_per_sm < 1 || cfg->ctas_per_sm > 4)) return RR_ERR_INVALID_ARG;
     if (cfg->threads != 0 && (cfg->threads < 64 || cfg->threads > 1024 || cfg->threads % 32 != 0))
       return RR_ERR_INVALID_ARG;
+    if (cfg->max_ctas < 0) return RR_ERR_INVALID_ARG;
   }
   ck->op = op;
   ck->R = R;
@@ -167,10 +170,11 @@ unsigned round16_down(unsigned long long x) { return (unsigned)(x & ~15ull); }
 // vectors need it) and every shared-memory size fits the device.
 rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int smem_per_sm, int smem_optin,
                       rr::RingParams *p, rr::Launch *l) {
-  const rr_launch_cfg zero = {0, 0, 0, 0, 0};
+  const rr_launch_cfg zero = {0, 0, 0, 0, 0, 0};
   const rr_launch_cfg &c = cfg ? *cfg : zero;
   const size_t E = ck.E;
   const unsigned long long N = ck.n;  // elements of this launch
+  auto capped = [&](int grid) { return (c.max_ctas > 0 && grid > c.max_ctas) ? c.max_ctas : grid; };
   if (sms < 1 || smem_per_sm < 1 || smem_optin < 1) return RR_ERR_INVALID_ARG;
 
   p->count = N;
@@ -203,7 +207,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   if (path == RR_PATH_SIMPLE) {
     const unsigned long long blocks = (N + l->threads - 1) / l->threads;
     const unsigned long long cap = (unsigned long long)sms * 8;
-    l->grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+    l->grid = capped((int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap));
     l->smem = 0;
     l->ctas_per_sm = 0;
     p->n_bulk = 0;
@@ -222,9 +226,21 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     return b > smem_optin ? (long long)smem_optin : b;
   };
 
+  // A grid capped below 3 CTAs per SM (say, beside compute kernels) gives every
+  // CTA its own SM; one issuing thread per SM then needs larger bulk copies to
+  // keep its SM's bandwidth (measured: 96 capped CTAs reached 0.77 of the full
+  // bandwidth with 8 KB tiles, 0.46 with 2 KB tiles).
+  const bool few_ctas = c.max_ctas > 0 && (unsigned long long)c.max_ctas < 3ull * (unsigned long long)sms &&
+                        c.ctas_per_sm == 0 && c.stages == 0;
+
   // Tile: 16 KB per stage across the slots, at least 2 KB per rank (smaller
   // bulk copies lose bandwidth), shrunk only when two stages do not fit one CTA.
   unsigned long long tile = (unsigned long long)c.tile_bytes;
+  if (tile == 0 && few_ctas) {
+    tile = 8192;
+    while (tile > 2048 && 3ull * (tile * slots + 8) > (unsigned long long)budget_for(1)) tile /= 2;
+    while (tile > 16 && 2ull * (tile * slots + 8) > (unsigned long long)budget_for(1)) tile = round16_down(tile / 2);
+  }
   if (tile == 0) {
     tile = round16_down(16384 / slots);
     if (tile < 2048) tile = 2048;
@@ -240,7 +256,10 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   // more bulk copies in flight than one deep pipeline: prefer 3 CTAs of 3
   // stages.  A message with at most 4 tiles per SM gets one CTA per tile.
   int ctas = c.ctas_per_sm, stages = c.stages;
-  if (ctas == 0 && stages == 0 && n_tiles <= 4ull * (unsigned long long)sms) {
+  if (few_ctas) {
+    ctas = 1;
+    stages = clamp_int((int)((unsigned long long)budget_for(1) / (stage_bytes + 8)), 2, 3);
+  } else if (ctas == 0 && stages == 0 && n_tiles <= 4ull * (unsigned long long)sms) {
     ctas = (int)((n_tiles + sms - 1) / sms);
     if (ctas < 1) ctas = 1;
     while (ctas > 1 && 2ull * (stage_bytes + 8) > (unsigned long long)budget_for(ctas)) --ctas;
@@ -262,12 +281,16 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   if (smem > (unsigned long long)budget) return RR_ERR_UNSUPPORTED;
 
   p->tile_elems = (int)(tile / E);
+  // store groups left in flight before a stage is refilled: deep pipelines
+  // split their stages between loads and stores
+  p->store_lag = stages >= 5 ? (stages - 1) / 2 : 1;
+  if (p->store_lag > 8) p->store_lag = 8;
   p->n_bulk = n_bulk;
   p->n_tiles = (n_bulk + p->tile_elems - 1) / p->tile_elems;
   p->stages = stages;
   p->slots = slots;
   const unsigned long long cap = (unsigned long long)sms * ctas;
-  l->grid = (int)(p->n_tiles < cap ? p->n_tiles : cap);
+  l->grid = capped((int)(p->n_tiles < cap ? p->n_tiles : cap));
   l->smem = (size_t)smem;
   l->ctas_per_sm = ctas;
   return RR_OK;
@@ -291,6 +314,7 @@ void export_plan(const rr::RingParams &p, const rr::Launch &l, size_t E, rr_laun
   chosen->stages = l.path == RR_PATH_BULK ? p.stages : 0;
   chosen->ctas_per_sm = l.ctas_per_sm;
   chosen->threads = l.threads;
+  chosen->max_ctas = l.grid;
 }
 
 // Plan and launch a validated collective on the current device.
@@ -495,7 +519,7 @@ rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs,
   Checked ck;
   rr_status st = check_args(op, in_bufs, out_bufs, R, count, dtype, wire, group_size, cfg, &ck);
   if (st != RR_OK) return st;
-  *chosen = rr_launch_cfg{RR_PATH_SIMPLE, 0, 0, 0, 0};
+  *chosen = rr_launch_cfg{RR_PATH_SIMPLE, 0, 0, 0, 0, 0};
   if (count == 0) return RR_OK;
   DeviceInfo dev;
   st = current_device(&dev);

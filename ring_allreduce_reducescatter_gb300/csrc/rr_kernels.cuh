@@ -27,8 +27,9 @@
 //    completion counted on an mbarrier); all threads fold 16-byte vectors out
 //    of shared memory and write the result over slot 0 of the stage; thread 0
 //    then writes slot 0 to the outputs with bulk asynchronous stores and
-//    refills the previous stage.  Loads of S-1 tiles stay in flight while a
-//    tile is folded.  Every wait is bounded.
+//    refills the stage of the tile D steps back once its stores have read
+//    shared memory (D = store_lag): D + 1 tiles of stores and S - D - 1 tiles
+//    of loads stay in flight while a tile is folded.  Every wait is bounded.
 #pragma once
 
 #include "rr_device.cuh"
@@ -374,12 +375,13 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
     if (threadIdx.x == 0) {
       issue_stores<OP, DT>(p, stage, t, pol);
       bulk_commit();
-      // refill the stage of tile j-1 once its stores have read shared memory
-      if (j >= 1 && j - 1 + S < n_local) {
-        bulk_wait_read<1>();
-        const int sp = (int)((j - 1) % S);
+      // refill the stage of tile j-D once its stores have read shared memory
+      const int D = p.store_lag;
+      if (j >= D && j - D + S < n_local) {
+        bulk_wait_read_upto(D);
+        const int sp = (int)((j - D) % S);
         issue_loads<OP, DT>(p, smem + (size_t)sp * stage_bytes, slot_bytes, &full[sp],
-                            first + (unsigned long long)(j - 1 + S) * step, pol);
+                            first + (unsigned long long)(j - D + S) * step, pol);
       }
     }
   }
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
     if (!ok) {
       atomicOr(p.status, kStatusWaitTimeout);
       // let the loads still in flight land before the shared memory is released
-      long long issued_end = (j >= 1 ? j - 1 : 0) + S;
+      long long issued_end = (j >= p.store_lag ? j - p.store_lag : 0) + S;
       if (issued_end > n_local) issued_end = n_local;
       for (long long u = j; u < issued_end; ++u)
         mbar_wait_bounded(&full[u % S], (uint32_t)((u / S) & 1), kWaitLimitNs);

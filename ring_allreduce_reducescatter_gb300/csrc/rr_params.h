@@ -36,6 +36,7 @@ struct RingParams {
   int G;                          // groups, R / L
   int tile_elems;                 // bulk path: elements per rank per tile
   int stages;                     // bulk path: pipeline depth
+  int store_lag;                  // bulk path: store groups left in flight before a stage is refilled (1..8)
   int slots;                      // bulk path: tiles of one stage (R, or 1 for AllGather)
   int algo;                       // AllReduce summation order: kAlgo*
   int hd_log2p;                   // halving-doubling: log2 of P, the largest power of two <= R

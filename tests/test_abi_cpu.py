@@ -176,7 +176,7 @@ def test_bad_launch_cfg(L):
     ins, outs = fake(4, 100, 4)
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(3, 0, 0, 0, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 24, 0, 0, 0)) == EINVAL
-    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 9, 0, 0)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 17, 0, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 1, 0, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 0, 5, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 0, 0, 1000)) == EINVAL
@@ -242,7 +242,7 @@ def test_planner_invariants_every_rank_count(L):
                             slots = 1 if op == AG else R
                             tile = ch["tile_bytes"]
                             assert tile >= 16 and tile % 16 == 0 and tile % E == 0, (R, N, tile)
-                            assert 2 <= ch["stages"] <= 8
+                            assert 2 <= ch["stages"] <= 16
                             assert smem == ch["stages"] * (tile * slots + 8)
                             assert smem <= min(GB300["optin"], GB300["smem_per_sm"] // ch["ctas_per_sm"] - 1024)
                             assert grid <= GB300["sms"] * ch["ctas_per_sm"]
@@ -340,3 +340,17 @@ def test_algo_arguments(L):
     assert call_algo(1, o=[ins[1]] + outs[1:]) == EALIAS
     for algo in (0, 1, 2):  # valid: validation passes and the call then needs a device
         assert call_algo(algo) not in (EINVAL, EALIAS, EUNSUP)
+
+
+def test_max_ctas_caps_the_grid(L):
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 28, F16)
+    assert st == OK and grid == 456
+    st, ch, grid, smem = plan_dev(L, AR, 8, 1 << 28, F16, cfg=(0, 0, 0, 0, 0, 40))
+    assert st == OK and grid == 40 and ch["max_ctas"] == 40
+    # a capped grid gets one CTA per SM with larger tiles
+    assert ch["ctas_per_sm"] == 1 and ch["tile_bytes"] == 8192 and ch["stages"] == 3 and smem <= GB300["optin"]
+    st, ch, _, smem = plan_dev(L, AR, 16, 1 << 26, F32, cfg=(0, 0, 0, 0, 0, 64))
+    assert st == OK and ch["tile_bytes"] == 4096 and smem <= GB300["optin"]
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 10, F16, aligned=0, cfg=(0, 0, 0, 0, 0, 3))
+    assert st == OK and grid == 3 and ch["path"] == 2
+    assert plan_dev(L, AR, 8, 1 << 20, F16, cfg=(0, 0, 0, 0, 0, -1))[0] == EINVAL

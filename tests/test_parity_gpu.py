@@ -484,3 +484,14 @@ def test_algorithm_full_size_sampled(rr, wl, algo):
         assert torch.equal(outs[r].view(torch.int16), outs[0].view(torch.int16))
     del outs, xs
     torch.cuda.empty_cache()
+
+
+def test_capped_grids(rr):
+    # a persistent grid of a few CTAs walks many tiles each; same bits
+    for dtype, wire in PAIRS[:4]:
+        xs = gen(8, 300_007, dtype, 99)
+        for cap in (1, 7, 100):
+            check_ar(rr, xs, wire, cfg=cfg_of(rr) if cap == 0 else rr.LaunchCfg(0, 0, 0, 0, 0, cap),
+                     what=f"max_ctas={cap} {NAME[dtype]}/{wire}")
+            check_ar(rr, xs, wire, cfg=rr.LaunchCfg(rr.PATH_SIMPLE, 0, 0, 0, 0, cap),
+                     what=f"simple max_ctas={cap} {NAME[dtype]}/{wire}")
