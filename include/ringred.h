@@ -29,7 +29,9 @@
  * the wire format (round to nearest even; no fused multiply-add; subnormals
  * kept).  With a binary32 wire the hop is the binary32 addition.  On a 16-bit
  * wire with binary32 storage, every input is first rounded to the wire format
- * and the result is widened back exactly.  The result is the same on every
+ * and the result is widened back exactly; with 16-bit storage on a binary32
+ * wire, every input is widened exactly and the result rounded once.  The
+ * result is the same on every
  * GPU and every launch configuration: it depends only on the inputs, R, L,
  * count and the formats.
  *
@@ -93,9 +95,12 @@ rr_status ring_allreduce(const void *const *in_bufs, void *const *out_bufs, int 
 
 /*
  * ring_allreduce_ex -- ring_allreduce with a wire format and a two-level ring.
- * wire: RR_FP32 only for RR_FP32 storage, or the storage type itself, or a
- *   16-bit wire under RR_FP32 storage ([p5] FP16 communication).  Supported
- *   (dtype, wire): (FP32,FP32) (FP16,FP16) (BF16,BF16) (FP32,BF16) (FP32,FP16).
+ * wire: the storage type itself; a 16-bit wire under RR_FP32 storage ([p5]
+ *   FP16 communication: inputs rounded to the wire, every hop rounded); or
+ *   RR_FP32 under 16-bit storage ([p5] FP16/FP32 mixed precision: inputs
+ *   widened exactly, hops in binary32, one rounding to the storage format at
+ *   the end).  Supported (dtype, wire): (FP32,FP32) (FP16,FP16) (BF16,BF16)
+ *   (FP32,BF16) (FP32,FP16) (FP16,FP32) (BF16,FP32).
  * group_size: L, ranks per group ([p5] "通信拓扑与带宽利用率"); 0 or R = the
  *   flat ring; otherwise L must divide R, and group g holds ranks gL..gL+L-1.
  */
@@ -126,9 +131,12 @@ rr_status ring_allgather(const void *const *in_bufs, void *const *out_bufs, int 
 
 /* Launch paths: RR_PATH_BULK stages tiles through shared memory with bulk
  * asynchronous copies (needs 16-byte aligned buffers, and for ReduceScatter /
- * AllGather chunk offsets that are multiples of 16 bytes); RR_PATH_SIMPLE is
- * one element per thread with plain loads and stores (any alignment). */
-typedef enum { RR_PATH_AUTO = 0, RR_PATH_BULK = 1, RR_PATH_SIMPLE = 2 } rr_path;
+ * AllGather chunk offsets that are multiples of 16 bytes); RR_PATH_DIRECT has
+ * every thread load its ranks' 16-byte vectors straight from global memory
+ * and store the results straight back (the same alignment needs, at most 256
+ * threads per CTA; one memory round trip, for small messages); RR_PATH_SIMPLE
+ * is one element per thread with plain loads and stores (any alignment). */
+typedef enum { RR_PATH_AUTO = 0, RR_PATH_BULK = 1, RR_PATH_SIMPLE = 2, RR_PATH_DIRECT = 3 } rr_path;
 
 /* Optional launch configuration; zero fields mean "choose automatically". */
 typedef struct {

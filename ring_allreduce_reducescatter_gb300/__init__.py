@@ -19,7 +19,7 @@ __all__ = [
     "allreduce_range", "allreduce_host", "allreduce_host_static", "host_workspace_bytes", "allreduce_algo",
     "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
-    "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE",
+    "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE", "PATH_DIRECT",
 ]
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_DIR, "libringred.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT = range(6)
 OP_ALLREDUCE, OP_REDUCE_SCATTER, OP_ALLGATHER = 0, 1, 2
-PATH_AUTO, PATH_BULK, PATH_SIMPLE = 0, 1, 2
+PATH_AUTO, PATH_BULK, PATH_SIMPLE, PATH_DIRECT = 0, 1, 2, 3
 FP32, FP16, BF16 = 0, 1, 2
 
 _TORCH_CODE = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}

@@ -88,7 +88,7 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
   if (L < 1 || L > R || R % L != 0) return RR_ERR_INVALID_ARG;
   if (op != RR_OP_ALLREDUCE && L != R) return RR_ERR_INVALID_ARG;
   if (cfg) {
-    if (cfg->path < RR_PATH_AUTO || cfg->path > RR_PATH_SIMPLE) return RR_ERR_INVALID_ARG;
+    if (cfg->path < RR_PATH_AUTO || cfg->path > RR_PATH_DIRECT) return RR_ERR_INVALID_ARG;
     if (cfg->tile_bytes != 0 && (cfg->tile_bytes < 16 || cfg->tile_bytes % 16 != 0 || cfg->tile_bytes > (1 << 20)))
       return RR_ERR_INVALID_ARG;
     if (cfg->stages != 0 && (cfg->stages < 2 || cfg->stages > kMaxStages)) return RR_ERR_INVALID_ARG;
@@ -164,6 +164,24 @@ int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
 unsigned round16_down(unsigned long long x) { return (unsigned)(x & ~15ull); }
 
+// Which of the two 16-byte-aligned paths is faster, from a measured sweep of
+// both (R = 2 .. 32, 1 MiB .. 512 MiB per rank, every collective; CUDA-graph
+// replay over inputs colder than L2).  The direct path keeps eight loads in
+// flight per thread and needs no barriers: it wins for small messages, for
+// every ReduceScatter with R >= 3 and for every AllReduce with R >= 8.  The
+// tile pipeline wins for two ranks, for 3..7 ranks between 2 and 64 MiB, for
+// AllGather with 16 or more ranks above 1 MiB, and for capped grids (each CTA
+// then owns an SM and moves 8 KB per bulk copy).
+bool prefer_direct(int op, int R, unsigned long long msg_bytes, int max_ctas) {
+  const unsigned long long MiB = 1ull << 20;
+  if (max_ctas > 0) return false;
+  if (op == RR_OP_ALLGATHER) return R < 16 || msg_bytes <= MiB;
+  if (op == RR_OP_REDUCE_SCATTER) return R >= 3;
+  if (R <= 2) return false;
+  if (R < 8) return msg_bytes <= MiB || msg_bytes >= 64 * MiB;
+  return true;
+}
+
 // Resolve the launch: path, tiles, stages, grid.  Fills every field of *p
 // except the buffer pointers and the status word.  Every tile size it picks is
 // a multiple of 16 bytes (the bulk copies and the 16-byte shared-memory
@@ -199,11 +217,34 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   const unsigned long long n_bulk = (N * E / 16) * 16 / E;
   const bool bulk_ok = ck.all_16b_aligned && chunks_aligned && n_bulk > 0;
   int path = c.path;
-  if (path == RR_PATH_BULK && !bulk_ok) return RR_ERR_UNSUPPORTED;
-  if (path == RR_PATH_AUTO) path = bulk_ok ? RR_PATH_BULK : RR_PATH_SIMPLE;
+  if ((path == RR_PATH_BULK || path == RR_PATH_DIRECT) && !bulk_ok) return RR_ERR_UNSUPPORTED;
+  if (path == RR_PATH_AUTO)
+    path = !bulk_ok ? RR_PATH_SIMPLE
+                    : (prefer_direct(ck.op, ck.R, (unsigned long long)ck.count * E, c.max_ctas) ? RR_PATH_DIRECT
+                                                                                                : RR_PATH_BULK);
 
   l->path = path;
   l->threads = c.threads ? c.threads : 256;
+  if (path == RR_PATH_DIRECT) {  // U 16-byte vectors per thread
+    if (l->threads > 256) return RR_ERR_UNSUPPORTED;
+    // eight loads in flight per thread: few ranks per group take several vectors
+    int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 2 ? 4 : ck.L <= 4 ? 2 : 1);
+    if (U > 2 && ck.dtype != RR_FP32 && ck.wire == RR_FP32) U = 2;  // binary32 accumulators are twice as wide
+    p->direct_u = U;
+    const unsigned long long vecs = n_bulk * E / 16;
+    const unsigned long long blocks = (vecs + (unsigned long long)l->threads * U - 1) / ((unsigned long long)l->threads * U);
+    const unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);
+    l->grid = capped((int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap));
+    l->smem = 0;
+    l->ctas_per_sm = 0;
+    p->n_bulk = n_bulk;
+    p->n_tiles = 0;
+    p->tile_elems = 0;
+    p->stages = 0;
+    p->slots = 0;
+    p->store_lag = 0;
+    return RR_OK;
+  }
   if (path == RR_PATH_SIMPLE) {
     const unsigned long long blocks = (N + l->threads - 1) / l->threads;
     const unsigned long long cap = (unsigned long long)sms * 8;

@@ -248,6 +248,25 @@ __device__ __forceinline__ unsigned long long chunk_end(int c, unsigned long lon
 }
 
 // --------------------------------------------------------------------------
+// 16-byte global accesses of the direct path: loads through the read-only
+// path without an L1 allocation (every byte is read once), stores marked as
+// streaming.  A thread only ever rereads what it wrote itself.
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void stg_stream(void *p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// --------------------------------------------------------------------------
 // PTX: mbarrier, bulk asynchronous copies, L2 policy, timer
 // --------------------------------------------------------------------------
 

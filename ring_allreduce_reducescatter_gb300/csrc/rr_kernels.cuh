@@ -398,6 +398,111 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
   }
 }
 
+// --------------------------------------------------------------------------
+// direct path: every thread takes U 16-byte vectors (a grid-stride apart) per
+// iteration, loads them straight from the ranks' buffers in batches of 8 / U
+// ranks (so eight 16-byte loads are in flight per thread whatever R is), folds
+// them in registers in the ring's order and stores the results straight to
+// the outputs: one DRAM round trip per vector, no shared memory, no barriers
+// --------------------------------------------------------------------------
+
+constexpr int kDirectThreads = 256;
+
+template <int OP, int DT, int WT, bool HD, int U>
+__global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __grid_constant__ RingParams p) {
+  using VT = Vec<DT, WT>;
+  using W = typename VT::W;
+  constexpr int V = VT::V;
+  constexpr int E = Fmt<DT>::bytes;
+  constexpr int NB = 8 / U;  // ranks per batch of loads
+  const unsigned long long nvec = p.n_bulk / V;
+  const unsigned long long T = (unsigned long long)gridDim.x * blockDim.x;
+  for (unsigned long long v0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < nvec; v0 += T * U) {
+    if constexpr (OP == kOpAllGather || HD) {
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const unsigned long long v = v0 + (unsigned long long)k * T;
+        if (v >= nvec) break;
+        const unsigned long long i0 = v * V, g0 = p.first + i0, boff = i0 * E;
+        if constexpr (OP == kOpAllGather) {
+          const int c = chunk_of(g0, p.base, p.L);
+          if (c != chunk_of(g0 + V - 1, p.base, p.L)) {
+            for (int e = 0; e < V; ++e) element_op<OP, DT, WT, HD>(p, i0 + e);
+            continue;
+          }
+          const uint4 val =
+              ldg_stream(static_cast<const unsigned char *>(p.in[c]) + (i0 - (unsigned long long)c * p.base) * E);
+          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, val);
+        } else {  // halving-doubling AllReduce
+          const int Ex = p.hd_extra;
+          auto x = [&](int r) { return VT::in(ldg_stream(static_cast<const unsigned char *>(p.in[r]) + boff)); };
+          auto leaf = [&](int u) { return u < Ex ? VT::hop(x(2 * u), x(2 * u + 1)) : x(u + Ex); };
+          auto add = [](W a, W b) { return VT::hop(a, b); };
+          const uint4 res = VT::out(hd_fold<W>(p.hd_log2p, leaf, add));
+          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, res);
+        }
+      }
+    } else {  // ring / naive fold, AllReduce or ReduceScatter
+      unsigned long long boff[U];
+      int c[U];
+      bool live[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const unsigned long long v = v0 + (unsigned long long)k * T;
+        live[k] = v < nvec;
+        boff[k] = v * V * E;
+        c[k] = 0;
+        if (live[k]) {
+          const unsigned long long g0 = p.first + v * V;
+          c[k] = start_rank(p, g0);
+          if (c[k] != start_rank(p, g0 + V - 1)) {  // straddles a chunk boundary: element by element
+            for (int e = 0; e < V; ++e) element_op<OP, DT, WT, HD>(p, v * V + e);
+            live[k] = false;
+          }
+        }
+      }
+      const int L = p.L;
+      W total[U];
+      for (int g = 0; g < p.G; ++g) {
+        W acc[U];
+        for (int k0 = 0; k0 < L; k0 += NB) {
+          uint4 x[U][NB];
+#pragma unroll
+          for (int k = 0; k < U; ++k)
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+              if (live[k] && k0 + j < L) {
+                int r = c[k] + k0 + j;
+                r -= (r >= L) ? L : 0;
+                x[k][j] = ldg_stream(static_cast<const unsigned char *>(p.in[g * L + r]) + boff[k]);
+              }
+#pragma unroll
+          for (int k = 0; k < U; ++k)
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+              if (live[k] && k0 + j < L) acc[k] = (k0 + j == 0) ? VT::in(x[k][j]) : VT::hop(acc[k], VT::in(x[k][j]));
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) total[k] = (g == 0) ? acc[k] : VT::hop(total[k], acc[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        if (!live[k]) continue;
+        const uint4 res = VT::out(total[k]);
+        if constexpr (OP == kOpAllReduce) {
+          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff[k], res);
+        } else {  // ReduceScatter: the vector lies in chunk c[k]
+          const unsigned long long i0 = boff[k] / E;
+          stg_stream(static_cast<unsigned char *>(p.out[c[k]]) + (i0 - (unsigned long long)c[k] * p.base) * E, res);
+        }
+      }
+    }
+  }
+  // the ragged end (under 16 bytes per rank)
+  for (unsigned long long i = p.n_bulk + (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count; i += T)
+    element_op<OP, DT, WT, HD>(p, i);
+}
+
 // A single CTA waits on a barrier that nothing completes; the bounded wait
 // must give up and record it.
 __global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long limit_ns);
@@ -420,6 +525,25 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
       if (dev < 64) smem_set[dev] = (int)l.smem;
     }
     rr_bulk_kernel<OP, DT, WT, HD><<<l.grid, l.threads, l.smem, s>>>(p);
+  } else if (l.path == RR_PATH_DIRECT) {
+    // vectors per thread: 1 for AllGather and halving-doubling; at most 2 when
+    // 16-bit storage is summed in binary32 (eight-float accumulators)
+    constexpr bool multi = !HD && OP != kOpAllGather;
+    constexpr bool wide = DT != kF32 && WT == kF32;
+    bool launched = false;
+    if constexpr (multi && !wide) {
+      if (p.direct_u >= 4) {
+        rr_direct_kernel<OP, DT, WT, HD, 4><<<l.grid, l.threads, 0, s>>>(p);
+        launched = true;
+      }
+    }
+    if constexpr (multi) {
+      if (!launched && p.direct_u >= 2) {
+        rr_direct_kernel<OP, DT, WT, HD, 2><<<l.grid, l.threads, 0, s>>>(p);
+        launched = true;
+      }
+    }
+    if (!launched) rr_direct_kernel<OP, DT, WT, HD, 1><<<l.grid, l.threads, 0, s>>>(p);
   } else {
     rr_simple_kernel<OP, DT, WT, HD><<<l.grid, l.threads, 0, s>>>(p);
   }

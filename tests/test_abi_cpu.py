@@ -174,7 +174,7 @@ def test_aliasing(L):
 
 def test_bad_launch_cfg(L):
     ins, outs = fake(4, 100, 4)
-    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(3, 0, 0, 0, 0)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(4, 0, 0, 0, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 24, 0, 0, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 17, 0, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 1, 0, 0)) == EINVAL
@@ -254,21 +254,32 @@ def test_planner_invariants_every_rank_count(L):
 
 
 def test_planner_paths(L):
+    BULK, SIMPLE, DIRECT = 1, 2, 3
     # unaligned buffers or sub-16-byte messages take the simple path
-    assert plan_dev(L, AR, 8, 1 << 20, F16, aligned=0)[1]["path"] == 2
-    assert plan_dev(L, AR, 8, 7, F16)[1]["path"] == 2
-    assert plan_dev(L, AR, 8, 1 << 20, F16)[1]["path"] == 1
-    # ReduceScatter / AllGather need chunk boundaries on 16 bytes for the bulk path
-    assert plan_dev(L, RS, 8, 8 * 1001, F16)[1]["path"] == 2
-    assert plan_dev(L, RS, 8, 8 * 1024, F16)[1]["path"] == 1
-    assert plan_dev(L, AG, 8, 8 * 1024, F32)[1]["path"] == 1
+    assert plan_dev(L, AR, 8, 1 << 20, F16, aligned=0)[1]["path"] == SIMPLE
+    assert plan_dev(L, AR, 8, 7, F16)[1]["path"] == SIMPLE
+    # the measured choice between the two aligned paths
+    assert plan_dev(L, AR, 8, 1 << 28, F16)[1]["path"] == DIRECT
+    assert plan_dev(L, AR, 32, 1 << 20, F16)[1]["path"] == DIRECT
+    assert plan_dev(L, AR, 2, 1 << 28, F16)[1]["path"] == BULK
+    assert plan_dev(L, AR, 4, 4 << 20, F32)[1]["path"] == BULK        # 16 MiB per rank
+    assert plan_dev(L, AR, 4, 64 << 20, F32)[1]["path"] == DIRECT     # 256 MiB per rank
+    assert plan_dev(L, AR, 4, 1 << 18, F32)[1]["path"] == DIRECT      # 1 MiB per rank
+    assert plan_dev(L, RS, 4, 1 << 22, F32)[1]["path"] == DIRECT
+    assert plan_dev(L, AG, 16, 1 << 24, F32)[1]["path"] == BULK
+    assert plan_dev(L, AG, 8, 1 << 24, F32)[1]["path"] == DIRECT
+    assert plan_dev(L, AR, 8, 1 << 28, F16, cfg=(0, 0, 0, 0, 0, 96))[1]["path"] == BULK  # capped grid
+    # ReduceScatter / AllGather need chunk boundaries on 16 bytes for the aligned paths
+    assert plan_dev(L, RS, 8, 8 * 1001, F16)[1]["path"] == SIMPLE
+    assert plan_dev(L, RS, 8, 8 * 1024, F16, cfg=(BULK, 0, 0, 0, 0))[1]["path"] == BULK
+    assert plan_dev(L, AG, 8, 8 * 1024, F32, cfg=(BULK, 0, 0, 0, 0))[1]["path"] == BULK
     # a forced bulk path the buffers do not allow is refused
     assert plan_dev(L, RS, 8, 8 * 1001, F16, cfg=(1, 0, 0, 0, 0))[0] == EUNSUP
     # a forced configuration that does not fit shared memory is refused
     assert plan_dev(L, AR, 64, 1 << 20, F32, cfg=(1, 4096, 8, 1, 0))[0] == EUNSUP
     # the two-level ring plans like the flat ring of all its ranks
     st, ch, _, _ = plan_dev(L, AR, 16, 1 << 24, F32, group=8)
-    assert st == OK and ch["path"] == 1
+    assert st == OK and ch["path"] == DIRECT
 
 
 # --------------------------------------------------------------------------
@@ -343,8 +354,10 @@ def test_algo_arguments(L):
 
 
 def test_max_ctas_caps_the_grid(L):
-    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 28, F16)
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 28, F16, cfg=(1, 0, 0, 0, 0))
     assert st == OK and grid == 456
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 28, F16)  # the direct path: 8 CTAs of 256 per SM
+    assert st == OK and ch["path"] == 3 and grid == 152 * 8
     st, ch, grid, smem = plan_dev(L, AR, 8, 1 << 28, F16, cfg=(0, 0, 0, 0, 0, 40))
     assert st == OK and grid == 40 and ch["max_ctas"] == 40
     # a capped grid gets one CTA per SM with larger tiles
@@ -354,3 +367,17 @@ def test_max_ctas_caps_the_grid(L):
     st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 10, F16, aligned=0, cfg=(0, 0, 0, 0, 0, 3))
     assert st == OK and grid == 3 and ch["path"] == 2
     assert plan_dev(L, AR, 8, 1 << 20, F16, cfg=(0, 0, 0, 0, 0, -1))[0] == EINVAL
+
+
+def test_direct_path_plans(L):
+    DIRECT = 3
+    st, ch, grid, smem = plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 0))
+    assert st == OK and ch["path"] == DIRECT and smem == 0
+    assert grid == min((1 << 19) * 2 // 16 // 256, 152 * 8)
+    # the same alignment needs as the bulk path, and at most 256 threads
+    assert plan_dev(L, AR, 8, 1 << 19, F16, aligned=0, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP
+    assert plan_dev(L, RS, 8, 8 * 1001, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP
+    assert plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 512))[0] == EUNSUP
+    assert plan_dev(L, AR, 8, 7, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP  # under 16 bytes
+    st, _, grid, _ = plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 128, 10))
+    assert st == OK and grid == 10

@@ -81,6 +81,11 @@ def cfg_of(rr, path=0, tile=0, stages=0, ctas=0, threads=0):
     return rr.LaunchCfg(path, tile, stages, ctas, threads)
 
 
+def direct_ok(N, R, E, op="ar"):
+    """The direct path's conditions (16-byte vectors; chunk offsets on 16 bytes for RS / AG)."""
+    return N * E >= 16 and (op == "ar" or (N // R * E) % 16 == 0)
+
+
 def run_ar(rr, xs, wire=None, group=0, cfg=None, inplace=False):
     if inplace:
         outs = [x.clone() for x in xs]
@@ -146,8 +151,11 @@ def test_allreduce_edge_grid(rr, dtype, wire, R):
             check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=64, stages=3), what=tag + " bulk64")
             check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=1024, stages=8, ctas=1,
                                                threads=128), what=tag + " bulk1k")
+            check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
     xs = gen(R, 65537, dtype, seed)
     check_ar(rr, xs, wire, inplace=True, what=f"AR in place R={R}")
+    check_ar(rr, xs, wire, inplace=True, cfg=cfg_of(rr, path=rr.PATH_DIRECT, threads=128),
+             what=f"AR in place direct R={R}")
 
 
 @pytest.mark.parametrize("G,L", [(2, 8), (2, 2), (3, 4), (4, 1), (2, 4), (8, 2)])
@@ -163,6 +171,7 @@ def test_two_level_grid(rr, G, L, dtype, wire):
         check_ar(rr, xs, wire, group=L, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
         if N * xs[0].element_size() >= 16:
             check_ar(rr, xs, wire, group=L, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=128), what=tag + " bulk128")
+            check_ar(rr, xs, wire, group=L, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
 
 
 @pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
@@ -173,6 +182,8 @@ def test_reduce_scatter_grid(rr, dtype, wire, R):
         tag = f"RS {NAME[dtype]}/{wire} R={R} N={N}"
         check_rs(rr, xs, wire, what=tag)
         check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+        if direct_ok(N, R, xs[0].element_size(), "rs"):
+            check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16], ids=str)
@@ -184,17 +195,21 @@ def test_allgather_grid(rr, dtype, R):
         tag = f"AG {NAME[dtype]} R={R} N={N}"
         check_ag(rr, chunks, N, what=tag)
         check_ag(rr, chunks, N, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+        if direct_ok(N, R, chunks[-1].element_size(), "ag"):
+            check_ag(rr, chunks, N, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
 
 
-def test_bulk_path_is_chosen_when_aligned(rr):
+def test_aligned_paths_are_chosen_when_aligned(rr):
     xs = gen(8, 1 << 20, torch.float16, 5)
     outs = [torch.empty_like(x) for x in xs]
-    assert rr.plan(rr.OP_ALLREDUCE, xs, outs, 1 << 20)["path"] == rr.PATH_BULK
+    assert rr.plan(rr.OP_ALLREDUCE, xs, outs, 1 << 20)["path"] in (rr.PATH_BULK, rr.PATH_DIRECT)
     # chunk boundaries off the 16-byte grid: ReduceScatter takes the simple path
     N = 8 * 1001
     xs = gen(8, N, torch.float16, 5)
     rs = [torch.empty(N // 8, dtype=torch.float16, device="cuda") for _ in range(8)]
     assert rr.plan(rr.OP_REDUCE_SCATTER, xs, rs, N)["path"] == rr.PATH_SIMPLE
+    with pytest.raises(rr.RingError):
+        rr.collective(rr.OP_REDUCE_SCATTER, xs, rs, N, cfg=cfg_of(rr, path=rr.PATH_DIRECT))
     with pytest.raises(rr.RingError) as e:
         rr.collective(rr.OP_REDUCE_SCATTER, xs, rs, N, cfg=cfg_of(rr, path=rr.PATH_BULK))
     assert e.value.status == rr.ERR_UNSUPPORTED
@@ -468,6 +483,8 @@ def test_algorithm_grid(rr, algo, dtype, wire):
             check_algo(rr, xs, wire, algo, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
             if N * xs[0].element_size() >= 16 and R <= 16:
                 check_algo(rr, xs, wire, algo, cfg=cfg_of(rr, path=rr.PATH_BULK, tile=256), what=tag + " bulk256")
+            if N * xs[0].element_size() >= 16:
+                check_algo(rr, xs, wire, algo, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
 
 
 @pytest.mark.parametrize("algo", ["hd", "naive"])
@@ -495,3 +512,12 @@ def test_capped_grids(rr):
                      what=f"max_ctas={cap} {NAME[dtype]}/{wire}")
             check_ar(rr, xs, wire, cfg=rr.LaunchCfg(rr.PATH_SIMPLE, 0, 0, 0, 0, cap),
                      what=f"simple max_ctas={cap} {NAME[dtype]}/{wire}")
+            check_ar(rr, xs, wire, cfg=rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 128, cap),
+                     what=f"direct max_ctas={cap} {NAME[dtype]}/{wire}")
+    # few ranks: the direct path takes several vectors per thread
+    for R in (2, 3, 4):
+        xs = gen(R, 300_007, torch.float16, 98)
+        for cap in (1, 7, 100):
+            check_ar(rr, xs, cfg=rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 256, cap), what=f"direct R={R} cap={cap}")
+            check_rs(rr, xs[:R], cfg=rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 64, cap), what=f"direct RS R={R} cap={cap}") \
+                if (300_007 // R * 2) % 16 == 0 else None
