@@ -243,7 +243,7 @@ def time_oracle(msg_mib, seed0=2000):
     return n * 2 / dt / 1e9, dt, n
 
 
-def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring"):
+def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring", cfg=None):
     """Time workload w: CUDA-graph replay of `launches` back-to-back calls over
     rotating buffer sets (>= 3x L2 in total).  Returns one table row."""
     import torch
@@ -264,9 +264,9 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring"):
         sets.append((ins, outs))
     def call(ins, outs, stream=None):
         if algo == "ring":
-            rr.collective(op, ins, outs, N, w.wire, w.group_size, stream)
+            rr.collective(op, ins, outs, N, w.wire, w.group_size, stream, cfg)
         else:
-            rr.allreduce_algo(ins, outs, w.wire, algo, stream)
+            rr.allreduce_algo(ins, outs, w.wire, algo, stream, cfg)
 
     for ins, outs in sets:  # warm up outside capture
         call(ins, outs)
@@ -296,7 +296,7 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring"):
            "msg_bytes": msg, "ms": round(t_ms, 5), "algbw_gbs": round(msg / t_ms / 1e6, 2),
            "busbw_gbs": round(busbw, 2), "hbm_gbs": round(alg / t_ms / 1e6, 1),
            "roofline_frac": round(alg / t_ms / 1e6 / peak, 4), "buffer_sets": nsets,
-           "plan": rr.plan(op, sets[0][0], sets[0][1], N, w.wire, w.group_size)}
+           "plan": rr.plan(op, sets[0][0], sets[0][1], N, w.wire, w.group_size, cfg)}
     del g, sets
     return row
 

@@ -70,7 +70,7 @@ extern "C" {
 typedef struct CUstream_st *cudaStream_t;
 
 #define RR_MAX_RANKS 64
-#define RR_ABI_VERSION 1
+#define RR_ABI_VERSION 2
 
 typedef enum { RR_FP32 = 0, RR_FP16 = 1, RR_BF16 = 2 } rr_dtype;
 
@@ -149,6 +149,11 @@ typedef struct {
                       that runs beside compute kernels can leave them SMs.
                       With fewer CTAs than 3 per SM and no stages / CTAs-per-SM
                       given, each CTA takes a whole SM with larger tiles. */
+  int early_launch; /* 0: the library's choice; 1: the kernel may be scheduled
+                      while the previous kernel on the stream is still
+                      running (programmatic dependent launch: it waits for that
+                      kernel's completion and writes before touching memory);
+                      2: plain stream order.  Never changes the result. */
 } rr_launch_cfg;
 
 /*

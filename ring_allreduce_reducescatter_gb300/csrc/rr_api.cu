@@ -49,6 +49,9 @@ rr_status current_device(DeviceInfo *out) {
 }
 
 constexpr int kMaxStages = 16;  // pipeline depth limit of the bulk path
+// Programmatic dependent launch by default: a kernel's launch overlaps the
+// previous kernel on the stream; it waits for that kernel before any access.
+constexpr bool kEarlyLaunchDefault = true;
 
 size_t elem_bytes(int t) { return t == RR_FP32 ? 4 : 2; }
 bool valid_type(int t) { return t == RR_FP32 || t == RR_FP16 || t == RR_BF16; }
@@ -96,6 +99,7 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
     if (cfg->threads != 0 && (cfg->threads < 64 || cfg->threads > 1024 || cfg->threads % 32 != 0))
       return RR_ERR_INVALID_ARG;
     if (cfg->max_ctas < 0) return RR_ERR_INVALID_ARG;
+    if (cfg->early_launch < 0 || cfg->early_launch > 2) return RR_ERR_INVALID_ARG;
   }
   ck->op = op;
   ck->R = R;
@@ -188,7 +192,7 @@ bool prefer_direct(int op, int R, unsigned long long msg_bytes, int max_ctas) {
 // vectors need it) and every shared-memory size fits the device.
 rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int smem_per_sm, int smem_optin,
                       rr::RingParams *p, rr::Launch *l) {
-  const rr_launch_cfg zero = {0, 0, 0, 0, 0, 0};
+  const rr_launch_cfg zero = {0, 0, 0, 0, 0, 0, 0};
   const rr_launch_cfg &c = cfg ? *cfg : zero;
   const size_t E = ck.E;
   const unsigned long long N = ck.n;  // elements of this launch
@@ -225,6 +229,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
 
   l->path = path;
   l->threads = c.threads ? c.threads : 256;
+  l->early_launch = c.early_launch == 0 ? kEarlyLaunchDefault : c.early_launch == 1;
   if (path == RR_PATH_DIRECT) {  // U 16-byte vectors per thread
     if (l->threads > 256) return RR_ERR_UNSUPPORTED;
     // eight loads in flight per thread: few ranks per group take several vectors
@@ -356,6 +361,7 @@ void export_plan(const rr::RingParams &p, const rr::Launch &l, size_t E, rr_laun
   chosen->ctas_per_sm = l.ctas_per_sm;
   chosen->threads = l.threads;
   chosen->max_ctas = l.grid;
+  chosen->early_launch = l.early_launch ? 1 : 2;
 }
 
 // Plan and launch a validated collective on the current device.

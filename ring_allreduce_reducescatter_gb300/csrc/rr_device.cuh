@@ -266,6 +266,18 @@ __device__ __forceinline__ void stg_stream(void *p, uint4 v) {
                : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the kernel before it on the stream still
+// runs.  grid_dependency_wait() blocks until that kernel has completed and its
+// writes are visible (at once for a kernel launched in plain stream order); it
+// comes first in every kernel, before any global memory access.
+// grid_dependents_launch() lets the next kernel on the stream be scheduled
+// once every CTA of this grid has executed it or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------------
 // PTX: mbarrier, bulk asynchronous copies, L2 policy, timer
 // --------------------------------------------------------------------------

@@ -166,6 +166,8 @@ __device__ __forceinline__ void element_op(const RingParams &p, unsigned long lo
 
 template <int OP, int DT, int WT, bool HD>
 __global__ void __launch_bounds__(1024) rr_simple_kernel(const __grid_constant__ RingParams p) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
   for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count; i += stride)
     element_op<OP, DT, WT, HD>(p, i);
@@ -329,6 +331,7 @@ __device__ __forceinline__ void issue_stores(const RingParams &p, const unsigned
 
 template <int OP, int DT, int WT, bool HD>
 __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ RingParams p) {
+  grid_dependency_wait();
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int E = Fmt<DT>::bytes;
   const int S = p.stages;
@@ -385,6 +388,9 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
       }
     }
   }
+  // Only now may the next kernel be scheduled: its CTAs would fit beside this
+  // persistent grid and, while they wait for it, slow it down (measured).
+  grid_dependents_launch();
   if (threadIdx.x == 0) {
     if (!ok) {
       atomicOr(p.status, kStatusWaitTimeout);
@@ -410,6 +416,10 @@ constexpr int kDirectThreads = 256;
 
 template <int OP, int DT, int WT, bool HD, int U>
 __global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __grid_constant__ RingParams p) {
+  // The next kernel may be scheduled at once: a large grid fills the SMs'
+  // registers or thread slots, so its CTAs take SMs only as this grid's leave.
+  grid_dependency_wait();
+  grid_dependents_launch();
   using VT = Vec<DT, WT>;
   using W = typename VT::W;
   constexpr int V = VT::V;
@@ -511,6 +521,23 @@ __global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long li
 // host side: one launch of (OP, DT, WT)
 // --------------------------------------------------------------------------
 
+// One launch of kernel k on the plan's grid, with programmatic stream
+// serialisation when the plan asks for it.
+inline cudaError_t launch_kernel(void (*k)(RingParams), const Launch &l, size_t smem, cudaStream_t s,
+                                 const RingParams &p) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3((unsigned)l.grid);
+  c.blockDim = dim3((unsigned)l.threads);
+  c.dynamicSmemBytes = smem;
+  c.stream = s;
+  c.attrs = attr;
+  c.numAttrs = l.early_launch ? 1 : 0;
+  return cudaLaunchKernelEx(&c, k, p);
+}
+
 template <int OP, int DT, int WT, bool HD>
 cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s) {
   if (l.path == RR_PATH_BULK) {
@@ -524,30 +551,21 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
       if (e != cudaSuccess) return e;
       if (dev < 64) smem_set[dev] = (int)l.smem;
     }
-    rr_bulk_kernel<OP, DT, WT, HD><<<l.grid, l.threads, l.smem, s>>>(p);
+    return launch_kernel(rr_bulk_kernel<OP, DT, WT, HD>, l, l.smem, s, p);
   } else if (l.path == RR_PATH_DIRECT) {
     // vectors per thread: 1 for AllGather and halving-doubling; at most 2 when
     // 16-bit storage is summed in binary32 (eight-float accumulators)
     constexpr bool multi = !HD && OP != kOpAllGather;
     constexpr bool wide = DT != kF32 && WT == kF32;
-    bool launched = false;
     if constexpr (multi && !wide) {
-      if (p.direct_u >= 4) {
-        rr_direct_kernel<OP, DT, WT, HD, 4><<<l.grid, l.threads, 0, s>>>(p);
-        launched = true;
-      }
+      if (p.direct_u >= 4) return launch_kernel(rr_direct_kernel<OP, DT, WT, HD, 4>, l, 0, s, p);
     }
     if constexpr (multi) {
-      if (!launched && p.direct_u >= 2) {
-        rr_direct_kernel<OP, DT, WT, HD, 2><<<l.grid, l.threads, 0, s>>>(p);
-        launched = true;
-      }
+      if (p.direct_u >= 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, HD, 2>, l, 0, s, p);
     }
-    if (!launched) rr_direct_kernel<OP, DT, WT, HD, 1><<<l.grid, l.threads, 0, s>>>(p);
-  } else {
-    rr_simple_kernel<OP, DT, WT, HD><<<l.grid, l.threads, 0, s>>>(p);
+    return launch_kernel(rr_direct_kernel<OP, DT, WT, HD, 1>, l, 0, s, p);
   }
-  return cudaGetLastError();
+  return launch_kernel(rr_simple_kernel<OP, DT, WT, HD>, l, 0, s, p);
 }
 
 template <int OP, int DT, int WT>

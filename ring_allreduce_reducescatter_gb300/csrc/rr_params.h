@@ -51,6 +51,7 @@ struct Launch {
   int threads;
   size_t smem;      // dynamic shared memory bytes
   int ctas_per_sm;
+  bool early_launch;  // launch with programmatic stream serialisation
 };
 
 // Defined in rr_inst_<storage>.cu: launch the kernel of (op, storage dtype,

@@ -52,7 +52,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version(L):
-    assert L.ring_abi_version() == 1
+    assert L.ring_abi_version() == 2
 
 
 def test_status_strings(L):
@@ -180,6 +180,20 @@ def test_bad_launch_cfg(L):
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 1, 0, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 0, 5, 0)) == EINVAL
     assert call(L, AR, ins, outs, 4, 100, F32, cfg=(1, 0, 0, 0, 1000)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(0, 0, 0, 0, 0, 0, 3)) == EINVAL
+    assert call(L, AR, ins, outs, 4, 100, F32, cfg=(0, 0, 0, 0, 0, 0, -1)) == EINVAL
+
+
+def test_early_launch_choice(L):
+    """Programmatic dependent launch is the default on every path; 2 asks for
+    plain stream order and 1 for the early launch, whatever the path."""
+    for path in (0, 1, 2, 3):
+        for op in (AR, RS, AG):
+            st, ch, _, _ = plan_dev(L, op, 8, 1 << 20, F16, cfg=(path, 0, 0, 0, 0) if path else None)
+            assert st == OK and ch["early_launch"] == 1, (path, op, ch)
+            for el in (1, 2):
+                st, ch, _, _ = plan_dev(L, op, 8, 1 << 20, F16, cfg=(path, 0, 0, 0, 0, 0, el))
+                assert st == OK and ch["early_launch"] == el, (path, op, el, ch)
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

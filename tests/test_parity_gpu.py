@@ -284,6 +284,80 @@ def test_streams_and_ordering(rr):
 
 
 # --------------------------------------------------------------------------
+# back-to-back dependent kernels: with programmatic dependent launch a kernel
+# may be scheduled while the one before it runs, and must still see its writes
+# --------------------------------------------------------------------------
+
+CHAIN_PATHS = {"bulk": 1, "direct": 3, "simple": 2}
+
+
+def chain_device(rr, xs, cfg, rounds, stream=None):
+    """RS -> AG -> in-place AR -> (a torch kernel) -> in-place AR -> RS -> AG ...,
+    every step reading what the step before wrote, enqueued with no sync."""
+    R, N = len(xs), xs[0].numel()
+    lens = [rr.chunk_count(N, R, c) for c in range(R)]
+    parts = [torch.empty(n, dtype=xs[0].dtype, device="cuda") for n in lens]
+    full = [torch.empty(N, dtype=xs[0].dtype, device="cuda") for _ in range(R)]
+    rr.collective(rr.OP_REDUCE_SCATTER, xs, parts, N, None, 0, stream, cfg)
+    for _ in range(rounds):
+        rr.collective(rr.OP_ALLGATHER, parts, full, N, None, 0, stream, cfg)
+        rr.collective(rr.OP_ALLREDUCE, full, full, N, None, 0, stream, cfg)
+        full[1].neg_()
+        rr.collective(rr.OP_ALLREDUCE, full, full, N, None, 0, stream, cfg)
+        rr.collective(rr.OP_REDUCE_SCATTER, full, parts, N, None, 0, stream, cfg)
+    rr.collective(rr.OP_ALLGATHER, parts, full, N, None, 0, stream, cfg)
+    return full
+
+
+def chain_oracle(xs, rounds):
+    dt = NAME[xs[0].dtype]
+    R, N = len(xs), xs[0].numel()
+    parts = oracle.reduce_scatter([host(x) for x in xs], dt).outs
+    for _ in range(rounds):
+        full = oracle.allgather(parts, N, dt).outs
+        full = oracle.allreduce(full, dt).outs
+        full[1] = -full[1] if dt == "f32" else full[1] ^ np.uint16(0x8000)
+        full = oracle.allreduce(full, dt).outs
+        parts = oracle.reduce_scatter(full, dt).outs
+    return oracle.allgather(parts, N, dt).outs
+
+
+@pytest.mark.parametrize("early", [1, 2], ids=["early", "ordered"])
+@pytest.mark.parametrize("path", list(CHAIN_PATHS))
+@pytest.mark.parametrize("N", [16 * 4 * 97, 4 * 65540])
+def test_dependent_launch_chain(rr, path, early, N):
+    R = 4
+    xs = gen(R, N, torch.float32, 21, scale=0.25)
+    cfg = rr.LaunchCfg(CHAIN_PATHS[path], 0, 0, 0, 0, 0, early)
+    got = chain_device(rr, xs, cfg, rounds=3)
+    torch.cuda.synchronize()
+    want = chain_oracle(xs, rounds=3)
+    for r in range(R):
+        assert_same(host(got[r]), want[r], f"{path} early={early} N={N} rank {r}")
+
+
+def test_dependent_launch_chain_in_a_graph(rr):
+    """The same chain captured in a CUDA graph (programmatic edges) and replayed."""
+    R, N = 8, 16 * 8 * 33
+    xs = gen(R, N, torch.float16, 22, scale=0.05)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain_device(rr, xs, None, rounds=1, stream=s)  # warm-up outside capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            got = chain_device(rr, xs, None, rounds=2, stream=s)
+    for _ in range(3):
+        for r in range(R):
+            got[r].fill_(7.0)
+        g.replay()
+    torch.cuda.synchronize()
+    want = chain_oracle(xs, rounds=2)
+    for r in range(R):
+        assert_same(host(got[r]), want[r], f"graph replay rank {r}")
+
+
+# --------------------------------------------------------------------------
 # the workloads, at full size, in the launch configuration the benchmark uses
 # --------------------------------------------------------------------------
 
