@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
 
 constexpr int kDirectThreads = 256;
 
-template <int OP, int DT, int WT, bool HD, int U>
+template <int OP, int DT, int WT, int U>
 __global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __grid_constant__ RingParams p) {
   // The next kernel may be scheduled at once: a large grid fills the SMs'
   // registers or thread slots, so its CTAs take SMs only as this grid's leave.
@@ -428,29 +428,20 @@ __global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __gr
   const unsigned long long nvec = p.n_bulk / V;
   const unsigned long long T = (unsigned long long)gridDim.x * blockDim.x;
   for (unsigned long long v0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < nvec; v0 += T * U) {
-    if constexpr (OP == kOpAllGather || HD) {
+    if constexpr (OP == kOpAllGather) {
 #pragma unroll
       for (int k = 0; k < U; ++k) {
         const unsigned long long v = v0 + (unsigned long long)k * T;
         if (v >= nvec) break;
         const unsigned long long i0 = v * V, g0 = p.first + i0, boff = i0 * E;
-        if constexpr (OP == kOpAllGather) {
-          const int c = chunk_of(g0, p.base, p.L);
-          if (c != chunk_of(g0 + V - 1, p.base, p.L)) {
-            for (int e = 0; e < V; ++e) element_op<OP, DT, WT, HD>(p, i0 + e);
-            continue;
-          }
-          const uint4 val =
-              ldg_stream(static_cast<const unsigned char *>(p.in[c]) + (i0 - (unsigned long long)c * p.base) * E);
-          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, val);
-        } else {  // halving-doubling AllReduce
-          const int Ex = p.hd_extra;
-          auto x = [&](int r) { return VT::in(ldg_stream(static_cast<const unsigned char *>(p.in[r]) + boff)); };
-          auto leaf = [&](int u) { return u < Ex ? VT::hop(x(2 * u), x(2 * u + 1)) : x(u + Ex); };
-          auto add = [](W a, W b) { return VT::hop(a, b); };
-          const uint4 res = VT::out(hd_fold<W>(p.hd_log2p, leaf, add));
-          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, res);
+        const int c = chunk_of(g0, p.base, p.L);
+        if (c != chunk_of(g0 + V - 1, p.base, p.L)) {
+          for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, i0 + e);
+          continue;
         }
+        const uint4 val =
+            ldg_stream(static_cast<const unsigned char *>(p.in[c]) + (i0 - (unsigned long long)c * p.base) * E);
+        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, val);
       }
     } else {  // ring / naive fold, AllReduce or ReduceScatter
       unsigned long long boff[U];
@@ -466,7 +457,7 @@ __global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __gr
           const unsigned long long g0 = p.first + v * V;
           c[k] = start_rank(p, g0);
           if (c[k] != start_rank(p, g0 + V - 1)) {  // straddles a chunk boundary: element by element
-            for (int e = 0; e < V; ++e) element_op<OP, DT, WT, HD>(p, v * V + e);
+            for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
             live[k] = false;
           }
         }
@@ -510,7 +501,7 @@ __global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __gr
   }
   // the ragged end (under 16 bytes per rank)
   for (unsigned long long i = p.n_bulk + (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count; i += T)
-    element_op<OP, DT, WT, HD>(p, i);
+    element_op<OP, DT, WT>(p, i);
 }
 
 // A single CTA waits on a barrier that nothing completes; the bounded wait
@@ -553,17 +544,21 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
     }
     return launch_kernel(rr_bulk_kernel<OP, DT, WT, HD>, l, l.smem, s, p);
   } else if (l.path == RR_PATH_DIRECT) {
-    // vectors per thread: 1 for AllGather and halving-doubling; at most 2 when
-    // 16-bit storage is summed in binary32 (eight-float accumulators)
-    constexpr bool multi = !HD && OP != kOpAllGather;
-    constexpr bool wide = DT != kF32 && WT == kF32;
-    if constexpr (multi && !wide) {
-      if (p.direct_u >= 4) return launch_kernel(rr_direct_kernel<OP, DT, WT, HD, 4>, l, 0, s, p);
+    if constexpr (HD) {
+      return launch_hd_direct(DT, WT, p, l, s);
+    } else {
+      // vectors per thread: 1 for AllGather; at most 2 when 16-bit storage is
+      // summed in binary32 (eight-float accumulators)
+      constexpr bool multi = OP != kOpAllGather;
+      constexpr bool wide = DT != kF32 && WT == kF32;
+      if constexpr (multi && !wide) {
+        if (p.direct_u >= 4) return launch_kernel(rr_direct_kernel<OP, DT, WT, 4>, l, 0, s, p);
+      }
+      if constexpr (multi) {
+        if (p.direct_u >= 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2>, l, 0, s, p);
+      }
+      return launch_kernel(rr_direct_kernel<OP, DT, WT, 1>, l, 0, s, p);
     }
-    if constexpr (multi) {
-      if (p.direct_u >= 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, HD, 2>, l, 0, s, p);
-    }
-    return launch_kernel(rr_direct_kernel<OP, DT, WT, HD, 1>, l, 0, s, p);
   }
   return launch_kernel(rr_simple_kernel<OP, DT, WT, HD>, l, 0, s, p);
 }

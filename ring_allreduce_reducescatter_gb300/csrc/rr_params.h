@@ -46,7 +46,7 @@ struct RingParams {
 
 // One launch, fully resolved by the planner.
 struct Launch {
-  int path;         // RR_PATH_BULK or RR_PATH_SIMPLE
+  int path;         // RR_PATH_BULK, RR_PATH_SIMPLE or RR_PATH_DIRECT
   int grid;
   int threads;
   size_t smem;      // dynamic shared memory bytes
@@ -58,6 +58,15 @@ struct Launch {
 // wire) on `stream`; returns the launch error.
 cudaError_t launch_f32(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
 cudaError_t launch_f16(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+// Defined in rr_inst_hd_<storage>.cu: the halving-doubling AllReduce on the
+// direct path (one kernel per tree size).
+cudaError_t launch_hd_direct_f32(int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+cudaError_t launch_hd_direct_f16(int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+cudaError_t launch_hd_direct_bf16(int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+inline cudaError_t launch_hd_direct(int dt, int wire, const RingParams &p, const Launch &l, cudaStream_t s) {
+  return dt == kF32 ? launch_hd_direct_f32(wire, p, l, s)
+                    : dt == kF16 ? launch_hd_direct_f16(wire, p, l, s) : launch_hd_direct_bf16(wire, p, l, s);
+}
 cudaError_t launch_bf16(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
 // Defined in rr_inst_f32.cu: the bounded-wait self test kernel.
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long limit_ns, cudaStream_t s);

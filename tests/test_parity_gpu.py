@@ -549,7 +549,7 @@ def check_algo(rr, xs, wire, algo, cfg=None, what=""):
 @pytest.mark.parametrize("algo", ["hd", "naive"])
 @pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
 def test_algorithm_grid(rr, algo, dtype, wire):
-    for R in (1, 2, 3, 4, 5, 7, 8, 12, 16, 17, 33, 64):
+    for R in (1, 2, 3, 4, 5, 7, 8, 12, 16, 17, 24, 33, 48, 64):
         for N in (1, R + 1, 4097, 65_537):
             xs = gen(R, N, dtype, 7 * R + N)
             tag = f"{algo} {NAME[dtype]}/{wire} R={R} N={N}"
