@@ -244,6 +244,18 @@ def time_oracle(msg_mib, seed0=2000):
     return n * 2 / dt / 1e9, dt, n
 
 
+def staggered_inputs(rr, wl, w, dev, in_lens=None, out_lens=None):
+    """Workload w's inputs and room for its outputs, each side R vectors in
+    one allocation, staggered (rank_buffers) so that the ranks' concurrent
+    accesses do not all fall on the same memory channels."""
+    in_lens = in_lens or [w.count] * w.R
+    out_lens = out_lens or [w.count] * w.R
+    ins = rr.rank_buffers(w.R, in_lens, w.dtype, dev)
+    for r in range(w.R):
+        wl.rank_values(w.wid, r, in_lens[r], w.dtype, w.dist, dev, out=ins[r])
+    return ins, rr.rank_buffers(w.R, out_lens, w.dtype, dev)
+
+
 def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring", cfg=None):
     """Time workload w: CUDA-graph replay of `launches` back-to-back calls over
     rotating buffer sets (>= 3x L2 in total).  Returns one table row."""
@@ -260,9 +272,13 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring", cfg=None):
     nsets = max(1, min(16, -(-3 * l2_bytes // set_bytes)))
     sets = []
     for k in range(nsets):
-        ins = wl.inputs(w, dev, lengths=in_lens) if k == 0 else [t.clone() for t in sets[0][0]]
-        outs = [torch.empty(n, dtype=w.dtype, device=dev) for n in out_lens]
-        sets.append((ins, outs))
+        if k == 0:
+            sets.append(staggered_inputs(rr, wl, w, dev, in_lens, out_lens))
+        else:
+            ins = rr.rank_buffers(R_, in_lens, w.dtype, dev)
+            for a, b in zip(ins, sets[0][0]):
+                a.copy_(b)
+            sets.append((ins, rr.rank_buffers(R_, out_lens, w.dtype, dev)))
     def call(ins, outs, stream=None):
         if algo == "ring":
             rr.collective(op, ins, outs, N, w.wire, w.group_size, stream, cfg)
@@ -354,8 +370,7 @@ def overlap_row(rr, wl, dev, pieces=8, max_ctas=0):
     import torch
 
     w = wl.config2(512)
-    xs = wl.inputs(w, dev)
-    outs = [torch.empty_like(x) for x in xs]
+    xs, outs = staggered_inputs(rr, wl, w, dev)
     N = w.count
     step = -(-N // pieces) // 256 * 256
     n = 8192
@@ -457,8 +472,7 @@ def run_ours(args):
     w = wl.config2(args.msg_mib)
     N = w.count
     msg = N * 2
-    xs = wl.inputs(w, dev)
-    outs = [torch.empty_like(x) for x in xs]
+    xs, outs = staggered_inputs(rr, wl, w, dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -529,8 +543,9 @@ def run_ours(args):
             torch.cuda.empty_cache()
             table.append(bucket_set_row(rr, wl, dev, peak))
             overlap = [overlap_row(rr, wl, dev, max_ctas=m) for m in (0, 128, 96)]
-            xs = wl.inputs(w, dev)
-        outs = [torch.empty_like(x) for x in xs]
+            xs, outs = staggered_inputs(rr, wl, w, dev)
+        else:
+            outs = rr.rank_buffers(R, N, torch.float16, dev)
 
     # end to end through the C ABI's host-buffer entry point (ring_allreduce_host):
     # inputs in page-locked host memory, every output copied back to the host,
@@ -567,7 +582,7 @@ def run_ours(args):
                "steps": args.e2e_steps, "api": "ring_allreduce_host",
                "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity}
         del host_in, host_out, ws
-        outs = [torch.empty_like(x) for x in xs]
+        outs = rr.rank_buffers(R, N, torch.float16, dev)
 
     if sampler:
         sampler.stop()

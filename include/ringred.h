@@ -56,6 +56,12 @@
  *     buffer, with one exception: ring_allreduce* accepts out_bufs[r] ==
  *     in_bufs[r] (in place).  Inputs may overlap one another.
  *   - 1 <= R <= RR_MAX_RANKS.
+ * Layout (speed only): the kernels access element i of every rank's vector
+ * at about the same time.  Vectors whose start addresses agree modulo a large
+ * power of two (separate allocations of one power-of-two size, rows of an
+ * unpadded [R][N] array) then load the same memory channels together; the
+ * R = 8, 512 MiB AllReduce measured about 2 % slower on them than on vectors
+ * staggered by 1-17 MiB (the Python binding's rank_buffers lays them out so).
  */
 #ifndef RINGRED_H
 #define RINGRED_H

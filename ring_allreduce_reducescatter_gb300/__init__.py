@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "RingError", "lib", "allreduce", "reduce_scatter", "allgather", "collective", "plan",
     "allreduce_range", "allreduce_host", "allreduce_host_static", "host_workspace_bytes", "allreduce_algo",
-    "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg",
+    "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg", "rank_buffers",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
     "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE", "PATH_DIRECT",
 ]
@@ -33,6 +33,33 @@ FP32, FP16, BF16 = 0, 1, 2
 _TORCH_CODE = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}
 _NAME_CODE = {"f32": FP32, "fp32": FP32, "float32": FP32, "f16": FP16, "fp16": FP16,
               "float16": FP16, "bf16": BF16, "bfloat16": BF16}
+
+
+RANK_STAGGER_BYTES = 2 << 20
+
+
+def rank_buffers(R: int, count, dtype: torch.dtype, device=None, stagger_bytes: int = RANK_STAGGER_BYTES):
+    """R rank vectors as views of one device allocation (plain torch memory;
+    the library itself allocates nothing).  ``count`` is one length for every
+    rank or a list of R lengths.  Each vector starts 256-byte aligned and
+    ``stagger_bytes`` past the end of the one before.  Vectors whose start
+    addresses agree modulo a large power of two (separate allocations of one
+    power-of-two size, or rows of an unpadded [R, N] tensor) send all their
+    concurrent accesses to the same memory channels: the R = 8, 512 MiB
+    AllReduce ran about 2 % slower on them than on vectors staggered by
+    1-17 MiB."""
+    counts = [int(count)] * R if isinstance(count, int) else [int(c) for c in count]
+    if len(counts) != R or min(counts, default=0) < 0:
+        raise ValueError("need R non-negative lengths")
+    e = torch.tensor([], dtype=dtype).element_size()
+    if stagger_bytes < 0 or stagger_bytes % 256:
+        raise ValueError("stagger_bytes must be a non-negative multiple of 256")
+    offs, off = [], 0
+    for c in counts:
+        offs.append(off)
+        off += (-(-c * e // 256) * 256 + stagger_bytes) // e
+    slab = torch.empty(max(off, 1), dtype=dtype, device=device)
+    return [slab[o:o + c] for o, c in zip(offs, counts)]
 
 
 class RingError(RuntimeError):

@@ -395,3 +395,32 @@ def test_direct_path_plans(L):
     assert plan_dev(L, AR, 8, 7, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP  # under 16 bytes
     st, _, grid, _ = plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 128, 10))
     assert st == OK and grid == 10
+
+
+def test_rank_buffers_layout():
+    """rank_buffers: R views of one allocation, each 256-byte aligned relative
+    to the first, staggered by the requested bytes, never overlapping."""
+    import torch
+
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    for dtype, e in ((torch.float32, 4), (torch.float16, 2), (torch.bfloat16, 2)):
+        for counts in (7, 65537, [3, 0, 11, 256]):
+            R = 4
+            for stagger in (0, 256, 2 << 20):
+                bufs = rr.rank_buffers(R, counts, dtype, "cpu", stagger_bytes=stagger)
+                lens = [counts] * R if isinstance(counts, int) else counts
+                assert [b.numel() for b in bufs] == lens
+                base = bufs[0].data_ptr()
+                ends = []
+                for b, n in zip(bufs, lens):
+                    if n == 0:
+                        continue
+                    off = b.data_ptr() - base
+                    assert off % 256 == 0
+                    assert all(off >= end + stagger for end in ends[-1:])
+                    ends.append(off + -(-n * e // 256) * 256)
+    with pytest.raises(ValueError):
+        rr.rank_buffers(2, 8, torch.float32, "cpu", stagger_bytes=100)
+    with pytest.raises(ValueError):
+        rr.rank_buffers(3, [1, 2], torch.float32, "cpu")

@@ -336,6 +336,23 @@ def test_dependent_launch_chain(rr, path, early, N):
         assert_same(host(got[r]), want[r], f"{path} early={early} N={N} rank {r}")
 
 
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_staggered_rank_buffers(rr, dtype, wire):
+    """Rank vectors laid out by rank_buffers (views of one allocation, odd
+    lengths padded to 256 bytes) reduce like separate tensors."""
+    R, N = 8, 65537
+    src = gen(R, N, dtype, 23)
+    ins = rr.rank_buffers(R, N, dtype, "cuda")
+    outs = rr.rank_buffers(R, N, dtype, "cuda", stagger_bytes=4096)
+    for a, b in zip(ins, src):
+        a.copy_(b)
+    rr.collective(rr.OP_ALLREDUCE, ins, outs, N, wire, 0, None, None)
+    torch.cuda.synchronize()
+    ref = oracle.allreduce([host(x) for x in src], NAME[dtype], wire)
+    for r in range(R):
+        assert_same(host(outs[r]), ref.outs[r], f"staggered rank {r}")
+
+
 def test_dependent_launch_chain_in_a_graph(rr):
     """The same chain captured in a CUDA graph (programmatic edges) and replayed."""
     R, N = 8, 16 * 8 * 33
