@@ -176,13 +176,16 @@ unsigned round16_down(unsigned long long x) { return (unsigned)(x & ~15ull); }
 // tile pipeline wins for two ranks, for 3..7 ranks between 2 and 64 MiB, for
 // AllGather with 16 or more ranks above 1 MiB, and for capped grids (each CTA
 // then owns an SM and moves 8 KB per bulk copy).
-bool prefer_direct(int op, int R, unsigned long long msg_bytes, int max_ctas) {
+bool prefer_direct(int op, int R, int L, unsigned long long msg_bytes, int max_ctas) {
   const unsigned long long MiB = 1ull << 20;
-  if (max_ctas > 0) return false;
-  if (op == RR_OP_ALLGATHER) return R < 16 || msg_bytes <= MiB;
+  if (max_ctas > 0) return false;                       // capped grids: one tile pipeline per SM
+  if (op == RR_OP_ALLGATHER) return true;
   if (op == RR_OP_REDUCE_SCATTER) return R >= 3;
   if (R <= 2) return false;
-  if (R < 8) return msg_bytes <= MiB || msg_bytes >= 64 * MiB;
+  if (L < R) return true;                               // two-level
+  if (R == 3) return msg_bytes <= 4 * MiB;              // six loads a thread: the tile pipeline above
+  if (R == 4) return msg_bytes <= 4 * MiB || msg_bytes >= 64 * MiB;
+  if (R == 16) return msg_bytes < 64 * MiB;             // two CTAs of three 32 KiB stages per SM
   return true;
 }
 
@@ -224,11 +227,13 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   if ((path == RR_PATH_BULK || path == RR_PATH_DIRECT) && !bulk_ok) return RR_ERR_UNSUPPORTED;
   if (path == RR_PATH_AUTO)
     path = !bulk_ok ? RR_PATH_SIMPLE
-                    : (prefer_direct(ck.op, ck.R, (unsigned long long)ck.count * E, c.max_ctas) ? RR_PATH_DIRECT
+                    : (prefer_direct(ck.op, ck.R, ck.L, (unsigned long long)ck.count * E, c.max_ctas) ? RR_PATH_DIRECT
                                                                                                 : RR_PATH_BULK);
 
   l->path = path;
-  l->threads = c.threads ? c.threads : 256;
+  // 128-thread CTAs on the direct path: finer grid granularity, measured 1-5 %
+  // faster than 256 up to 16 MiB per rank and the same above
+  l->threads = c.threads ? c.threads : (path == RR_PATH_DIRECT ? 128 : 256);
   l->early_launch = c.early_launch == 0 ? kEarlyLaunchDefault : c.early_launch == 1;
   if (path == RR_PATH_DIRECT) {  // U 16-byte vectors per thread
     if (l->threads > 256) return RR_ERR_UNSUPPORTED;
@@ -236,10 +241,32 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 2 ? 4 : ck.L <= 4 ? 2 : 1);
     if (U > 2 && ck.dtype != RR_FP32 && ck.wire == RR_FP32) U = 2;  // binary32 accumulators are twice as wide
     p->direct_u = U;
+    // One vector per thread: a third CTA per SM (registers capped at 85) keeps
+    // more loads in flight when a thread has fewer than seven (measured: R = 5
+    // 0.88 -> 0.98, R = 9 0.93 -> 0.99 of the copy bandwidth at 256 MiB); a
+    // thread with seven or eight keeps DRAM busy with two, which did better
+    // on large messages (R = 8, 256 MiB: 1.004 against 0.991).
+    const unsigned long long msg_bytes = (unsigned long long)ck.count * E;
+    const bool full_batch = (ck.R == 7 || ck.R == 8) && msg_bytes >= (64ull << 20);
+    const bool wide = ck.dtype != RR_FP32 && ck.wire == RR_FP32;  // eight binary32 accumulators: 128 registers
+    l->direct_occ = (U == 1 && ck.op != RR_OP_ALLGATHER && !full_batch && !wide) ? 3 : 2;
     const unsigned long long vecs = n_bulk * E / 16;
     const unsigned long long blocks = (vecs + (unsigned long long)l->threads * U - 1) / ((unsigned long long)l->threads * U);
     const unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);
+    // Vectors over a chunk boundary (ring order, boundaries off the 16-byte
+    // grid): one extra CTA folds them, so the main loop stays lean.
+    const unsigned long long V = 16 / E;
+    p->straddle_cta = (ck.op == RR_OP_ALLREDUCE && ck.algo == RR_ALGO_RING && ck.L > 1 && p->base > 0 &&
+                       (p->base % V != 0 || ck.first % V != 0))
+                          ? 1
+                          : 0;
     l->grid = capped((int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap));
+    if (p->straddle_cta) {
+      if (!(c.max_ctas > 0 && l->grid >= c.max_ctas))
+        l->grid += 1;                      // one more CTA
+      else if (l->grid < 2)
+        p->straddle_cta = 0;               // a one-CTA cap: the main loop folds them element by element
+    }
     l->smem = 0;
     l->ctas_per_sm = 0;
     p->n_bulk = n_bulk;

@@ -414,19 +414,110 @@ __global__ void __launch_bounds__(1024) rr_bulk_kernel(const __grid_constant__ R
 
 constexpr int kDirectThreads = 256;
 
-template <int OP, int DT, int WT, int U>
-__global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __grid_constant__ RingParams p) {
+// The first nbytes bytes of a, the rest of b.
+__device__ __forceinline__ uint4 blend_bytes(uint4 a, uint4 b, int nbytes) {
+  auto word = [nbytes](uint32_t x, uint32_t y, int w) -> uint32_t {
+    const int lo = w * 4;
+    if (nbytes >= lo + 4) return x;
+    if (nbytes <= lo) return y;
+    const uint32_t keep = (1u << (8 * (nbytes - lo))) - 1u;  // the low bytes come from a
+    return (x & keep) | (y & ~keep);
+  };
+  return make_uint4(word(a.x, b.x, 0), word(a.y, b.y, 1), word(a.z, b.z, 2), word(a.w, b.w, 3));
+}
+
+// An AllReduce vector whose elements lie in two adjacent chunks c0 and
+// c0 + 1: the first ones start the ring at rank c0 (c0, c0+1, ..., c0+L-1),
+// the others at c0 + 1 (c0+1, ..., c0+L-1, then c0).  Both folds share one
+// pass of 16-byte loads in the first order; the second keeps rank c0's vector
+// aside and adds it last.  Vectors over more chunks (chunks shorter than a
+// vector) go element by element.
+template <int DT, int WT>
+__device__ __forceinline__ void straddle_vec(const RingParams &p, unsigned long long v, int c0, int c_last) {
+  using VT = Vec<DT, WT>;
+  using W = typename VT::W;
+  constexpr int V = VT::V;
+  constexpr int E = Fmt<DT>::bytes;
+  const unsigned long long i0 = v * V, boff = i0 * E;
+  const int L = p.L;
+  if (c_last != c0 + 1) {
+    for (int e = 0; e < V; ++e) element_op<kOpAllReduce, DT, WT>(p, i0 + e);
+    return;
+  }
+  const int split = (int)(chunk_end(c0, p.base, L, p.total) - (p.first + i0));  // elements starting at c0
+  W total_a, total_b;
+  for (int g = 0; g < p.G; ++g) {
+    W a, b;
+    uint4 first;
+    for (int k0 = 0; k0 < L; k0 += 4) {  // rare: a short batch keeps its registers few
+      uint4 x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (k0 + j < L) {
+          int r = c0 + k0 + j;
+          r -= (r >= L) ? L : 0;
+          x[j] = ldg_stream(static_cast<const unsigned char *>(p.in[g * L + r]) + boff);
+        }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int k = k0 + j;
+        if (k >= L) break;
+        const W w = VT::in(x[j]);
+        if (k == 0) {
+          a = w;
+          first = x[j];
+        } else {
+          a = VT::hop(a, w);
+          b = (k == 1) ? w : VT::hop(b, w);
+        }
+      }
+    }
+    b = VT::hop(b, VT::in(first));
+    total_a = (g == 0) ? a : VT::hop(total_a, a);
+    total_b = (g == 0) ? b : VT::hop(total_b, b);
+  }
+  const uint4 res = blend_bytes(VT::out(total_a), VT::out(total_b), split * E);
+  for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, res);
+}
+
+// The AllReduce vectors that straddle a chunk boundary, done by one extra CTA
+// of the direct grid (the other CTAs skip them): at most one per boundary b
+// (chunk b starts at global index b * base), taken by the boundary that falls
+// first inside it.
+template <int DT, int WT>
+__device__ __forceinline__ void straddle_pass(const RingParams &p) {
+  constexpr int V = Vec<DT, WT>::V;
+  for (int b = 1 + threadIdx.x; b < p.L; b += blockDim.x) {
+    const unsigned long long gb = (unsigned long long)b * p.base;
+    if (gb <= p.first || gb - p.first >= p.n_bulk || (gb - p.first) % V == 0) continue;
+    const unsigned long long v = (gb - p.first) / V, g0 = p.first + v * V;
+    if ((unsigned long long)(b - 1) * p.base > g0) continue;  // an earlier boundary lies inside this vector
+    const int c0 = start_rank(p, g0), c_last = start_rank(p, g0 + V - 1);
+    if (c0 != c_last) straddle_vec<DT, WT>(p, v, c0, c_last);
+  }
+}
+
+// OCC: 256-thread CTAs per SM the registers are budgeted for (2: up to 128
+// registers a thread, 3: up to 85).
+template <int OP, int DT, int WT, int U, int OCC>
+__global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __grid_constant__ RingParams p) {
   // The next kernel may be scheduled at once: a large grid fills the SMs'
   // registers or thread slots, so its CTAs take SMs only as this grid's leave.
   grid_dependency_wait();
   grid_dependents_launch();
+  if constexpr (OP == kOpAllReduce) {
+    if (p.straddle_cta && blockIdx.x == gridDim.x - 1) {
+      straddle_pass<DT, WT>(p);
+      return;
+    }
+  }
   using VT = Vec<DT, WT>;
   using W = typename VT::W;
   constexpr int V = VT::V;
   constexpr int E = Fmt<DT>::bytes;
   constexpr int NB = 8 / U;  // ranks per batch of loads
   const unsigned long long nvec = p.n_bulk / V;
-  const unsigned long long T = (unsigned long long)gridDim.x * blockDim.x;
+  const unsigned long long T = (unsigned long long)(gridDim.x - p.straddle_cta) * blockDim.x;
   for (unsigned long long v0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < nvec; v0 += T * U) {
     if constexpr (OP == kOpAllGather) {
 #pragma unroll
@@ -456,8 +547,9 @@ __global__ void __launch_bounds__(kDirectThreads, 2) rr_direct_kernel(const __gr
         if (live[k]) {
           const unsigned long long g0 = p.first + v * V;
           c[k] = start_rank(p, g0);
-          if (c[k] != start_rank(p, g0 + V - 1)) {  // straddles a chunk boundary: element by element
-            for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
+          if (c[k] != start_rank(p, g0 + V - 1)) {  // straddles a chunk boundary
+            if (!p.straddle_cta)
+              for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
             live[k] = false;
           }
         }
@@ -552,12 +644,15 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
       constexpr bool multi = OP != kOpAllGather;
       constexpr bool wide = DT != kF32 && WT == kF32;
       if constexpr (multi && !wide) {
-        if (p.direct_u >= 4) return launch_kernel(rr_direct_kernel<OP, DT, WT, 4>, l, 0, s, p);
+        if (p.direct_u >= 4) return launch_kernel(rr_direct_kernel<OP, DT, WT, 4, 2>, l, 0, s, p);
       }
       if constexpr (multi) {
-        if (p.direct_u >= 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2>, l, 0, s, p);
+        if (p.direct_u >= 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
+        if constexpr (!wide) {
+          if (l.direct_occ == 3) return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 3>, l, 0, s, p);
+        }
       }
-      return launch_kernel(rr_direct_kernel<OP, DT, WT, 1>, l, 0, s, p);
+      return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
     }
   }
   return launch_kernel(rr_simple_kernel<OP, DT, WT, HD>, l, 0, s, p);

@@ -42,6 +42,7 @@ struct RingParams {
   int algo;                       // AllReduce summation order: kAlgo*
   int hd_log2p;                   // halving-doubling: log2 of P, the largest power of two <= R
   int hd_extra;                   // halving-doubling: R - P ranks folded in pairs first
+  int straddle_cta;               // direct AllReduce: 1 if the grid's last CTA folds the vectors over chunk boundaries
 };
 
 // One launch, fully resolved by the planner.
@@ -51,7 +52,8 @@ struct Launch {
   int threads;
   size_t smem;      // dynamic shared memory bytes
   int ctas_per_sm;
-  bool early_launch;  // launch with programmatic stream serialisation
+  bool early_launch;   // launch with programmatic stream serialisation
+  int direct_occ = 2;  // direct path, one vector per thread: 256-thread CTAs per SM it is compiled for (2 or 3)
 };
 
 // Defined in rr_inst_<storage>.cu: launch the kernel of (op, storage dtype,

@@ -279,8 +279,14 @@ def test_planner_paths(L):
     assert plan_dev(L, AR, 4, 4 << 20, F32)[1]["path"] == BULK        # 16 MiB per rank
     assert plan_dev(L, AR, 4, 64 << 20, F32)[1]["path"] == DIRECT     # 256 MiB per rank
     assert plan_dev(L, AR, 4, 1 << 18, F32)[1]["path"] == DIRECT      # 1 MiB per rank
+    assert plan_dev(L, AR, 3, 1 << 20, F32)[1]["path"] == DIRECT      # 4 MiB per rank
+    assert plan_dev(L, AR, 3, 1 << 22, F32)[1]["path"] == BULK        # 16 MiB per rank
+    for R in (5, 6, 7, 9, 12, 24, 32):
+        assert plan_dev(L, AR, R, 1 << 26, F32)[1]["path"] == DIRECT
+    assert plan_dev(L, AR, 16, 1 << 22, F32)[1]["path"] == DIRECT     # 16 MiB per rank
+    assert plan_dev(L, AR, 16, 1 << 24, F32)[1]["path"] == BULK       # 64 MiB per rank
     assert plan_dev(L, RS, 4, 1 << 22, F32)[1]["path"] == DIRECT
-    assert plan_dev(L, AG, 16, 1 << 24, F32)[1]["path"] == BULK
+    assert plan_dev(L, AG, 16, 1 << 24, F32)[1]["path"] == DIRECT
     assert plan_dev(L, AG, 8, 1 << 24, F32)[1]["path"] == DIRECT
     assert plan_dev(L, AR, 8, 1 << 28, F16, cfg=(0, 0, 0, 0, 0, 96))[1]["path"] == BULK  # capped grid
     # ReduceScatter / AllGather need chunk boundaries on 16 bytes for the aligned paths
@@ -370,8 +376,8 @@ def test_algo_arguments(L):
 def test_max_ctas_caps_the_grid(L):
     st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 28, F16, cfg=(1, 0, 0, 0, 0))
     assert st == OK and grid == 456
-    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 28, F16)  # the direct path: 8 CTAs of 256 per SM
-    assert st == OK and ch["path"] == 3 and grid == 152 * 8
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 28, F16)  # the direct path: 16 CTAs of 128 per SM
+    assert st == OK and ch["path"] == 3 and ch["threads"] == 128 and grid == 152 * 16
     st, ch, grid, smem = plan_dev(L, AR, 8, 1 << 28, F16, cfg=(0, 0, 0, 0, 0, 40))
     assert st == OK and grid == 40 and ch["max_ctas"] == 40
     # a capped grid gets one CTA per SM with larger tiles
@@ -387,7 +393,7 @@ def test_direct_path_plans(L):
     DIRECT = 3
     st, ch, grid, smem = plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 0))
     assert st == OK and ch["path"] == DIRECT and smem == 0
-    assert grid == min((1 << 19) * 2 // 16 // 256, 152 * 8)
+    assert ch["threads"] == 128 and grid == min((1 << 19) * 2 // 16 // 128, 152 * 16)
     # the same alignment needs as the bulk path, and at most 256 threads
     assert plan_dev(L, AR, 8, 1 << 19, F16, aligned=0, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP
     assert plan_dev(L, RS, 8, 8 * 1001, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP
@@ -395,6 +401,22 @@ def test_direct_path_plans(L):
     assert plan_dev(L, AR, 8, 7, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP  # under 16 bytes
     st, _, grid, _ = plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 128, 10))
     assert st == OK and grid == 10
+
+
+def test_direct_path_straddle_cta(L):
+    """Chunk boundaries off the 16-byte grid get one extra CTA (within a cap,
+    the cap's last CTA; a one-CTA cap folds them in the main loop)."""
+    DIRECT = 3
+    N = 6 * 87381  # base 87381 binary16 elements: boundaries fall inside vectors
+    blocks = -(-(N * 2 // 16) // 128)
+    st, ch, grid, _ = plan_dev(L, AR, 6, N, F16, cfg=(DIRECT, 0, 0, 0, 0))
+    assert st == OK and grid == blocks + 1
+    for cap in (1, 2, 7):
+        st, ch, grid, _ = plan_dev(L, AR, 6, N, F16, cfg=(DIRECT, 0, 0, 0, 0, cap))
+        assert st == OK and grid == cap
+    # aligned boundaries, ReduceScatter, and the naive order need none
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 0))
+    assert grid == (1 << 19) * 2 // 16 // 128
 
 
 def test_rank_buffers_layout():

@@ -337,6 +337,27 @@ def test_dependent_launch_chain(rr, path, early, N):
 
 
 @pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_vectors_over_chunk_boundaries(rr, dtype, wire):
+    """Chunk boundaries inside 16-byte vectors: the direct path's extra CTA
+    folds those vectors in two ring orders at once (and chunks shorter than a
+    vector element by element); every cap of the grid, in place and not."""
+    V = 16 // torch.tensor([], dtype=dtype).element_size()
+    for R in (3, 5, 6, 7, 9, 12, 24):
+        for base in (V * 2500 + 1, V * 2501 + V // 2, V * 999 + V - 1, 3):
+            N = R * base + (R - 1)
+            xs = gen(R, N, dtype, 53 * R + base)
+            tag = f"straddle {NAME[dtype]}/{wire} R={R} base={base}"
+            check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag)
+            if dtype == torch.float16 and wire is None:
+                for cap in (1, 2, 7):
+                    check_ar(rr, xs, wire, cfg=rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, cap),
+                             what=f"{tag} cap={cap}")
+                check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), inplace=True, what=tag + " in place")
+                check_ar(rr, xs, wire, group=R if R % 3 else 3, cfg=cfg_of(rr, path=rr.PATH_DIRECT),
+                         what=tag + " grouped")
+
+
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
 def test_staggered_rank_buffers(rr, dtype, wire):
     """Rank vectors laid out by rank_buffers (views of one allocation, odd
     lengths padded to 256 bytes) reduce like separate tensors."""
