@@ -183,8 +183,6 @@ bool prefer_direct(int op, int R, int L, unsigned long long msg_bytes, int max_c
   if (op == RR_OP_REDUCE_SCATTER) return R >= 3;
   if (R <= 2) return false;
   if (L < R) return true;                               // two-level
-  if (R == 3) return msg_bytes <= 4 * MiB;              // six loads a thread: the tile pipeline above
-  if (R == 4) return msg_bytes <= 4 * MiB || msg_bytes >= 64 * MiB;
   if (R == 16) return msg_bytes < 64 * MiB;             // two CTAs of three 32 KiB stages per SM
   return true;
 }
@@ -241,15 +239,18 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 2 ? 4 : ck.L <= 4 ? 2 : 1);
     if (U > 2 && ck.dtype != RR_FP32 && ck.wire == RR_FP32) U = 2;  // binary32 accumulators are twice as wide
     p->direct_u = U;
-    // One vector per thread: a third CTA per SM (registers capped at 85) keeps
-    // more loads in flight when a thread has fewer than seven (measured: R = 5
-    // 0.88 -> 0.98, R = 9 0.93 -> 0.99 of the copy bandwidth at 256 MiB); a
-    // thread with seven or eight keeps DRAM busy with two, which did better
-    // on large messages (R = 8, 256 MiB: 1.004 against 0.991).
+    // A third CTA per SM (registers capped at 85) keeps more loads in flight
+    // (measured at 256 MiB, of the copy bandwidth: R = 5 0.88 -> 0.98, R = 9
+    // 0.93 -> 0.99, R = 3 0.85 -> 0.96).  Threads whose group is exactly one
+    // batch of seven or eight loads (R = 7 or 8; two-level rings of 4- or
+    // 8-rank groups) keep DRAM busy with two, which did better from 64 MiB
+    // (R = 8, 256 MiB: 1.006 against 0.991); flat rings of three or four ranks
+    // (two vectors a thread) do not.
     const unsigned long long msg_bytes = (unsigned long long)ck.count * E;
-    const bool full_batch = (ck.R == 7 || ck.R == 8) && msg_bytes >= (64ull << 20);
+    const int batch = U * ck.L;  // loads of one group a thread issues together
+    const bool full_batch = (batch == 7 || batch == 8) && msg_bytes >= (64ull << 20) && !(U == 2 && ck.L == ck.R);
     const bool wide = ck.dtype != RR_FP32 && ck.wire == RR_FP32;  // eight binary32 accumulators: 128 registers
-    l->direct_occ = (U == 1 && ck.op != RR_OP_ALLGATHER && !full_batch && !wide) ? 3 : 2;
+    l->direct_occ = (U <= 2 && ck.op != RR_OP_ALLGATHER && !full_batch && !wide) ? 3 : 2;
     const unsigned long long vecs = n_bulk * E / 16;
     const unsigned long long blocks = (vecs + (unsigned long long)l->threads * U - 1) / ((unsigned long long)l->threads * U);
     const unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);

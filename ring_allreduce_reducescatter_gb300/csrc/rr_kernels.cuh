@@ -646,11 +646,14 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
       if constexpr (multi && !wide) {
         if (p.direct_u >= 4) return launch_kernel(rr_direct_kernel<OP, DT, WT, 4, 2>, l, 0, s, p);
       }
+      if constexpr (multi && !wide) {
+        if (p.direct_u >= 2)
+          return l.direct_occ == 3 ? launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 3>, l, 0, s, p)
+                                   : launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
+        if (l.direct_occ == 3) return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 3>, l, 0, s, p);
+      }
       if constexpr (multi) {
         if (p.direct_u >= 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
-        if constexpr (!wide) {
-          if (l.direct_occ == 3) return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 3>, l, 0, s, p);
-        }
       }
       return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
     }

@@ -276,12 +276,7 @@ def test_planner_paths(L):
     assert plan_dev(L, AR, 8, 1 << 28, F16)[1]["path"] == DIRECT
     assert plan_dev(L, AR, 32, 1 << 20, F16)[1]["path"] == DIRECT
     assert plan_dev(L, AR, 2, 1 << 28, F16)[1]["path"] == BULK
-    assert plan_dev(L, AR, 4, 4 << 20, F32)[1]["path"] == BULK        # 16 MiB per rank
-    assert plan_dev(L, AR, 4, 64 << 20, F32)[1]["path"] == DIRECT     # 256 MiB per rank
-    assert plan_dev(L, AR, 4, 1 << 18, F32)[1]["path"] == DIRECT      # 1 MiB per rank
-    assert plan_dev(L, AR, 3, 1 << 20, F32)[1]["path"] == DIRECT      # 4 MiB per rank
-    assert plan_dev(L, AR, 3, 1 << 22, F32)[1]["path"] == BULK        # 16 MiB per rank
-    for R in (5, 6, 7, 9, 12, 24, 32):
+    for R in (3, 4, 5, 6, 7, 9, 12, 24, 32):
         assert plan_dev(L, AR, R, 1 << 26, F32)[1]["path"] == DIRECT
     assert plan_dev(L, AR, 16, 1 << 22, F32)[1]["path"] == DIRECT     # 16 MiB per rank
     assert plan_dev(L, AR, 16, 1 << 24, F32)[1]["path"] == BULK       # 64 MiB per rank
