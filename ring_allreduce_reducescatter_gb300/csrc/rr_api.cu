@@ -240,18 +240,21 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     if (U > 2 && ck.dtype != RR_FP32 && ck.wire == RR_FP32) U = 2;  // binary32 accumulators are twice as wide
     p->direct_u = U;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
-    // (measured at 256 MiB, of the copy bandwidth: R = 5 0.88 -> 0.98, R = 9
-    // 0.93 -> 0.99, R = 3 0.85 -> 0.96).  Threads whose group is exactly one
-    // batch of seven or eight loads (R = 7 or 8; two-level rings of 4- or
-    // 8-rank groups) keep DRAM busy with two, which did better from 64 MiB
-    // (R = 8, 256 MiB: 1.006 against 0.991); flat rings of three or four ranks
-    // (two vectors a thread) do not.
+    // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5
+    // 0.88 -> 0.98, R = 9 0.93 -> 0.99, R = 3 0.85 -> 0.96).  A grid that
+    // two CTAs per SM cover in one wave (twice that for 16 or more ranks)
+    // finishes sooner with the 128-register code (1 MiB: 3-10 %).  Threads
+    // whose group is exactly one batch of seven or eight loads (R = 7 or 8;
+    // two-level rings of 4- or 8-rank groups) keep DRAM busy with two, which
+    // did better from 64 MiB (R = 8, 256 MiB: 1.006 against 0.991); flat rings
+    // of three or four ranks (two vectors a thread) do not.
+    const unsigned long long vecs = n_bulk * E / 16;
     const unsigned long long msg_bytes = (unsigned long long)ck.count * E;
     const int batch = U * ck.L;  // loads of one group a thread issues together
     const bool full_batch = (batch == 7 || batch == 8) && msg_bytes >= (64ull << 20) && !(U == 2 && ck.L == ck.R);
     const bool wide = ck.dtype != RR_FP32 && ck.wire == RR_FP32;  // eight binary32 accumulators: 128 registers
-    l->direct_occ = (U <= 2 && ck.op != RR_OP_ALLGATHER && !full_batch && !wide) ? 3 : 2;
-    const unsigned long long vecs = n_bulk * E / 16;
+    const bool looping = vecs > (unsigned long long)sms * 512ull * (unsigned long long)U * (ck.L >= 16 ? 2ull : 1ull);
+    l->direct_occ = (U <= 2 && ck.op != RR_OP_ALLGATHER && looping && !full_batch && !wide) ? 3 : 2;
     const unsigned long long blocks = (vecs + (unsigned long long)l->threads * U - 1) / ((unsigned long long)l->threads * U);
     const unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);
     // Vectors over a chunk boundary (ring order, boundaries off the 16-byte

@@ -337,6 +337,24 @@ def test_dependent_launch_chain(rr, path, early, N):
 
 
 @pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_direct_occupancy_variants(rr, dtype, wire):
+    """Messages large enough that the direct path's threads loop (the
+    85-register variant with one and two vectors a thread) and grouped rings
+    (the 128-register variant), with ragged chunk boundaries."""
+    V = 16 // torch.tensor([], dtype=dtype).element_size()
+    for R, group, N in ((3, 0, 3 * (1 << 19) + 5), (5, 0, 5 * 300_001), (9, 0, 9 * 200_003),
+                        (8, 4, 8 * 150_001), (16, 0, 16 * 160_001)):
+        xs = gen(R, N, dtype, 61 * R + group)
+        plan = rr.plan(rr.OP_ALLREDUCE, xs, [torch.empty_like(x) for x in xs], N, wire, group)
+        assert plan["path"] == rr.PATH_DIRECT or R == 16, plan
+        check_ar(rr, xs, wire, group=group, cfg=cfg_of(rr, path=rr.PATH_DIRECT),
+                 what=f"occupancy {NAME[dtype]}/{wire} R={R} group={group} N={N} V={V}")
+    R, N = 4, 4 * (1 << 19)
+    xs = gen(R, N, dtype, 67)
+    check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=f"occupancy RS {NAME[dtype]}/{wire}")
+
+
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
 def test_vectors_over_chunk_boundaries(rr, dtype, wire):
     """Chunk boundaries inside 16-byte vectors: the direct path's extra CTA
     folds those vectors in two ring orders at once (and chunks shorter than a
