@@ -131,6 +131,10 @@ rr_status ring_reduce_scatter_ex(const void *const *in_bufs, void *const *out_bu
  * in_bufs[c]: ring_chunk_count(count, R, c) elements (chunk c).  out_bufs[r]:
  * `count` elements; every output receives all chunks in order:
  *   out_bufs[r][ring_chunk_offset(count, R, c) + j] = in_bufs[c][j].
+ * Every AllGather schedule on the pages (the ring, the tree of recursive
+ * doubling, gather to one rank then broadcast) delivers exactly these copies;
+ * with all ranks in one GPU's memory the kernel is the copy itself, so this
+ * one entry point stands for all of them.
  */
 rr_status ring_allgather(const void *const *in_bufs, void *const *out_bufs, int R, size_t count,
                          rr_dtype dtype, cudaStream_t stream);

@@ -88,6 +88,9 @@ def load(path: str):
     L.orc_allreduce_algo.argtypes = [vpp, vpp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.POINTER(Opts)]
     L.orc_allreduce_algo.restype = ctypes.c_int
+    L.orc_allgather_algo.argtypes = [vpp, vpp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                     ctypes.POINTER(Opts)]
+    L.orc_allgather_algo.restype = ctypes.c_int
     L.orc_fold_gathered_algo.argtypes = [vpp, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     L.orc_fold_gathered_algo.restype = ctypes.c_int
@@ -218,6 +221,17 @@ def allgather(ins, count, dtype="f32", trace_cap=0, fault=None, poll_limit=0):
     outs = [np.empty(count, dtype=NP_STORAGE[dtype]) for _ in range(R)]
     o, sent, tr = _opts(R, trace_cap, fault, poll_limit)
     st = lib().orc_allgather(_ptrs(ins), _ptrs(outs), R, count, DTYPES[dtype], ctypes.byref(o))
+    return _finish(st, outs, o, sent, tr, R)
+
+
+def allgather_algo(ins, count, dtype="f32", algo="ring", trace_cap=0, fault=None, poll_limit=0):
+    """Literal AllGather by schedule ("ring", "hd" = the tree / recursive doubling, "naive" =
+    gather to rank 0 then broadcast); ins[c] holds chunk c of a ``count``-element vector."""
+    R = len(ins)
+    _check(ins, dtype)
+    outs = [np.empty(count, dtype=NP_STORAGE[dtype]) for _ in range(R)]
+    o, sent, tr = _opts(R, trace_cap, fault, poll_limit)
+    st = lib().orc_allgather_algo(_ptrs(ins), _ptrs(outs), R, count, DTYPES[dtype], ALGOS[algo], ctypes.byref(o))
     return _finish(st, outs, o, sent, tr, R)
 
 

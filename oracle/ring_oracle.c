@@ -668,6 +668,91 @@ static void naive_reduce_broadcast(ring_sim *s, int R, size_t count) {
   }
 }
 
+/* first chunk held by virtual rank v of the tree AllGather (v = P: the end) */
+static int tree_first_chunk(int v, int E) { return v < E ? 2 * v : v + E; }
+
+static void tree_allgather(ring_sim *s, int R, size_t count) {
+  const int P = floor_pow2(R), E = R - P, steps = log2_exact(P);
+  for (int k = 0; k < E; k++) /* the extra ranks hand their chunks to their odd neighbours */
+    sim_send(s, ORC_PHASE_PRE, 0, 2 * k, 2 * k + 1, 2 * k, orc_chunk_off(count, R, 2 * k),
+             orc_chunk_len(count, R, 2 * k));
+  for (int k = 0; k < E && s->status == ORC_OK; k++)
+    recv_copy(s, 2 * k + 1, 2 * k, 2 * k, orc_chunk_off(count, R, 2 * k), orc_chunk_len(count, R, 2 * k));
+  /* virtual rank v holds the chunks of virtual ranks [lo[v], hi[v]) */
+  int lo[64], hi[64];
+  for (int v = 0; v < P; v++) {
+    lo[v] = v;
+    hi[v] = v + 1;
+  }
+  for (int t = 0; t < steps && s->status == ORC_OK; t++) {
+    const int d = 1 << t;
+    for (int v = 0; v < P; v++) {
+      const int c0 = tree_first_chunk(lo[v], E), c1 = tree_first_chunk(hi[v], E);
+      const size_t a = orc_chunk_off(count, R, c0), b = c1 >= R ? count : orc_chunk_off(count, R, c1);
+      sim_send(s, ORC_PHASE_AG, t, hd_rank(v, E), hd_rank(v ^ d, E), c0, a, b - a);
+    }
+    int new_lo[64], new_hi[64];
+    for (int v = 0; v < P && s->status == ORC_OK; v++) {
+      const int u = v ^ d;
+      const int c0 = tree_first_chunk(lo[u], E), c1 = tree_first_chunk(hi[u], E);
+      const size_t a = orc_chunk_off(count, R, c0), b = c1 >= R ? count : orc_chunk_off(count, R, c1);
+      recv_copy(s, hd_rank(v, E), hd_rank(u, E), c0, a, b - a);
+      new_lo[v] = lo[v] < lo[u] ? lo[v] : lo[u];
+      new_hi[v] = hi[v] > hi[u] ? hi[v] : hi[u];
+    }
+    for (int v = 0; v < P; v++) {
+      lo[v] = new_lo[v];
+      hi[v] = new_hi[v];
+    }
+  }
+  for (int k = 0; k < E && s->status == ORC_OK; k++) sim_send(s, ORC_PHASE_POST, 0, 2 * k + 1, 2 * k, -1, 0, count);
+  for (int k = 0; k < E && s->status == ORC_OK; k++) recv_copy(s, 2 * k, 2 * k + 1, -1, 0, count);
+}
+
+static void naive_gather_broadcast(ring_sim *s, int R, size_t count) {
+  for (int k = 1; k < R && s->status == ORC_OK; k++) { /* rank 0 collects chunk k */
+    const size_t off = orc_chunk_off(count, R, k), len = orc_chunk_len(count, R, k);
+    sim_send(s, ORC_PHASE_RS, k - 1, k, 0, k, off, len);
+    recv_copy(s, 0, k, k, off, len);
+  }
+  for (int k = 1; k < R && s->status == ORC_OK; k++) { /* and sends the whole vector out */
+    sim_send(s, ORC_PHASE_AG, k - 1, 0, k, -1, 0, count);
+    recv_copy(s, k, 0, -1, 0, count);
+  }
+}
+
+int orc_allgather_algo(const void *const *in, void *const *out, int R, size_t count, int dtype, int algo,
+                       orc_opts *opts) {
+  if (algo == ORC_ALGO_RING) return orc_allgather(in, out, R, count, dtype, opts);
+  if (algo != ORC_ALGO_HALVING_DOUBLING && algo != ORC_ALGO_NAIVE) return ORC_EINVAL;
+  if (R < 1 || R > 64 || !in || !out) return ORC_EINVAL;
+  if (!valid_type(dtype)) return ORC_EUNSUPPORTED;
+  for (int r = 0; r < R; r++) {
+    if (count > 0 && !out[r]) return ORC_EINVAL;
+    if (orc_chunk_len(count, R, r) > 0 && !in[r]) return ORC_EINVAL;
+  }
+  ring_sim s;
+  int st = sim_init(&s, R, dtype, count, count, opts);
+  if (st != ORC_OK) {
+    sim_free(&s);
+    return st;
+  }
+  for (int r = 0; r < R; r++) { /* rank r starts with chunk r */
+    size_t off = orc_chunk_off(count, R, r), len = orc_chunk_len(count, R, r);
+    if (len) memcpy(s.W[r] + off * s.ew, in[r], len * s.ew);
+  }
+  if (algo == ORC_ALGO_NAIVE)
+    naive_gather_broadcast(&s, R, count);
+  else
+    tree_allgather(&s, R, count);
+  if (s.status == ORC_OK)
+    for (int r = 0; r < R; r++)
+      if (count) memcpy(out[r], s.W[r], count * s.ew);
+  st = s.status;
+  sim_free(&s);
+  return st;
+}
+
 int orc_allreduce_algo(const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
                        int algo, orc_opts *opts) {
   if (algo == ORC_ALGO_RING) return orc_allreduce(in, out, R, count, dtype, wire, 0, opts);

@@ -169,6 +169,22 @@ int orc_allgather(const void *const *in, void *const *out, int R, size_t count, 
 int orc_allreduce_algo(const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
                        int algo, orc_opts *opts);
 
+/*
+ * AllGather by schedule (in/out as orc_allgather; every schedule delivers the
+ * same copies, only the messages differ).  ORC_ALGO_RING is orc_allgather.
+ * ORC_ALGO_NAIVE (gather, then broadcast): ranks 1..R-1 send their chunks to
+ * rank 0 in rank order, then rank 0 sends the whole vector to ranks 1..R-1.
+ * ORC_ALGO_HALVING_DOUBLING (the tree AllGather, recursive doubling; reading:
+ * the textbook schedule, the pages give no steps): with P the largest power
+ * of two <= R and E = R - P, rank 2k (k < E) first sends its chunk to rank
+ * 2k+1; virtual rank v (rank 2v+1 for v < E, rank v+E otherwise) then holds
+ * a contiguous run of chunks, and at step t = 0..log2(P)-1 virtual ranks v and
+ * v ^ 2^t swap everything they hold; rank 2k+1 finally sends the whole vector
+ * to rank 2k.
+ */
+int orc_allgather_algo(const void *const *in, void *const *out, int R, size_t count, int dtype, int algo,
+                       orc_opts *opts);
+
 /* Closed form of orc_allreduce_algo at sampled elements (as orc_fold_gathered). */
 int orc_fold_gathered_algo(const void *const *vals, const uint64_t *idx, size_t n, int R, size_t count,
                            int dtype, int wire, int algo, void *out);

@@ -83,6 +83,70 @@ def pin_algo_traffic_and_schedule():
             assert hd.sent_bytes == [2 * (R - 1) * S // R] * R  # the same volume as the ring
 
 
+def ag_inputs(rng, R, N, dtype):
+    """Chunk c of a random N-element vector, for c < R."""
+    full = rand_inputs(rng, 1, N, dtype)[0]
+    return full, [full[oracle.chunk_off(N, R, c):oracle.chunk_off(N, R, c) + oracle.chunk_len(N, R, c)].copy()
+                  for c in range(R)]
+
+
+def pin_allgather_schedules():
+    """Every AllGather schedule delivers, to every rank, the chunks in place:
+    out[r][off(c) + j] = in[c][j] (the definition, built here with numpy)."""
+    rng = np.random.default_rng(35)
+    for dtype in ("f32", "f16", "bf16"):
+        for R in (1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16, 17):
+            for N in (0, 1, R - 1, R, 4 * R + 3, 1001):
+                full, chunks = ag_inputs(rng, R, N, dtype)
+                for algo in ("ring", "hd", "naive"):
+                    res = oracle.allgather_algo(chunks, N, dtype, algo)
+                    assert res.status == oracle.OK, (dtype, R, N, algo, res.status)
+                    for r in range(R):
+                        assert bits(res.outs[r]).tolist() == bits(full).tolist(), (dtype, R, N, algo, r)
+
+
+def pin_allgather_traffic_and_schedule():
+    for R in RS_:
+        N = 4 * R * 3
+        full, chunks = ag_inputs(np.random.default_rng(R), R, N, "f32")
+        S = 4 * N
+        nv = oracle.allgather_algo(chunks, N, "f32", "naive", trace_cap=1 << 14)
+        assert nv.sent_bytes == [(R - 1) * S] + [S // R] * (R - 1)  # chunks in, whole vectors out
+        tr = oracle.allgather_algo(chunks, N, "f32", "hd", trace_cap=1 << 14)
+        P = 1
+        while P * 2 <= R:
+            P *= 2
+        E, steps = R - P, P.bit_length() - 1
+        ag = [m for m in tr.trace if m[0] == oracle.PHASE_AG]
+        assert len(ag) == P * steps  # log2(P) steps of P messages
+        assert len([m for m in tr.trace if m[0] == oracle.PHASE_PRE]) == E
+        assert len([m for m in tr.trace if m[0] == oracle.PHASE_POST]) == E
+        vrank = {(2 * v + 1 if v < E else v + E): v for v in range(P)}
+        for (_, t, src, dst, _, nbytes) in ag:  # partners 1, 2, 4, ... apart, each step doubling the data
+            assert vrank[src] ^ vrank[dst] == 1 << t
+            if E == 0:
+                assert nbytes == (1 << t) * S // R
+        if E == 0:
+            assert tr.sent_bytes == [(R - 1) * S // R] * R  # the same volume as the ring AllGather
+
+
+def test_allgather_schedules_deliver_the_definition():
+    pin_allgather_schedules()
+
+
+def test_allgather_traffic_and_schedule():
+    pin_allgather_traffic_and_schedule()
+
+
+def test_allgather_schedule_faults():
+    full, chunks = ag_inputs(np.random.default_rng(36), 6, 600, "f32")
+    r = oracle.allgather_algo(chunks, 600, "f32", "hd", fault=(oracle.FAULT_DROP, 1, oracle.PHASE_AG, 1))
+    assert r.status == oracle.ETIMEOUT
+    r = oracle.allgather_algo(chunks, 600, "f32", "naive", fault=(oracle.FAULT_DUP, 2, oracle.PHASE_RS, 1))
+    assert r.status == oracle.EPROTO
+    assert oracle.allgather_algo(chunks, 600, "f32", "hd").status == oracle.OK
+
+
 def test_golden_algorithms():
     pin_golden_algorithms()
 
@@ -147,6 +211,15 @@ MUTATIONS = {
     # the collector adds in reverse rank order
     "naive_order": ("      y = x[0];\n      for (int r = 1; r < R; r++) y = orc_wire_add(wire, y, x[r]);",
                     "      y = x[R - 1];\n      for (int r = R - 2; r >= 0; r--) y = orc_wire_add(wire, y, x[r]);"),
+    # the tree AllGather starts with the farthest partner
+    "tree_ag_partner_order": ("    const int d = 1 << t;\n    for (int v = 0; v < P; v++) {\n      const int c0 = tree_first_chunk",
+                              "    const int d = P >> (t + 1);\n    for (int v = 0; v < P; v++) {\n      const int c0 = tree_first_chunk"),
+    # the extra rank's chunk lands one chunk off
+    "tree_ag_extra_chunk": ("static int tree_first_chunk(int v, int E) { return v < E ? 2 * v : v + E; }",
+                            "static int tree_first_chunk(int v, int E) { return v < E ? 2 * v + 1 : v + E; }"),
+    # the broadcast skips the last rank
+    "naive_ag_broadcast": ("  for (int k = 1; k < R && s->status == ORC_OK; k++) { /* and sends the whole vector out */",
+                           "  for (int k = 1; k < R - 1 && s->status == ORC_OK; k++) { /* and sends the whole vector out */"),
 }
 
 
@@ -158,7 +231,8 @@ def test_planted_mistake_in_algorithms_is_caught(name, tmp_path, monkeypatch):
     lib = oracle.load(oracle.build_variant(src.replace(old, new), str(tmp_path / "libvariant.so")))
     monkeypatch.setattr(oracle, "_lib", lib)
     caught = []
-    for pin in (pin_golden_algorithms, pin_algo_closed_form, pin_algo_integers, pin_algo_traffic_and_schedule):
+    for pin in (pin_golden_algorithms, pin_algo_closed_form, pin_algo_integers, pin_algo_traffic_and_schedule,
+                pin_allgather_schedules, pin_allgather_traffic_and_schedule):
         try:
             pin()
         except (AssertionError, RuntimeError, KeyError):

@@ -199,6 +199,23 @@ def test_allgather_grid(rr, dtype, R):
             check_ag(rr, chunks, N, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
 
 
+@pytest.mark.parametrize("algo", ["hd", "naive"])
+def test_allgather_equals_every_schedule(rr, algo):
+    """On one GPU the AllGather is a copy: ring_allgather's outputs equal the
+    oracle's tree (recursive doubling) and gather-broadcast schedules bit for bit."""
+    for dtype in (torch.float32, torch.float16, torch.bfloat16):
+        for R in (3, 5, 8, 12):
+            N = R * 4099 + 5
+            lens = [oracle.chunk_len(N, R, c) for c in range(R)]
+            chunks = gen(R, 0, dtype, 71 * R, lengths=lens)
+            outs = rr.allgather(chunks, N)
+            torch.cuda.synchronize()
+            ref = oracle.allgather_algo([host(c) for c in chunks], N, NAME[dtype], algo)
+            assert ref.status == oracle.OK
+            for r in range(R):
+                assert_same(host(outs[r]), ref.outs[r], f"AG vs {algo} {NAME[dtype]} R={R} rank {r}")
+
+
 def test_aligned_paths_are_chosen_when_aligned(rr):
     xs = gen(8, 1 << 20, torch.float16, 5)
     outs = [torch.empty_like(x) for x in xs]
