@@ -69,7 +69,7 @@ def measured_hbm_peak():
 
 DEVICE_SOURCES = ("rr_kernels.cuh", "rr_device.cuh", "rr_params.h", "rr_inst_f32.cu", "rr_inst_f16.cu",
                   "rr_inst_bf16.cu", "rr_hd_direct.cuh", "rr_inst_hd_f32.cu", "rr_inst_hd_f16.cu",
-                  "rr_inst_hd_bf16.cu")
+                  "rr_inst_hd_bf16.cu", "rr_inst_f32_narrow.cu")
 
 
 def kernel_sources_digest():

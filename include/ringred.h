@@ -331,6 +331,14 @@ rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t s
 /* RR_ABI_VERSION of the library. */
 int ring_abi_version(void);
 
+/*
+ * The CUDA runtime error (a cudaError_t value) behind the calling thread's
+ * most recent RR_ERR_CUDA, or 0 if it has had none, and the runtime's
+ * description of it ("no CUDA error" for 0; a static string).
+ */
+int ring_last_cuda_error(void);
+const char *ring_last_cuda_error_string(void);
+
 #ifdef __cplusplus
 }
 #endif

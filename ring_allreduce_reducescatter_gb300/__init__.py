@@ -65,7 +65,12 @@ def rank_buffers(R: int, count, dtype: torch.dtype, device=None, stagger_bytes: 
 class RingError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.cuda_error = 0
+        msg = f"{what}: {status_string(status)} (status {status})"
+        if status == ERR_CUDA:
+            self.cuda_error = int(lib().ring_last_cuda_error())
+            msg += f": CUDA error {self.cuda_error}, {lib().ring_last_cuda_error_string().decode()}"
+        super().__init__(msg)
 
 
 class LaunchCfg(ctypes.Structure):
@@ -124,6 +129,10 @@ def lib() -> ctypes.CDLL:
         L.ring_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
         L.ring_abi_version.argtypes = []
         L.ring_abi_version.restype = i
+        L.ring_last_cuda_error.argtypes = []
+        L.ring_last_cuda_error.restype = i
+        L.ring_last_cuda_error_string.argtypes = []
+        L.ring_last_cuda_error_string.restype = ctypes.c_char_p
         _lib = L
     return _lib
 

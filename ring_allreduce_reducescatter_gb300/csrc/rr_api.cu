@@ -26,20 +26,29 @@ struct DeviceInfo {
 };
 
 constexpr int kMaxDevices = 64;
+
+// The CUDA runtime error behind the calling thread's last RR_ERR_CUDA.
+thread_local int g_last_cuda_error = 0;
+bool cuda_ok(cudaError_t e) {
+  if (e == cudaSuccess) return true;
+  g_last_cuda_error = (int)e;
+  return false;
+}
+
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_devices_mu;
 
 rr_status current_device(DeviceInfo *out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
+  if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_devices_mu);
   DeviceInfo &d = g_devices[dev];
   if (!d.valid) {
     void *addr = nullptr;
-    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaGetSymbolAddress(&addr, g_rr_status_word) != cudaSuccess)
+    if (!cuda_ok(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) ||
+        !cuda_ok(cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) ||
+        !cuda_ok(cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) ||
+        !cuda_ok(cudaGetSymbolAddress(&addr, g_rr_status_word)))
       return RR_ERR_CUDA;
     d.status = static_cast<unsigned int *>(addr);
     d.valid = true;
@@ -255,6 +264,11 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     const bool wide = ck.dtype != RR_FP32 && ck.wire == RR_FP32;  // eight binary32 accumulators: 128 registers
     const bool looping = vecs > (unsigned long long)sms * 512ull * (unsigned long long)U * (ck.L >= 16 ? 2ull : 1ull);
     l->direct_occ = (U <= 2 && ck.op != RR_OP_ALLGATHER && looping && !full_batch && !wide) ? 3 : 2;
+    // Halving-doubling loads a whole tree (up to 16 vectors) per batch: a third
+    // CTA helped only below seven ranks (R = 5: 0.85 -> 1.00 at 256 MiB; R = 12:
+    // 1.01 -> 0.99).
+    if (ck.algo == RR_ALGO_HALVING_DOUBLING)
+      l->direct_occ = (ck.R < 7 && looping && !wide) ? 3 : 2;
     const unsigned long long blocks = (vecs + (unsigned long long)l->threads * U - 1) / ((unsigned long long)l->threads * U);
     const unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);
     // Vectors over a chunk boundary (ring order, boundaries off the 16-byte
@@ -412,7 +426,7 @@ rr_status launch_checked(const Checked &ck, const void *const *in, void *const *
     e = rr::launch_f16(ck.op, ck.wire, p, l, stream);
   else
     e = rr::launch_bf16(ck.op, ck.wire, p, l, stream);
-  return e == cudaSuccess ? RR_OK : RR_ERR_CUDA;
+  return cuda_ok(e) ? RR_OK : RR_ERR_CUDA;
 }
 
 rr_status run(int op, const void *const *in, void *const *out, int R, size_t count, int dtype, int wire,
@@ -441,18 +455,18 @@ Pipe g_pipes[kMaxDevices];
 
 rr_status pipe_for_current_device(Pipe **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
+  if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
   Pipe &pp = g_pipes[dev];
   std::lock_guard<std::mutex> lock(g_devices_mu);
   if (!pp.valid) {
-    if (cudaStreamCreateWithFlags(&pp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&pp.d2h, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&pp.start, cudaEventDisableTiming) != cudaSuccess)
+    if (!cuda_ok(cudaStreamCreateWithFlags(&pp.h2d, cudaStreamNonBlocking)) ||
+        !cuda_ok(cudaStreamCreateWithFlags(&pp.d2h, cudaStreamNonBlocking)) ||
+        !cuda_ok(cudaEventCreateWithFlags(&pp.start, cudaEventDisableTiming)))
       return RR_ERR_CUDA;
     for (int k = 0; k < kHostSlots; ++k)
-      if (cudaEventCreateWithFlags(&pp.copied_in[k], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&pp.folded[k], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&pp.copied_out[k], cudaEventDisableTiming) != cudaSuccess)
+      if (!cuda_ok(cudaEventCreateWithFlags(&pp.copied_in[k], cudaEventDisableTiming)) ||
+          !cuda_ok(cudaEventCreateWithFlags(&pp.folded[k], cudaEventDisableTiming)) ||
+          !cuda_ok(cudaEventCreateWithFlags(&pp.copied_out[k], cudaEventDisableTiming)))
         return RR_ERR_CUDA;
     pp.valid = true;
   }
@@ -485,7 +499,7 @@ rr_status host_pipeline(const void *const *host_in, void *const *host_out, int R
   st = pipe_for_current_device(&pp);
   if (st != RR_OK) return st;
   std::lock_guard<std::mutex> lock(pp->mu);
-  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  auto ok = [](cudaError_t e) { return cuda_ok(e); };
   // the copies start after the work already enqueued on `stream`
   if (!ok(cudaEventRecord(pp->start, stream)) || !ok(cudaStreamWaitEvent(pp->h2d, pp->start, 0))) return RR_ERR_CUDA;
   const size_t pieces = (count + piece - 1) / piece;
@@ -544,11 +558,11 @@ std::mutex g_static_scratch_mu;
 // Once per device, with that device current: look up the array's device address.
 rr_status static_scratch_for_current_device(unsigned char **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
+  if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= kMaxDevices) return RR_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_static_scratch_mu);
   if (!g_static_scratch_addr[dev]) {
     void *addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_rr_static_scratch) != cudaSuccess || !addr) return RR_ERR_CUDA;
+    if (!cuda_ok(cudaGetSymbolAddress(&addr, g_rr_static_scratch)) || !addr) return RR_ERR_CUDA;
     g_static_scratch_addr[dev] = static_cast<unsigned char *>(addr);
   }
   *out = g_static_scratch_addr[dev];
@@ -663,9 +677,9 @@ rr_status ring_device_status(unsigned int *flags) {
   rr_status st = current_device(&dev);
   if (st != RR_OK) return st;
   unsigned int v = 0, zero = 0;
-  if (cudaDeviceSynchronize() != cudaSuccess) return RR_ERR_CUDA;
-  if (cudaMemcpyFromSymbol(&v, g_rr_status_word, sizeof(v)) != cudaSuccess) return RR_ERR_CUDA;
-  if (v != 0 && cudaMemcpyToSymbol(g_rr_status_word, &zero, sizeof(zero)) != cudaSuccess) return RR_ERR_CUDA;
+  if (!cuda_ok(cudaDeviceSynchronize())) return RR_ERR_CUDA;
+  if (!cuda_ok(cudaMemcpyFromSymbol(&v, g_rr_status_word, sizeof(v)))) return RR_ERR_CUDA;
+  if (v != 0 && !cuda_ok(cudaMemcpyToSymbol(g_rr_status_word, &zero, sizeof(zero)))) return RR_ERR_CUDA;
   *flags = v;
   return RR_OK;
 }
@@ -675,8 +689,8 @@ rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t s
   DeviceInfo dev;
   rr_status st = current_device(&dev);
   if (st != RR_OK) return st;
-  if (rr::launch_wait_probe(dev.status, limit_ns, stream) != cudaSuccess) return RR_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return RR_ERR_CUDA;
+  if (!cuda_ok(rr::launch_wait_probe(dev.status, limit_ns, stream))) return RR_ERR_CUDA;
+  if (!cuda_ok(cudaStreamSynchronize(stream))) return RR_ERR_CUDA;
   unsigned int flags = 0;
   st = ring_device_status(&flags);
   if (st != RR_OK) return st;
@@ -684,6 +698,12 @@ rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t s
 }
 
 int ring_abi_version(void) { return RR_ABI_VERSION; }
+
+int ring_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *ring_last_cuda_error_string(void) {
+  return g_last_cuda_error ? cudaGetErrorString((cudaError_t)g_last_cuda_error) : "no CUDA error";
+}
 
 rr_status ring_allreduce_algo(const void *const *in_bufs, void *const *out_bufs, int R, size_t count, rr_dtype dtype,
                               rr_dtype wire, rr_algo algo, const rr_launch_cfg *cfg, cudaStream_t stream) {

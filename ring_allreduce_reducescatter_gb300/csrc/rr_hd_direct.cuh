@@ -60,8 +60,28 @@ __device__ __forceinline__ typename VT::W hd_vec(const RingParams &p, unsigned l
   }
 }
 
+// Element i by the same tree, with scalar loads (the ragged end).
 template <int DT, int WT, int LOG2P, bool EXTRA>
-__global__ void __launch_bounds__(kDirectThreads, 2) rr_hd_direct_kernel(const __grid_constant__ RingParams p) {
+__device__ __forceinline__ typename Fmt<DT>::type hd_scalar(const RingParams &p, unsigned long long i) {
+  using S = typename Fmt<DT>::type;
+  using SC = Scalar<DT, WT>;
+  using W = typename SC::W;
+  const int Ex = EXTRA ? p.hd_extra : 0;
+  auto x = [&](int r) { return SC::in(static_cast<const S *>(p.in[r])[i]); };
+  auto leaf = [&](int v) {
+    if constexpr (EXTRA) {
+      if (v < Ex) return hop(x(2 * v), x(2 * v + 1));
+    }
+    return x(v + Ex);
+  };
+  auto add = [](W a, W b) { return hop(a, b); };
+  return SC::out(hd_tree<LOG2P, W>(leaf, add));
+}
+
+// OCC: 256-thread CTAs per SM the registers are budgeted for, as for the ring's
+// direct kernel.
+template <int DT, int WT, int LOG2P, bool EXTRA, int OCC>
+__global__ void __launch_bounds__(kDirectThreads, OCC) rr_hd_direct_kernel(const __grid_constant__ RingParams p) {
   grid_dependency_wait();
   grid_dependents_launch();
   using VT = Vec<DT, WT>;
@@ -75,16 +95,28 @@ __global__ void __launch_bounds__(kDirectThreads, 2) rr_hd_direct_kernel(const _
     for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, res);
   }
   // the ragged end (under 16 bytes per rank)
-  for (unsigned long long i = p.n_bulk + (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count; i += T)
-    element_op<kOpAllReduce, DT, WT, true>(p, i);
+  for (unsigned long long i = p.n_bulk + (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count;
+       i += T) {
+    const typename Fmt<DT>::type y = hd_scalar<DT, WT, LOG2P, EXTRA>(p, i);
+    for (int r = 0; r < p.R; ++r) static_cast<typename Fmt<DT>::type *>(p.out[r])[i] = y;
+  }
+}
+
+template <int DT, int WT, int LOG2P, bool EXTRA>
+cudaError_t launch_occ(const RingParams &p, const Launch &l, cudaStream_t s) {
+  constexpr bool wide = DT != kF32 && WT == kF32;
+  if constexpr (!wide) {
+    if (l.direct_occ == 3) return launch_kernel(rr_hd_direct_kernel<DT, WT, LOG2P, EXTRA, 3>, l, 0, s, p);
+  }
+  return launch_kernel(rr_hd_direct_kernel<DT, WT, LOG2P, EXTRA, 2>, l, 0, s, p);
 }
 
 template <int DT, int WT, int LOG2P>
 cudaError_t launch_size(const RingParams &p, const Launch &l, cudaStream_t s) {
   if constexpr (LOG2P > 0) {
-    if (p.hd_extra > 0) return launch_kernel(rr_hd_direct_kernel<DT, WT, LOG2P, true>, l, 0, s, p);
+    if (p.hd_extra > 0) return launch_occ<DT, WT, LOG2P, true>(p, l, s);
   }
-  return launch_kernel(rr_hd_direct_kernel<DT, WT, LOG2P, false>, l, 0, s, p);
+  return launch_occ<DT, WT, LOG2P, false>(p, l, s);
 }
 
 template <int DT, int WT>

@@ -1,5 +1,5 @@
-// rr_inst_f32.cu -- kernels with binary32 storage (wire: binary32, bfloat16
-// or binary16), and the bounded-wait probe kernel.
+// rr_inst_f32.cu -- kernels with binary32 storage on a binary32 wire (the
+// 16-bit wires are in rr_inst_f32_narrow.cu), and the bounded-wait probe kernel.
 #include "rr_kernels.cuh"
 
 namespace rr {
@@ -23,14 +23,10 @@ cudaError_t launch_f32(int op, int wire, const RingParams &p, const Launch &l, c
   switch (op) {
     case kOpAllReduce:
       if (wire == kF32) return launch_one<kOpAllReduce, kF32, kF32>(p, l, s);
-      if (wire == kBF16) return launch_one<kOpAllReduce, kF32, kBF16>(p, l, s);
-      if (wire == kF16) return launch_one<kOpAllReduce, kF32, kF16>(p, l, s);
-      break;
+      return launch_f32_narrow(op, wire, p, l, s);
     case kOpReduceScatter:
       if (wire == kF32) return launch_one<kOpReduceScatter, kF32, kF32>(p, l, s);
-      if (wire == kBF16) return launch_one<kOpReduceScatter, kF32, kBF16>(p, l, s);
-      if (wire == kF16) return launch_one<kOpReduceScatter, kF32, kF16>(p, l, s);
-      break;
+      return launch_f32_narrow(op, wire, p, l, s);
     case kOpAllGather:
       return launch_one<kOpAllGather, kF32, kF32>(p, l, s);
   }

@@ -59,6 +59,7 @@ struct Launch {
 // Defined in rr_inst_<storage>.cu: launch the kernel of (op, storage dtype,
 // wire) on `stream`; returns the launch error.
 cudaError_t launch_f32(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+cudaError_t launch_f32_narrow(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
 cudaError_t launch_f16(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
 // Defined in rr_inst_hd_<storage>.cu: the halving-doubling AllReduce on the
 // direct path (one kernel per tree size).

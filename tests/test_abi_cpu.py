@@ -51,6 +51,21 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_last_cuda_error_is_recorded(L):
+    """Without a GPU a valid call fails in the runtime: RR_ERR_CUDA, and the
+    runtime error behind it is kept for the calling thread."""
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    rr.lib()
+    ins, outs = fake(4, 100, 4)
+    st = call(L, AR, ins, outs, 4, 100, F32)
+    assert st == ECUDA
+    assert L.ring_last_cuda_error() != 0
+    assert L.ring_last_cuda_error_string() not in (b"", b"no CUDA error")
+    err = rr.RingError(rr.ERR_CUDA, "probe")
+    assert err.cuda_error == L.ring_last_cuda_error() and "CUDA error" in str(err)
+
+
 def test_abi_version(L):
     assert L.ring_abi_version() == 2
 
