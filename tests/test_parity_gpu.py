@@ -461,6 +461,58 @@ def check_sampled(rr, xs, outs, wire=None, group=0, what=""):
                 f"{what}: output {r} differs from output 0"
 
 
+def big_inputs(R, N, dtype, seed, piece=1 << 28):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    xs = []
+    for _ in range(R):
+        x = torch.empty(N, dtype=dtype, device="cuda")
+        for a in range(0, N, piece):
+            b = min(N, a + piece)
+            x[a:b].copy_(torch.randn(b - a, generator=g, device="cuda") * 0.01)
+        xs.append(x)
+    return xs
+
+
+@pytest.mark.parametrize("R,N", [(2, (1 << 32) + (1 << 20) + 5), (3, (1 << 32) + 7)])
+def test_counts_beyond_32_bits(rr, R, N):
+    """Rank vectors of more than 2^32 elements (8 GiB of binary16 each): every
+    element index and byte offset needs 64 bits.  Each path, sampled against the
+    closed form (chunk boundaries, both ends, random elements)."""
+    xs = big_inputs(R, N, torch.float16, 81 + R)
+    outs = [torch.empty_like(x) for x in xs]
+    for path in (rr.PATH_AUTO, rr.PATH_DIRECT, rr.PATH_BULK, rr.PATH_SIMPLE):
+        for o in outs:
+            o.fill_(float("nan"))
+        rr.collective(rr.OP_ALLREDUCE, xs, outs, N, None, 0, None, cfg_of(rr, path=path))
+        torch.cuda.synchronize()
+        check_sampled(rr, xs, outs, what=f"N=2^32+{N - (1 << 32)} R={R} path={path}")
+    del xs, outs
+    torch.cuda.empty_cache()
+
+
+def test_reduce_scatter_beyond_32_bits(rr):
+    """ReduceScatter of two 2^32 + 16 element vectors: output chunks start past
+    the 8 GiB mark of the inputs."""
+    R, N = 2, (1 << 32) + 16
+    xs = big_inputs(R, N, torch.float16, 91)
+    base = N // R
+    outs = [torch.empty(base, dtype=torch.float16, device="cuda") for _ in range(R)]
+    idx = np.unique(np.concatenate([np.arange(0, 64), np.arange(base - 64, base),
+                                    np.random.default_rng(5).integers(0, base, 1 << 16)])).astype(np.int64)
+    for path in (rr.PATH_AUTO, rr.PATH_DIRECT, rr.PATH_BULK):
+        rr.collective(rr.OP_REDUCE_SCATTER, xs, outs, N, None, 0, None, cfg_of(rr, path=path))
+        torch.cuda.synchronize()
+        for c in range(R):
+            gi = idx + c * base  # global indices of chunk c's sampled elements
+            tg = torch.from_numpy(gi).cuda()
+            vals = [host(x[tg]) for x in xs]
+            want = oracle.fold_gathered(vals, gi.astype(np.uint64), N, "f16", None, 0)
+            assert_same(host(outs[c][torch.from_numpy(idx).cuda()]), want, f"RS 2^32+ path={path} chunk {c}")
+    del xs, outs
+    torch.cuda.empty_cache()
+
+
 def test_workload1_full(rr, wl):
     w = wl.config1()
     xs = wl.inputs(w, "cuda")
