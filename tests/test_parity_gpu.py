@@ -158,6 +158,34 @@ def test_allreduce_edge_grid(rr, dtype, wire, R):
              what=f"AR in place direct R={R}")
 
 
+@pytest.mark.parametrize("dtype,wire", [(torch.float32, None), (torch.float16, None), (torch.float32, "bf16"),
+                                        (torch.bfloat16, "f32")], ids=lambda v: str(v))
+def test_maximum_rank_counts(rr, dtype, wire):
+    """The largest rank counts (up to RR_MAX_RANKS = 64): flat and two-level
+    AllReduce, ReduceScatter and AllGather on every path."""
+    for R in (33, 64):
+        for N in (1, R - 1, R, R + 1, 4097, 64 * 1031 + 5):
+            xs = gen(R, N, dtype, 7 * R + N)
+            tag = f"max R={R} {NAME[dtype]}/{wire} N={N}"
+            check_ar(rr, xs, wire, what=tag)
+            check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_SIMPLE), what=tag + " simple")
+            if N * xs[0].element_size() >= 16:
+                check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
+                check_ar(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_BULK), what=tag + " bulk")
+            if R == 64 and N > R:
+                check_ar(rr, xs, wire, group=8, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " 8x8")
+                check_ar(rr, xs, wire, group=16, what=tag + " 4x16")
+    R = 64
+    N = R * 2048
+    xs = gen(R, N, dtype, 77)
+    check_rs(rr, xs, wire, what="max RS")
+    check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_BULK), what="max RS bulk")
+    if wire is None:
+        lens = [oracle.chunk_len(N + 13, R, c) for c in range(R)]
+        chunks = gen(R, 0, dtype, 78, lengths=lens)
+        check_ag(rr, chunks, N + 13, what="max AG")
+
+
 @pytest.mark.parametrize("G,L", [(2, 8), (2, 2), (3, 4), (4, 1), (2, 4), (8, 2)])
 @pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
 def test_two_level_grid(rr, G, L, dtype, wire):
