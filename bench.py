@@ -487,9 +487,10 @@ def run_ours(args):
     sampler = ClockSampler(gpu_id) if local == 0 else None
     time.sleep(0.5 if sampler else 0)
 
-    # timed region: exactly K steps, barrier + synchronize on both sides
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # timed region: exactly K steps, barrier + synchronize on both sides.  One
+    # ring kernel per step and nothing else on the stream, so the kernel's
+    # average launch duration is the region's time over K (events between the
+    # launches would also stop each launch from overlapping the one before).
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
@@ -498,16 +499,14 @@ def run_ours(args):
     region1 = torch.cuda.Event(enable_timing=True)
     region0.record(stream)
     for k in range(args.steps):
-        starts[k].record(stream)
         step()
-        ends[k].record(stream)
     region1.record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
     if pg:
         pg.barrier()
     region_ms = region0.elapsed_time(region1)
-    kern_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    kern_ms = region_ms / args.steps
     if rr.device_status() != 0:
         raise RuntimeError("device status set during the timed region")
     gpu_launches = args.steps  # one ring_allreduce kernel per step
