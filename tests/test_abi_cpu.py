@@ -46,6 +46,28 @@ def test_header_declares_the_collectives():
         assert want in names
 
 
+def test_header_is_c_and_links_from_c(L, tmp_path):
+    """include/ringred.h compiles as C11 (no CUDA or C++ headers) and a C
+    program links libringred.so and gets the documented answers."""
+    import subprocess
+
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    exe = tmp_path / "abi_from_c"
+    libdir = os.path.dirname(rr.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "csrc", "abi_from_c.c"), "-o", str(exe), "-L", libdir, "-lringred",
+                    f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    lines = dict(l.split(" ", 1) for l in out if l)
+    assert lines["abi"] == "2"
+    assert out[1:5] == ["chunk 0 2 0", "chunk 1 2 2", "chunk 2 2 4", "chunk 3 4 6"]
+    assert lines["bad_rank_count"] == str(EINVAL) and lines["bad_dtype"] == str(EINVAL)
+    assert lines["unsupported_pair"] == str(EUNSUP) and lines["alias"] == str(EALIAS)
+    assert lines["empty"] == str(OK)
+    assert "alias" in lines["status"].lower() or "overlap" in lines["status"].lower()
+
+
 def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
