@@ -143,9 +143,10 @@ rr_status ring_allgather(const void *const *in_bufs, void *const *out_bufs, int 
  * asynchronous copies (needs 16-byte aligned buffers, and for ReduceScatter /
  * AllGather chunk offsets that are multiples of 16 bytes); RR_PATH_DIRECT has
  * every thread load its ranks' 16-byte vectors straight from global memory
- * and store the results straight back (the same alignment needs, at most 256
- * threads per CTA; one memory round trip, for small messages); RR_PATH_SIMPLE
- * is one element per thread with plain loads and stores (any alignment). */
+ * and store the results straight back (16-byte aligned buffers, at most 256
+ * threads per CTA; chunk offsets off the 16-byte grid are handled by building
+ * each vector from two aligned loads); RR_PATH_SIMPLE is one element per
+ * thread with plain loads and stores (any alignment). */
 typedef enum { RR_PATH_AUTO = 0, RR_PATH_BULK = 1, RR_PATH_SIMPLE = 2, RR_PATH_DIRECT = 3 } rr_path;
 
 /* Optional launch configuration; zero fields mean "choose automatically". */

@@ -229,13 +229,21 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   // chunk boundaries on 16-byte multiples (segments are copied per chunk)
   const bool chunks_aligned = ck.op == RR_OP_ALLREDUCE || (p->base * E) % 16 == 0;
   const unsigned long long n_bulk = (N * E / 16) * 16 / E;
-  const bool bulk_ok = ck.all_16b_aligned && chunks_aligned && n_bulk > 0;
+  const bool vec_ok = ck.all_16b_aligned && n_bulk > 0;
+  const bool bulk_ok = vec_ok && chunks_aligned;
   int path = c.path;
-  if ((path == RR_PATH_BULK || path == RR_PATH_DIRECT) && !bulk_ok) return RR_ERR_UNSUPPORTED;
-  if (path == RR_PATH_AUTO)
-    path = !bulk_ok ? RR_PATH_SIMPLE
-                    : (prefer_direct(ck.op, ck.R, ck.L, (unsigned long long)ck.count * E, c.max_ctas) ? RR_PATH_DIRECT
-                                                                                                : RR_PATH_BULK);
+  if (path == RR_PATH_BULK && !bulk_ok) return RR_ERR_UNSUPPORTED;
+  if (path == RR_PATH_DIRECT && !vec_ok) return RR_ERR_UNSUPPORTED;
+  if (path == RR_PATH_AUTO) {
+    if (!vec_ok)
+      path = RR_PATH_SIMPLE;
+    else if (!chunks_aligned)  // ReduceScatter / AllGather with chunk boundaries off the 16-byte grid
+      path = RR_PATH_DIRECT;
+    else
+      path = prefer_direct(ck.op, ck.R, ck.L, (unsigned long long)ck.count * E, c.max_ctas) ? RR_PATH_DIRECT
+                                                                                             : RR_PATH_BULK;
+  }
+  p->shifted = (path == RR_PATH_DIRECT && !chunks_aligned) ? 1 : 0;
 
   l->path = path;
   // 128-thread CTAs on the direct path: finer grid granularity, measured 1-5 %
@@ -247,6 +255,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // eight loads in flight per thread: few ranks per group take several vectors
     int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 2 ? 4 : ck.L <= 4 ? 2 : 1);
     if (U > 2 && ck.dtype != RR_FP32 && ck.wire == RR_FP32) U = 2;  // binary32 accumulators are twice as wide
+    if (p->shifted) U = 1;  // the shifted kernel: one vector a thread
     p->direct_u = U;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
     // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5

@@ -261,6 +261,37 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   return v;
 }
 
+// 16-byte load that allocates in L1: the shifted ReduceScatter / AllGather
+// read each aligned block twice (as one thread's upper and the next thread's
+// lower half).
+__device__ __forceinline__ uint4 ldg_l1(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// The 16 bytes that start sh bytes into the 32 bytes lo:hi (0 <= sh < 16).
+__device__ __forceinline__ uint4 funnel16(uint4 lo, uint4 hi, int sh) {
+  const unsigned b = (unsigned)(sh & 3) * 8u;
+  uint32_t a0, a1, a2, a3, a4;
+  switch (sh >> 2) {
+    case 0:
+      a0 = lo.x, a1 = lo.y, a2 = lo.z, a3 = lo.w, a4 = hi.x;
+      break;
+    case 1:
+      a0 = lo.y, a1 = lo.z, a2 = lo.w, a3 = hi.x, a4 = hi.y;
+      break;
+    case 2:
+      a0 = lo.z, a1 = lo.w, a2 = hi.x, a3 = hi.y, a4 = hi.z;
+      break;
+    default:
+      a0 = lo.w, a1 = hi.x, a2 = hi.y, a3 = hi.z, a4 = hi.w;
+      break;
+  }
+  return make_uint4(__funnelshift_r(a0, a1, b), __funnelshift_r(a1, a2, b), __funnelshift_r(a2, a3, b),
+                    __funnelshift_r(a3, a4, b));
+}
+
 __device__ __forceinline__ void stg_stream(void *p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");

@@ -601,6 +601,101 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
 __global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long limit_ns);
 
 // --------------------------------------------------------------------------
+// ReduceScatter / AllGather whose chunk boundaries are off the 16-byte grid:
+// the chunk-local buffers (the ReduceScatter outputs, the AllGather inputs)
+// are then shifted against the rank vectors by (c * base) mod V elements.
+// Each thread takes one 16-byte vector aligned in the shifted buffer and
+// builds the matching bytes of the other side from two aligned loads.
+// --------------------------------------------------------------------------
+
+template <int OP, int DT, int WT>
+__global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __grid_constant__ RingParams p) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  using VT = Vec<DT, WT>;
+  using W = typename VT::W;
+  constexpr int V = VT::V;
+  constexpr int E = Fmt<DT>::bytes;
+  const int L = p.L;
+  const unsigned long long base = p.base, N = p.total;
+  const unsigned long long T = (unsigned long long)gridDim.x * blockDim.x;
+  const unsigned long long tid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if constexpr (OP == kOpReduceScatter) {
+    // Chunk by chunk (the shift is the chunk's), each warp takes 31
+    // consecutive output vectors: lane t loads the aligned block under vector
+    // t's start, which is also the upper block lane t - 1 needs (a shuffle);
+    // lane 31 only supplies that block.  A vector whose upper block would pass
+    // the end of the rank vectors goes element by element, and so do the
+    // elements past a chunk's last full vector.
+    const unsigned lane = threadIdx.x & 31u;
+    const unsigned long long warp = tid >> 5, n_warps = T >> 5;
+    const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
+    for (int c = 0; c < L; ++c) {
+      const unsigned long long len = c < L - 1 ? base : len_last, nv = len / V, g0 = (unsigned long long)c * base;
+      const int shift = (int)(g0 % V);  // elements
+      const int sh = shift * E;         // bytes
+      for (unsigned long long u0 = warp * 31; u0 < nv; u0 += n_warps * 31) {  // the same trip count for the warp
+        const unsigned long long u = u0 + lane;
+        const unsigned long long ga = g0 + u * V - (unsigned long long)shift;  // block under vector u's start
+        const bool load = u <= nv && ga + V <= N;
+        const bool act = lane < 31u && u < nv;
+        const bool tail = act && sh != 0 && ga + 2 * V > N;  // no upper block to shift in
+        W acc;
+        for (int k0 = 0; k0 < L; k0 += 8) {
+          uint4 blk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (k0 + j < L) {
+              int r = c + k0 + j;
+              r -= (r >= L) ? L : 0;
+              blk[j] = load ? ldg_stream(static_cast<const unsigned char *>(p.in[r]) + ga * E)
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (k0 + j < L) {
+              const uint4 next = make_uint4(__shfl_down_sync(0xffffffffu, blk[j].x, 1),
+                                            __shfl_down_sync(0xffffffffu, blk[j].y, 1),
+                                            __shfl_down_sync(0xffffffffu, blk[j].z, 1),
+                                            __shfl_down_sync(0xffffffffu, blk[j].w, 1));
+              const W x = VT::in(sh ? funnel16(blk[j], next, sh) : blk[j]);
+              acc = (k0 + j == 0) ? x : VT::hop(acc, x);
+            }
+        }
+        if (tail) {
+          for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, g0 + u * V + e);
+        } else if (act) {
+          stg_stream(static_cast<unsigned char *>(p.out[c]) + u * V * E, VT::out(acc));
+        }
+      }
+    }
+    for (unsigned long long t = tid; t < (unsigned long long)L * V; t += T) {
+      const int c = (int)(t / V), e = (int)(t % V);
+      const unsigned long long len = c < L - 1 ? base : len_last, full = len / V * V;
+      if (full + e < len) element_op<OP, DT, WT>(p, (unsigned long long)c * base + full + e);
+    }
+  } else {  // AllGather: output vectors aligned in the rank vectors, sources shifted in each chunk
+    const unsigned long long nvec = p.n_bulk / V;
+    for (unsigned long long v = tid; v < nvec; v += T) {
+      const unsigned long long gs = v * V;
+      const int c = chunk_of(gs, base, L);
+      const unsigned long long o = gs - (unsigned long long)c * base;  // offset in chunk c's buffer
+      const unsigned long long oa = o / V * V, len = chunk_end(c, base, L, N) - (unsigned long long)c * base;
+      const int sh = (int)(o - oa) * E;
+      if (c != chunk_of(gs + V - 1, base, L) || (sh != 0 && oa + 2 * V > len)) {
+        for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, gs + e);
+        continue;
+      }
+      const unsigned char *src = static_cast<const unsigned char *>(p.in[c]) + oa * E;
+      const uint4 lo = ldg_l1(src);
+      const uint4 x = sh ? funnel16(lo, ldg_l1(src + 16), sh) : lo;
+      for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + gs * E, x);
+    }
+    for (unsigned long long i = p.n_bulk + tid; i < p.count; i += T) element_op<OP, DT, WT>(p, i);
+  }
+}
+
+// --------------------------------------------------------------------------
 // host side: one launch of (OP, DT, WT)
 // --------------------------------------------------------------------------
 
@@ -638,7 +733,10 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
   } else if (l.path == RR_PATH_DIRECT) {
     if constexpr (HD) {
       return launch_hd_direct(DT, WT, p, l, s);
-    } else {
+    } else if constexpr (OP != kOpAllReduce) {
+      if (p.shifted) return launch_kernel(rr_shift_kernel<OP, DT, WT>, l, 0, s, p);
+    }
+    if constexpr (!HD) {
       // vectors per thread: 1 for AllGather; at most 2 when 16-bit storage is
       // summed in binary32 (eight-float accumulators)
       constexpr bool multi = OP != kOpAllGather;

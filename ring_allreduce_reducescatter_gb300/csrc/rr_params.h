@@ -43,6 +43,7 @@ struct RingParams {
   int hd_log2p;                   // halving-doubling: log2 of P, the largest power of two <= R
   int hd_extra;                   // halving-doubling: R - P ranks folded in pairs first
   int straddle_cta;               // direct AllReduce: 1 if the grid's last CTA folds the vectors over chunk boundaries
+  int shifted;                    // direct ReduceScatter / AllGather: chunk boundaries off the 16-byte grid
 };
 
 // One launch, fully resolved by the planner.

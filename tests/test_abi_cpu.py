@@ -321,8 +321,11 @@ def test_planner_paths(L):
     assert plan_dev(L, AG, 16, 1 << 24, F32)[1]["path"] == DIRECT
     assert plan_dev(L, AG, 8, 1 << 24, F32)[1]["path"] == DIRECT
     assert plan_dev(L, AR, 8, 1 << 28, F16, cfg=(0, 0, 0, 0, 0, 96))[1]["path"] == BULK  # capped grid
-    # ReduceScatter / AllGather need chunk boundaries on 16 bytes for the aligned paths
-    assert plan_dev(L, RS, 8, 8 * 1001, F16)[1]["path"] == SIMPLE
+    # ReduceScatter / AllGather with chunk boundaries off the 16-byte grid: the
+    # direct path's shifted kernel; the tile pipeline needs them on the grid
+    assert plan_dev(L, RS, 8, 8 * 1001, F16)[1]["path"] == DIRECT
+    assert plan_dev(L, AG, 8, 8 * 1001 + 3, F32)[1]["path"] == DIRECT
+    assert plan_dev(L, RS, 8, 8 * 1001, F16, aligned=0)[1]["path"] == SIMPLE
     assert plan_dev(L, RS, 8, 8 * 1024, F16, cfg=(BULK, 0, 0, 0, 0))[1]["path"] == BULK
     assert plan_dev(L, AG, 8, 8 * 1024, F32, cfg=(BULK, 0, 0, 0, 0))[1]["path"] == BULK
     # a forced bulk path the buffers do not allow is refused
@@ -428,7 +431,7 @@ def test_direct_path_plans(L):
     assert ch["threads"] == 128 and grid == min((1 << 19) * 2 // 16 // 128, 152 * 16)
     # the same alignment needs as the bulk path, and at most 256 threads
     assert plan_dev(L, AR, 8, 1 << 19, F16, aligned=0, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP
-    assert plan_dev(L, RS, 8, 8 * 1001, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP
+    assert plan_dev(L, RS, 8, 8 * 1001, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == OK  # the shifted kernel
     assert plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 512))[0] == EUNSUP
     assert plan_dev(L, AR, 8, 7, F16, cfg=(DIRECT, 0, 0, 0, 0))[0] == EUNSUP  # under 16 bytes
     st, _, grid, _ = plan_dev(L, AR, 8, 1 << 19, F16, cfg=(DIRECT, 0, 0, 0, 128, 10))

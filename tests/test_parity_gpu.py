@@ -82,8 +82,9 @@ def cfg_of(rr, path=0, tile=0, stages=0, ctas=0, threads=0):
 
 
 def direct_ok(N, R, E, op="ar"):
-    """The direct path's conditions (16-byte vectors; chunk offsets on 16 bytes for RS / AG)."""
-    return N * E >= 16 and (op == "ar" or (N // R * E) % 16 == 0)
+    """The direct path's condition: at least one 16-byte vector (chunk offsets
+    off the 16-byte grid take its shifted ReduceScatter / AllGather kernel)."""
+    return N * E >= 16
 
 
 def run_ar(rr, xs, wire=None, group=0, cfg=None, inplace=False):
@@ -227,6 +228,26 @@ def test_allgather_grid(rr, dtype, R):
             check_ag(rr, chunks, N, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
 
 
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_shifted_reduce_scatter_and_allgather(rr, dtype, wire):
+    """Chunk boundaries at every offset off the 16-byte grid: the direct path
+    builds each vector from two aligned loads.  Chunk lengths from below one
+    vector to several grid strides, the last vectors near the buffer ends."""
+    E = torch.tensor([], dtype=dtype).element_size()
+    V = 16 // E
+    for R in (2, 3, 5, 8, 24):
+        for base in [V * k + j for k in (0, 1, 37) for j in range(1, V)] + [V * 20011 + 1, V * 20011 + V - 1]:
+            N = R * base + (R // 2)
+            xs = gen(R, N, dtype, 13 * R + base)
+            tag = f"shifted {NAME[dtype]}/{wire} R={R} base={base}"
+            cfg = cfg_of(rr, path=rr.PATH_DIRECT) if direct_ok(N, R, E) else None  # under 16 bytes: simple
+            check_rs(rr, xs, wire, cfg=cfg, what="RS " + tag)
+            if wire is None:
+                lens = [oracle.chunk_len(N, R, c) for c in range(R)]
+                chunks = gen(R, 0, dtype, 17 * R + base, lengths=lens)
+                check_ag(rr, chunks, N, cfg=cfg, what="AG " + tag)
+
+
 @pytest.mark.parametrize("algo", ["hd", "naive"])
 def test_allgather_equals_every_schedule(rr, algo):
     """On one GPU the AllGather is a copy: ring_allgather's outputs equal the
@@ -248,13 +269,13 @@ def test_aligned_paths_are_chosen_when_aligned(rr):
     xs = gen(8, 1 << 20, torch.float16, 5)
     outs = [torch.empty_like(x) for x in xs]
     assert rr.plan(rr.OP_ALLREDUCE, xs, outs, 1 << 20)["path"] in (rr.PATH_BULK, rr.PATH_DIRECT)
-    # chunk boundaries off the 16-byte grid: ReduceScatter takes the simple path
+    # chunk boundaries off the 16-byte grid: ReduceScatter takes the direct
+    # path's shifted kernel; the tile pipeline refuses
     N = 8 * 1001
     xs = gen(8, N, torch.float16, 5)
     rs = [torch.empty(N // 8, dtype=torch.float16, device="cuda") for _ in range(8)]
-    assert rr.plan(rr.OP_REDUCE_SCATTER, xs, rs, N)["path"] == rr.PATH_SIMPLE
-    with pytest.raises(rr.RingError):
-        rr.collective(rr.OP_REDUCE_SCATTER, xs, rs, N, cfg=cfg_of(rr, path=rr.PATH_DIRECT))
+    assert rr.plan(rr.OP_REDUCE_SCATTER, xs, rs, N)["path"] == rr.PATH_DIRECT
+    check_rs(rr, xs, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what="shifted RS")
     with pytest.raises(rr.RingError) as e:
         rr.collective(rr.OP_REDUCE_SCATTER, xs, rs, N, cfg=cfg_of(rr, path=rr.PATH_BULK))
     assert e.value.status == rr.ERR_UNSUPPORTED
