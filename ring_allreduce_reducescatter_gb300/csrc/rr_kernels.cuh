@@ -608,7 +608,9 @@ __global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long li
 // builds the matching bytes of the other side from two aligned loads.
 // --------------------------------------------------------------------------
 
-template <int OP, int DT, int WT>
+// US: rows of output vectors a warp takes at once (ReduceScatter; 2 for up to
+// four ranks, so that a lane keeps eight loads in flight).
+template <int OP, int DT, int WT, int US>
 __global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __grid_constant__ RingParams p) {
   grid_dependency_wait();
   grid_dependents_launch();
@@ -621,51 +623,80 @@ __global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __gri
   const unsigned long long T = (unsigned long long)gridDim.x * blockDim.x;
   const unsigned long long tid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
   if constexpr (OP == kOpReduceScatter) {
-    // Chunk by chunk (the shift is the chunk's), each warp takes 31
-    // consecutive output vectors: lane t loads the aligned block under vector
-    // t's start, which is also the upper block lane t - 1 needs (a shuffle);
-    // lane 31 only supplies that block.  A vector whose upper block would pass
-    // the end of the rank vectors goes element by element, and so do the
-    // elements past a chunk's last full vector.
+    // Chunk by chunk (the shift is the chunk's), each warp takes US rows of
+    // 31 consecutive output vectors: in a row, lane t loads the aligned block
+    // under vector t's start, which is also the upper block lane t - 1 needs
+    // (a shuffle); lane 31 only supplies that block.  A vector whose upper
+    // block would pass the end of the rank vectors goes element by element,
+    // and so do the elements past a chunk's last full vector.
+    constexpr int NB = 8 / US;  // ranks per batch: 8 loads in flight a lane
     const unsigned lane = threadIdx.x & 31u;
     const unsigned long long warp = tid >> 5, n_warps = T >> 5;
     const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
-    for (int c = 0; c < L; ++c) {
+    // work items: one per 31 * US output vectors of a chunk, numbered across
+    // all chunks so that every warp's items spread over the chunks
+    constexpr unsigned long long per_item = 31ull * US;
+    const unsigned long long ipc = (base / V + per_item - 1) / per_item;      // items in chunks 0..L-2
+    const unsigned long long ipl = (len_last / V + per_item - 1) / per_item;  // items in the last chunk
+    const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
+    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
+      int c;
+      unsigned long long item;
+      if (w < (unsigned long long)(L - 1) * ipc) {
+        c = (int)(w / ipc);
+        item = w - (unsigned long long)c * ipc;
+      } else {
+        c = L - 1;
+        item = w - (unsigned long long)(L - 1) * ipc;
+      }
       const unsigned long long len = c < L - 1 ? base : len_last, nv = len / V, g0 = (unsigned long long)c * base;
       const int shift = (int)(g0 % V);  // elements
       const int sh = shift * E;         // bytes
-      for (unsigned long long u0 = warp * 31; u0 < nv; u0 += n_warps * 31) {  // the same trip count for the warp
-        const unsigned long long u = u0 + lane;
-        const unsigned long long ga = g0 + u * V - (unsigned long long)shift;  // block under vector u's start
-        const bool load = u <= nv && ga + V <= N;
-        const bool act = lane < 31u && u < nv;
-        const bool tail = act && sh != 0 && ga + 2 * V > N;  // no upper block to shift in
-        W acc;
-        for (int k0 = 0; k0 < L; k0 += 8) {
-          uint4 blk[8];
+      {
+        const unsigned long long u0 = item * per_item;
+        unsigned long long u[US], ga[US];
+        bool load[US], act[US], tail[US];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (k0 + j < L) {
-              int r = c + k0 + j;
-              r -= (r >= L) ? L : 0;
-              blk[j] = load ? ldg_stream(static_cast<const unsigned char *>(p.in[r]) + ga * E)
-                            : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (k0 + j < L) {
-              const uint4 next = make_uint4(__shfl_down_sync(0xffffffffu, blk[j].x, 1),
-                                            __shfl_down_sync(0xffffffffu, blk[j].y, 1),
-                                            __shfl_down_sync(0xffffffffu, blk[j].z, 1),
-                                            __shfl_down_sync(0xffffffffu, blk[j].w, 1));
-              const W x = VT::in(sh ? funnel16(blk[j], next, sh) : blk[j]);
-              acc = (k0 + j == 0) ? x : VT::hop(acc, x);
-            }
+        for (int k = 0; k < US; ++k) {
+          u[k] = u0 + 31ull * k + lane;
+          ga[k] = g0 + u[k] * V - (unsigned long long)shift;  // block under vector u's start
+          load[k] = u[k] <= nv && ga[k] + V <= N;
+          act[k] = lane < 31u && u[k] < nv;
+          tail[k] = act[k] && sh != 0 && ga[k] + 2 * V > N;  // no upper block to shift in
         }
-        if (tail) {
-          for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, g0 + u * V + e);
-        } else if (act) {
-          stg_stream(static_cast<unsigned char *>(p.out[c]) + u * V * E, VT::out(acc));
+        W acc[US];
+        for (int k0 = 0; k0 < L; k0 += NB) {
+          uint4 blk[US][NB];
+#pragma unroll
+          for (int k = 0; k < US; ++k)
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+              if (k0 + j < L) {
+                int r = c + k0 + j;
+                r -= (r >= L) ? L : 0;
+                blk[k][j] = load[k] ? ldg_stream(static_cast<const unsigned char *>(p.in[r]) + ga[k] * E)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+              }
+#pragma unroll
+          for (int k = 0; k < US; ++k)
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+              if (k0 + j < L) {
+                const uint4 next = make_uint4(__shfl_down_sync(0xffffffffu, blk[k][j].x, 1),
+                                              __shfl_down_sync(0xffffffffu, blk[k][j].y, 1),
+                                              __shfl_down_sync(0xffffffffu, blk[k][j].z, 1),
+                                              __shfl_down_sync(0xffffffffu, blk[k][j].w, 1));
+                const W x = VT::in(sh ? funnel16(blk[k][j], next, sh) : blk[k][j]);
+                acc[k] = (k0 + j == 0) ? x : VT::hop(acc[k], x);
+              }
+        }
+#pragma unroll
+        for (int k = 0; k < US; ++k) {
+          if (tail[k]) {
+            for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, g0 + u[k] * V + e);
+          } else if (act[k]) {
+            stg_stream(static_cast<unsigned char *>(p.out[c]) + u[k] * V * E, VT::out(acc[k]));
+          }
         }
       }
     }
@@ -734,7 +765,12 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
     if constexpr (HD) {
       return launch_hd_direct(DT, WT, p, l, s);
     } else if constexpr (OP != kOpAllReduce) {
-      if (p.shifted) return launch_kernel(rr_shift_kernel<OP, DT, WT>, l, 0, s, p);
+      if (p.shifted) {
+        if constexpr (OP == kOpReduceScatter) {
+          if (p.L <= 4) return launch_kernel(rr_shift_kernel<OP, DT, WT, 2>, l, 0, s, p);
+        }
+        return launch_kernel(rr_shift_kernel<OP, DT, WT, 1>, l, 0, s, p);
+      }
     }
     if constexpr (!HD) {
       // vectors per thread: 1 for AllGather; at most 2 when 16-bit storage is
