@@ -30,6 +30,15 @@
 //    refills the stage of the tile D steps back once its stores have read
 //    shared memory (D = store_lag): D + 1 tiles of stores and S - D - 1 tiles
 //    of loads stay in flight while a tile is folded.  Every wait is bounded.
+//  rr_direct_kernel: every thread loads its ranks' 16-byte vectors straight
+//    from HBM in batches of eight loads, folds them in registers and stores
+//    the result to every output; one extra CTA folds the AllReduce vectors
+//    that straddle a chunk boundary.
+//  rr_shift_kernel: ReduceScatter / AllGather whose chunk boundaries are off
+//    the 16-byte grid (vectors built from two aligned blocks).
+//  The halving-doubling direct kernels are in rr_hd_direct.cuh.
+//  Every kernel starts with the programmatic-launch wait, so a launch may
+//  overlap the kernel before it on the stream.
 #pragma once
 
 #include "rr_device.cuh"
