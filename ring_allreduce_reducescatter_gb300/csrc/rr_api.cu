@@ -178,13 +178,14 @@ int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 unsigned round16_down(unsigned long long x) { return (unsigned)(x & ~15ull); }
 
 // Which of the two 16-byte-aligned paths is faster, from a measured sweep of
-// both (R = 2 .. 32, 1 MiB .. 512 MiB per rank, every collective; CUDA-graph
+// both (R = 2 .. 32, 256 KiB .. 512 MiB per rank, every collective; CUDA-graph
 // replay over inputs colder than L2).  The direct path keeps eight loads in
-// flight per thread and needs no barriers: it wins for small messages, for
-// every ReduceScatter with R >= 3 and for every AllReduce with R >= 8.  The
-// tile pipeline wins for two ranks, for 3..7 ranks between 2 and 64 MiB, for
-// AllGather with 16 or more ranks above 1 MiB, and for capped grids (each CTA
-// then owns an SM and moves 8 KB per bulk copy).
+// flight per thread and needs no barriers: it wins for every AllGather, every
+// ReduceScatter with R >= 3, every two-level ring and every flat AllReduce of
+// 3..32 ranks but one case.  The tile pipeline wins for one or two ranks, for
+// a flat ring of 16 ranks from 64 MiB per rank (two CTAs of three 32 KiB
+// stages fit an SM exactly), and for capped grids (each CTA then owns an SM
+// and moves 8 KB per bulk copy).
 bool prefer_direct(int op, int R, int L, unsigned long long msg_bytes, int max_ctas) {
   const unsigned long long MiB = 1ull << 20;
   if (max_ctas > 0) return false;                       // capped grids: one tile pipeline per SM
@@ -225,8 +226,9 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   p->hd_log2p = log2p;
   p->hd_extra = ck.R - P;
 
-  // bulk path: 16-byte aligned buffers, and for ReduceScatter / AllGather
-  // chunk boundaries on 16-byte multiples (segments are copied per chunk)
+  // the 16-byte paths need 16-byte aligned buffers; the tile pipeline also
+  // needs ReduceScatter / AllGather chunk boundaries on 16-byte multiples
+  // (segments are copied per chunk), the direct path's shifted kernel not
   const bool chunks_aligned = ck.op == RR_OP_ALLREDUCE || (p->base * E) % 16 == 0;
   const unsigned long long n_bulk = (N * E / 16) * 16 / E;
   const bool vec_ok = ck.all_16b_aligned && n_bulk > 0;
