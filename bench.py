@@ -72,12 +72,36 @@ DEVICE_SOURCES = ("rr_kernels.cuh", "rr_device.cuh", "rr_params.h", "rr_inst_f32
                   "rr_inst_hd_bf16.cu", "rr_inst_f32_narrow.cu")
 
 
+def code_only(text):
+    """C / C++ source without its comments and with runs of whitespace folded,
+    so that a comment edit does not count as a change of the code."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':  # string literals (the inline PTX) are code
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sources_digest():
-    """Digest of the device code (the kernels, not the host-side planner)."""
+    """Digest of the device code (the kernels, not the host-side planner;
+    comments and layout do not count)."""
     h = hashlib.sha256()
     for name in DEVICE_SOURCES:
-        with open(os.path.join(ROOT, "ring_allreduce_reducescatter_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "ring_allreduce_reducescatter_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

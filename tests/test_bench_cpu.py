@@ -93,3 +93,14 @@ def test_clock_summary_flags_throttling():
     c = s.summary(0.9, 1.3)
     assert c["samples"] == 2 and c["sm_mhz"] == 1925.0 and c["sm_max_mhz"] == 2070.0
     assert c["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_kernel_digest_ignores_comments_only():
+    import bench
+
+    src = 'int f(int x) { // add one\n  return x + 1; /* done */ }\nconst char *s = "a//b /* c */";\n'
+    same = 'int f(int x) {\n  return x + 1;\n}\nconst char *s = "a//b /* c */"; // note\n'
+    other = 'int f(int x) { return x + 2; }\nconst char *s = "a//b /* c */";\n'
+    assert bench.code_only(src) == bench.code_only(same)
+    assert bench.code_only(src) != bench.code_only(other)
+    assert '"a//b /* c */"' in bench.code_only(src)
