@@ -182,7 +182,8 @@ unsigned round16_down(unsigned long long x) { return (unsigned)(x & ~15ull); }
 // replay over inputs colder than L2).  The direct path keeps eight loads in
 // flight per thread and needs no barriers: it wins for every AllGather, every
 // ReduceScatter with R >= 3, every two-level ring and every flat AllReduce of
-// 3..32 ranks but one case.  The tile pipeline wins for one or two ranks, for
+// 3..32 ranks but one case.  The tile pipeline wins for one or two ranks from
+// 4 MiB per rank, for
 // a flat ring of 16 ranks from 64 MiB per rank (two CTAs of three 32 KiB
 // stages fit an SM exactly), and for capped grids (each CTA then owns an SM
 // and moves 8 KB per bulk copy).
@@ -191,7 +192,7 @@ bool prefer_direct(int op, int R, int L, unsigned long long msg_bytes, int max_c
   if (max_ctas > 0) return false;                       // capped grids: one tile pipeline per SM
   if (op == RR_OP_ALLGATHER) return true;
   if (op == RR_OP_REDUCE_SCATTER) return R >= 3;
-  if (R <= 2) return false;
+  if (R <= 2) return msg_bytes <= MiB;                  // the tile pipeline from 4 MiB (0.90 against 0.78)
   if (L < R) return true;                               // two-level
   if (R == 16) return msg_bytes < 64 * MiB;             // two CTAs of three 32 KiB stages per SM
   return true;
@@ -255,8 +256,10 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   if (path == RR_PATH_DIRECT) {  // U 16-byte vectors per thread
     if (l->threads > 256) return RR_ERR_UNSUPPORTED;
     // eight loads in flight per thread: few ranks per group take several vectors
-    int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 2 ? 4 : ck.L <= 4 ? 2 : 1);
-    if (U > 2 && ck.dtype != RR_FP32 && ck.wire == RR_FP32) U = 2;  // binary32 accumulators are twice as wide
+    // (two vectors for up to four ranks per group: for two ranks, four vectors a
+    // thread reached 0.61 of the copy bandwidth and two vectors at three CTAs
+    // per SM 0.78, at 256 MiB)
+    int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 4 ? 2 : 1);
     if (p->shifted) U = 1;  // the shifted kernel: one vector a thread
     p->direct_u = U;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_hd_direct_kernel(const
 template <int DT, int WT, int LOG2P, bool EXTRA>
 cudaError_t launch_occ(const RingParams &p, const Launch &l, cudaStream_t s) {
   constexpr bool wide = DT != kF32 && WT == kF32;
-  if constexpr (!wide) {
+  if constexpr (!wide && LOG2P <= 2) {  // the planner asks for three CTAs below seven ranks only
     if (l.direct_occ == 3) return launch_kernel(rr_hd_direct_kernel<DT, WT, LOG2P, EXTRA, 3>, l, 0, s, p);
   }
   return launch_kernel(rr_hd_direct_kernel<DT, WT, LOG2P, EXTRA, 2>, l, 0, s, p);

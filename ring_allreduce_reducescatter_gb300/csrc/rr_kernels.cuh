@@ -782,13 +782,9 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
       }
     }
     if constexpr (!HD) {
-      // vectors per thread: 1 for AllGather; at most 2 when 16-bit storage is
-      // summed in binary32 (eight-float accumulators)
+      // vectors per thread: 1 for AllGather, 1 or 2 otherwise
       constexpr bool multi = OP != kOpAllGather;
       constexpr bool wide = DT != kF32 && WT == kF32;
-      if constexpr (multi && !wide) {
-        if (p.direct_u >= 4) return launch_kernel(rr_direct_kernel<OP, DT, WT, 4, 2>, l, 0, s, p);
-      }
       if constexpr (multi && !wide) {
         if (p.direct_u >= 2)
           return l.direct_occ == 3 ? launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 3>, l, 0, s, p)

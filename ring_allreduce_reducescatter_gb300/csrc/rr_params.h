@@ -38,7 +38,7 @@ struct RingParams {
   int stages;                     // bulk path: pipeline depth
   int store_lag;                  // bulk path: store groups left in flight before a stage is refilled (1..8)
   int slots;                      // bulk path: tiles of one stage (R, or 1 for AllGather)
-  int direct_u;                   // direct path: vectors per thread and iteration (1, 2 or 4)
+  int direct_u;                   // direct path: vectors per thread and iteration (1 or 2)
   int algo;                       // AllReduce summation order: kAlgo*
   int hd_log2p;                   // halving-doubling: log2 of P, the largest power of two <= R
   int hd_extra;                   // halving-doubling: R - P ranks folded in pairs first
