@@ -714,7 +714,61 @@ __global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __gri
       const unsigned long long len = c < L - 1 ? base : len_last, full = len / V * V;
       if (full + e < len) element_op<OP, DT, WT>(p, (unsigned long long)c * base + full + e);
     }
-  } else {  // AllGather: output vectors aligned in the rank vectors, sources shifted in each chunk
+  } else if (L <= 4) {
+    // AllGather with few ranks, where the loads weigh most: rows of 32 output
+    // vectors aligned to 32 vectors (512-byte store segments), clipped to one
+    // chunk and numbered across the chunks; lane t loads the aligned source
+    // block under vector t's start, which is also the upper block lane t - 1
+    // needs (a shuffle), and lane 31 loads its upper block itself.  Vectors
+    // over a chunk boundary (at most one per boundary, taken by the first
+    // boundary inside it), vectors whose upper block would pass the end of the
+    // chunk's buffer and the ragged end go element by element.
+    const unsigned lane = threadIdx.x & 31u;
+    const unsigned long long warp = tid >> 5, n_warps = T >> 5;
+    const unsigned long long nvec = p.n_bulk / V;  // output vectors wholly before the ragged end
+    const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
+    const unsigned long long ipc = (base / V + 64) / 32, ipl = (len_last / V + 64) / 32;  // rows per chunk, at most
+    const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
+    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
+      int c;
+      unsigned long long item;
+      if (w < (unsigned long long)(L - 1) * ipc) {
+        c = (int)(w / ipc);
+        item = w - (unsigned long long)c * ipc;
+      } else {
+        c = L - 1;
+        item = w - (unsigned long long)(L - 1) * ipc;
+      }
+      const unsigned long long cb = (unsigned long long)c * base, len = c < L - 1 ? base : len_last;
+      const unsigned long long vf = (cb + V - 1) / V;  // first output vector wholly in the chunk
+      const unsigned long long ve = (cb + len) / V < nvec ? (cb + len) / V : nvec;  // one past the last
+      const int sh = (int)((vf * V - cb) % V) * E;     // where a vector's source starts in its aligned block
+      const unsigned long long v = (vf / 32 + item) * 32 + lane;
+      const bool act = v >= vf && v < ve;
+      // the aligned source block under vector v's start (o - oa = sh / E for every v of the chunk)
+      const unsigned long long o = v * V - cb, oa = o - (o % V);
+      const bool load = v >= vf && v <= ve && oa + V <= len;
+      const bool tail = act && sh != 0 && oa + 2 * V > len;
+      const unsigned char *src = static_cast<const unsigned char *>(p.in[c]);
+      const uint4 blk = load ? ldg_stream(src + oa * E) : make_uint4(0u, 0u, 0u, 0u);
+      uint4 next = make_uint4(__shfl_down_sync(0xffffffffu, blk.x, 1), __shfl_down_sync(0xffffffffu, blk.y, 1),
+                              __shfl_down_sync(0xffffffffu, blk.z, 1), __shfl_down_sync(0xffffffffu, blk.w, 1));
+      if (lane == 31u && act && sh != 0 && !tail) next = ldg_stream(src + (oa + V) * E);
+      if (tail) {
+        for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
+      } else if (act) {
+        const uint4 x = sh ? funnel16(blk, next, sh) : blk;
+        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + v * V * E, x);
+      }
+    }
+    for (unsigned long long b = 1 + tid; b < (unsigned long long)L; b += T) {  // vectors over a boundary
+      const unsigned long long gb = b * base, vb = gb / V;
+      if (gb % V == 0 || vb >= nvec) continue;
+      if ((b - 1) * base > vb * V) continue;  // an earlier boundary lies inside this vector
+      for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, vb * V + e);
+    }
+    for (unsigned long long i = p.n_bulk + tid; i < p.count; i += T) element_op<OP, DT, WT>(p, i);
+  } else {  // AllGather: each thread an output vector, two aligned loads of its source block pair
     const unsigned long long nvec = p.n_bulk / V;
     for (unsigned long long v = tid; v < nvec; v += T) {
       const unsigned long long gs = v * V;
