@@ -48,7 +48,12 @@
  *     up is recorded in the device status word (ring_device_status).
  *   - Argument errors are detected before anything is enqueued and return
  *     RR_ERR_INVALID_ARG / RR_ERR_UNSUPPORTED / RR_ERR_ALIAS; nothing is
- *     written then.  A failed launch returns RR_ERR_CUDA.
+ *     written then.  A failed launch returns RR_ERR_CUDA (and
+ *     ring_last_cuda_error names the runtime error).
+ *   - Kernels are launched with programmatic stream serialisation by default
+ *     (rr_launch_cfg.early_launch): a launch may be scheduled while the kernel
+ *     before it on the stream runs, but every kernel waits for that kernel's
+ *     completion and writes before touching memory, so stream order holds.
  *   - count == 0 returns RR_OK and enqueues nothing.  A buffer of zero
  *     elements may be NULL.  Every other buffer must be non-NULL and aligned
  *     to its element size; 16-byte aligned buffers take the fast path.
