@@ -289,7 +289,9 @@ rr_status ring_allreduce_host_static(const void *const *host_in, void *const *ho
 /*
  * ring_plan -- the launch configuration ring_collective would use for these
  * arguments (after validation; nothing is enqueued).  *chosen receives the
- * path and the resolved tile / stage / CTA / thread counts.
+ * path and the resolved tile / stage / CTA-per-SM / thread counts (0 where
+ * the path has none), max_ctas = the grid's CTA count, and early_launch = 1
+ * (programmatic launch) or 2 (plain stream order).
  */
 rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs, int R,
                     size_t count, rr_dtype dtype, rr_dtype wire, int group_size,
