@@ -735,6 +735,18 @@ def test_algorithm_grid(rr, algo, dtype, wire):
                 check_algo(rr, xs, wire, algo, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=tag + " direct")
 
 
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_algorithm_occupancy_variants(rr, dtype, wire):
+    """Messages large enough that the direct path's threads loop, so that
+    halving-doubling below seven ranks runs its three-CTA kernels (with and
+    without extra ranks), and the naive order its looping ring kernel."""
+    for R, N in ((3, 3 * 400_003), (4, 4 * 300_007), (5, 5 * 250_001), (6, 6 * 200_003), (12, 12 * 100_003)):
+        xs = gen(R, N, dtype, 91 * R)
+        for algo in ("hd", "naive"):
+            check_algo(rr, xs, wire, algo, cfg=cfg_of(rr, path=rr.PATH_DIRECT),
+                       what=f"{algo} {NAME[dtype]}/{wire} R={R} N={N} direct")
+
+
 @pytest.mark.parametrize("algo", ["hd", "naive"])
 def test_algorithm_full_size_sampled(rr, wl, algo):
     xs = wl.inputs(wl.config2(512), "cuda")
