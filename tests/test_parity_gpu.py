@@ -415,9 +415,9 @@ def test_direct_occupancy_variants(rr, dtype, wire):
         assert plan["path"] == rr.PATH_DIRECT or R == 16, plan
         check_ar(rr, xs, wire, group=group, cfg=cfg_of(rr, path=rr.PATH_DIRECT),
                  what=f"occupancy {NAME[dtype]}/{wire} R={R} group={group} N={N} V={V}")
-    R, N = 4, 4 * (1 << 19)
-    xs = gen(R, N, dtype, 67)
-    check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=f"occupancy RS {NAME[dtype]}/{wire}")
+    for R, N in ((4, 4 * (1 << 19)), (8, 8 * 300_000), (12, 12 * 160_000)):  # two vectors a thread, then one
+        xs = gen(R, N, dtype, 67 + R)
+        check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=f"occupancy RS {NAME[dtype]}/{wire} R={R}")
 
 
 @pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
