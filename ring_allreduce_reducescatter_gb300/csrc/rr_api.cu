@@ -284,7 +284,17 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     if (ck.algo == RR_ALGO_HALVING_DOUBLING)
       l->direct_occ = (ck.R < 7 && looping && !wide) ? 3 : 2;
     const unsigned long long blocks = (vecs + (unsigned long long)l->threads * U - 1) / ((unsigned long long)l->threads * U);
-    const unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);
+    unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);
+    // ReduceScatter, and ring AllReduce over groups of at most three ranks, do
+    // better on two whole waves of the resident CTAs than on sixteen 128-thread
+    // CTAs per SM (2.67 waves at three CTAs per SM).  Measured at 256 MiB per
+    // rank, of the copy bandwidth: ReduceScatter R = 4 0.95 -> 0.99, R = 5
+    // 0.74 -> 0.79, R = 16 0.96 -> 0.99; AllReduce R = 3 0.96 -> 0.99; two-level
+    // 4 x 2 at 64 MiB 0.90 -> 0.95.  AllReduce over four or more ranks a group
+    // and AllGather lost 1-9 % on any whole number of waves from one to four.
+    if (ck.algo == RR_ALGO_RING && !p->shifted &&
+        (ck.op == RR_OP_REDUCE_SCATTER || (ck.op == RR_OP_ALLREDUCE && ck.L <= 3)))
+      cap = (unsigned long long)sms * (unsigned long long)l->direct_occ * (256ull / l->threads) * 2ull;
     // Vectors over a chunk boundary (ring order, boundaries off the 16-byte
     // grid): one extra CTA folds them, so the main loop stays lean.
     const unsigned long long V = 16 / E;

@@ -454,6 +454,25 @@ def test_direct_path_straddle_cta(L):
     assert grid == (1 << 19) * 2 // 16 // 128
 
 
+def test_direct_grid_waves(L):
+    """Looping direct grids: ReduceScatter and AllReduce over groups of at most
+    three ranks take two whole waves of the resident CTAs (three 256-thread
+    CTAs' worth of registers per SM: 6 CTAs of 128 a wave); other AllReduce
+    and AllGather launches take sixteen 128-thread CTAs per SM."""
+    sms, n = GB300["sms"], 1 << 26  # 256 MiB of binary32 per rank
+    assert plan_dev(L, RS, 4, n, F32)[2] == sms * 6 * 2
+    assert plan_dev(L, RS, 16, n, F32)[2] == sms * 6 * 2
+    assert plan_dev(L, AR, 3, 3 << 24, F16)[2] == sms * 6 * 2
+    assert plan_dev(L, AR, 8, 1 << 26, F32, group=2)[2] == sms * 6 * 2
+    assert plan_dev(L, AR, 4, 1 << 27, F16)[2] == sms * 16
+    assert plan_dev(L, AR, 8, 1 << 28, F16)[2] == sms * 16
+    assert plan_dev(L, AG, 4, n, F32)[2] == sms * 16
+    # ReduceScatter with one full batch of eight loads a thread: two CTAs per SM, two waves
+    assert plan_dev(L, RS, 8, n, F32)[2] == sms * 4 * 2
+    # a grid that fits under the cap is not changed
+    assert plan_dev(L, RS, 4, 1 << 20, F32)[2] == (1 << 20) * 4 // 16 // 256
+
+
 def test_rank_buffers_layout():
     """rank_buffers: R views of one allocation, each 256-byte aligned relative
     to the first, staggered by the requested bytes, never overlapping."""
