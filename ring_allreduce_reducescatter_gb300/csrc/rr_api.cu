@@ -260,6 +260,14 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // thread reached 0.61 of the copy bandwidth and two vectors at three CTAs
     // per SM 0.78, at 256 MiB)
     int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 4 ? 2 : 1);
+    // ReduceScatter stores one vector per R loads, so nearly all its traffic is
+    // loads and it wants more of them in flight: two vectors a thread (batches
+    // of four ranks) from 64 MiB per rank.  Measured at 256 MiB per rank,
+    // binary32, of the copy bandwidth: R = 5 0.79 -> 0.90, R = 8 0.95 -> 1.04,
+    // R = 9 0.87 -> 1.00, R = 16 0.99 -> 1.04 (results bit-identical); R = 9 at
+    // 4 MiB lost 3 %.
+    if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && (unsigned long long)ck.count * E >= (64ull << 20))
+      U = 2;
     if (p->shifted) U = 1;  // the shifted kernel: one vector a thread
     p->direct_u = U;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight

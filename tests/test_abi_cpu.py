@@ -467,8 +467,12 @@ def test_direct_grid_waves(L):
     assert plan_dev(L, AR, 4, 1 << 27, F16)[2] == sms * 16
     assert plan_dev(L, AR, 8, 1 << 28, F16)[2] == sms * 16
     assert plan_dev(L, AG, 4, n, F32)[2] == sms * 16
-    # ReduceScatter with one full batch of eight loads a thread: two CTAs per SM, two waves
-    assert plan_dev(L, RS, 8, n, F32)[2] == sms * 4 * 2
+    # ReduceScatter from 64 MiB per rank takes two vectors a thread, so R = 8 is
+    # not one batch of eight loads (which would keep two CTAs per SM): three
+    # CTAs per SM, two waves
+    assert plan_dev(L, RS, 8, n, F32)[2] == sms * 6 * 2
+    # chunk boundaries off the 16-byte grid: the shifted kernel keeps sixteen
+    assert plan_dev(L, RS, 8, (64 << 20) // 4 - 8, F32)[2] == sms * 16
     # a grid that fits under the cap is not changed
     assert plan_dev(L, RS, 4, 1 << 20, F32)[2] == (1 << 20) * 4 // 16 // 256
 
