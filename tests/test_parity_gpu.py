@@ -420,6 +420,39 @@ def test_direct_occupancy_variants(rr, dtype, wire):
         check_rs(rr, xs, wire, cfg=cfg_of(rr, path=rr.PATH_DIRECT), what=f"occupancy RS {NAME[dtype]}/{wire} R={R}")
 
 
+@pytest.mark.parametrize("dtype,wire", [(torch.float32, None), (torch.float16, None), (torch.float32, "bf16"),
+                                        (torch.bfloat16, "f32")], ids=lambda v: str(v))
+def test_reduce_scatter_two_vectors_large(rr, dtype, wire):
+    """ReduceScatter of 64 MiB or more per rank over five and nine ranks: two
+    vectors a thread in batches of four ranks (the last batch partial), chunk
+    boundaries on the 16-byte grid, a ragged last chunk.  Every output element
+    is written; sampled elements (every chunk boundary, both ends, random ones)
+    equal the oracle's closed form."""
+    E = torch.tensor([], dtype=dtype).element_size()
+    V = 16 // E
+    for R in (5, 9):
+        base = -(-(64 << 20) // (E * R * V)) * V  # a multiple of V elements; R * base * E >= 64 MiB
+        N = R * base + (R - 2)  # floor(N / R) = base: the last chunk takes R - 2 more
+        xs = gen(R, N, dtype, 71 * R + E)
+        parts = [torch.full((rr.chunk_count(N, R, c),), float("nan"), dtype=dtype, device="cuda") for c in range(R)]
+        assert rr.plan(rr.OP_REDUCE_SCATTER, xs, parts, N, wire)["path"] == rr.PATH_DIRECT
+        rr.collective(rr.OP_REDUCE_SCATTER, xs, parts, N, wire)
+        torch.cuda.synchronize()
+        what = f"RS two vectors {NAME[dtype]}/{wire} R={R} N={N}"
+        for c in range(R):
+            assert not torch.isnan(parts[c]).any(), f"{what}: chunk {c} has unwritten elements"
+        idx = sample_indices(N, R)
+        vals = [host(x[torch.from_numpy(idx).cuda()]) for x in xs]
+        want = oracle.fold_gathered(vals, idx.astype(np.uint64), N, NAME[dtype], wire, 0)
+        owner = np.minimum(idx // base, R - 1)
+        for c in range(R):
+            sel = np.flatnonzero(owner == c)
+            loc = torch.from_numpy(idx[sel] - c * base).cuda()
+            assert_same(host(parts[c][loc]), want[sel], f"{what} chunk {c}")
+        del xs, parts
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
 def test_vectors_over_chunk_boundaries(rr, dtype, wire):
     """Chunk boundaries inside 16-byte vectors: the direct path's extra CTA
