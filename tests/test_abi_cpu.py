@@ -302,6 +302,9 @@ def test_planner_invariants_every_rank_count(L):
                                 assert (N // R * E) % 16 == 0
                         else:
                             assert 64 <= ch["threads"] <= 1024
+                        if ch["path"] == 3:  # direct: at most sixteen 128-thread CTAs per SM, plus one
+                            assert ch["threads"] == 128 and smem == 0
+                            assert grid <= GB300["sms"] * 16 + 1, (R, op, dtype, N, grid)
 
 
 def test_planner_paths(L):
