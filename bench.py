@@ -243,6 +243,33 @@ def dist_setup():
     return world, rank, local
 
 
+def free_port():
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def replica_launch_command(n, argv, port):
+    """The command that starts n ranks of this script, one per GPU, through
+    torch.distributed.run on this node (rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
+
+
+def launch_replicas(n, argv):
+    """`--gpus N` (N > 1) started without a launcher: run N ranks of this
+    script under torch.distributed.run and return its exit status.  Each rank
+    runs its own replica of the workload on GPU LOCAL_RANK; rank 0 prints the
+    JSON line.  NCCL's initialisation log stays on (unless NCCL_DEBUG is set),
+    so the communicator lines show N ranks."""
+    env = dict(os.environ)
+    env.setdefault("NCCL_DEBUG", "INFO")
+    env.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
+    return subprocess.call(replica_launch_command(n, argv, free_port()), env=env)
+
+
 # --------------------------------------------------------------------------
 # CPU oracle timing (the baseline, and the reference arm)
 # --------------------------------------------------------------------------
@@ -551,7 +578,7 @@ def run_ours(args):
     # launches over rotating buffer sets at least 3x the L2 size, so every
     # launch reads inputs that are not in L2 and no host time is included
     sweep, table, overlap = [], [], None
-    if not args.no_sweep:
+    if not args.no_sweep and world == 1:  # per-GPU tables: every replica would measure the same
         del outs
         torch.cuda.empty_cache()
         for mib in SWEEP_MIB:
@@ -696,6 +723,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) != args.gpus:
+        ap.error(f"--gpus {args.gpus} but the launcher started WORLD_SIZE={os.environ['WORLD_SIZE']} ranks")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
     if args.impl == "reference":
         run_reference(args)
     else:

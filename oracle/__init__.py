@@ -12,7 +12,9 @@ Element conventions: ``"f32"`` arrays are ``numpy.float32``; ``"f16"`` and
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -38,14 +40,33 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
           "-Wall", "-Wextra"]
 
 
+def _digest() -> str:
+    """Digest of the oracle's sources, the gcc command line and the machine type."""
+    h = hashlib.sha256()
+    for f in (_SRC, _HDR):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    h.update(" ".join(CFLAGS).encode() + platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle into ``libringoracle.so`` (gcc, plain C11)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))):
-        return _LIB_PATH
+    """Compile the oracle into ``libringoracle.so`` (gcc, plain C11).  A library
+    is reused only when the digest recorded beside it (``.libringoracle.digest``)
+    matches its sources, flags and machine type."""
+    digest = _digest()
+    stamp = os.path.join(_HERE, ".libringoracle.digest")
+    if not force and os.path.exists(_LIB_PATH) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == digest:
+                return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
+    with open(stamp + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(stamp + f".tmp{os.getpid()}", stamp)
     return _LIB_PATH
 
 

@@ -297,18 +297,38 @@ def host_workspace_bytes(R: int, piece_count: int, dtype) -> int:
     return int(lib().ring_allreduce_host_workspace(R, piece_count, _code(dtype)))
 
 
+def _check_host_buffers(host_ins, host_outs):
+    """The host-buffer entry points copy count * element-size bytes per rank
+    to and from the given addresses, and the C ABI cannot see how large a host
+    buffer is, so every size is checked here: one input and one output per
+    rank, all contiguous CPU tensors of one dtype holding exactly N elements.
+    Returns (R, N)."""
+    if not host_ins:
+        raise ValueError("host_ins: need at least one rank")
+    R, N, dtype = len(host_ins), host_ins[0].numel(), host_ins[0].dtype
+    if len(host_outs) != R:
+        raise ValueError(f"host_outs: {len(host_outs)} buffers for {R} ranks")
+    for name, ts in (("host_ins", host_ins), ("host_outs", host_outs)):
+        for r, t in enumerate(ts):
+            if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or not t.is_contiguous():
+                raise ValueError(f"{name}[{r}]: every buffer must be a contiguous CPU tensor")
+            if t.dtype != dtype:
+                raise ValueError(f"{name}[{r}]: dtype {t.dtype}, expected {dtype}")
+            if t.numel() != N:
+                raise ValueError(f"{name}[{r}]: {t.numel()} elements, expected {N}")
+    return R, N
+
+
 def allreduce_host(host_ins, host_outs=None, workspace: Optional[torch.Tensor] = None, wire=None,
                    group_size: int = 0, stream=None, piece_count: int = 1 << 24):
     """ring_allreduce_host: CPU tensors in and out (page-locked for overlap),
     pipelined through a device workspace (allocated here if not given)."""
     host_ins = list(host_ins)
-    dtype = host_ins[0].dtype
-    for t in host_ins:
-        if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != dtype:
-            raise ValueError("host_ins: contiguous CPU tensors of one dtype")
     if host_outs is None:
         host_outs = [torch.empty_like(t, pin_memory=t.is_pinned()) for t in host_ins]
-    R, N = len(host_ins), host_ins[0].numel()
+    host_outs = list(host_outs)
+    R, N = _check_host_buffers(host_ins, host_outs)
+    dtype = host_ins[0].dtype
     if workspace is None:
         nbytes = host_workspace_bytes(R, min(piece_count, max(N, 1)), dtype)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=torch.cuda.current_device())
@@ -329,11 +349,8 @@ def allreduce_host_static(host_ins, host_outs, wire=None, group_size: int = 0, p
     staging memory built into the library, so nothing is allocated (host_outs
     must be given; it may be host_ins for in place)."""
     host_ins, host_outs = list(host_ins), list(host_outs)
+    R, N = _check_host_buffers(host_ins, host_outs)
     dtype = host_ins[0].dtype
-    for t in host_ins + host_outs:
-        if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != dtype:
-            raise ValueError("host buffers: contiguous CPU tensors of one dtype")
-    R, N = len(host_ins), host_ins[0].numel()
     dt = _code(dtype)
     wt = dt if wire is None else _code(wire)
     hin = (ctypes.c_void_p * R)(*[t.data_ptr() for t in host_ins])

@@ -3,12 +3,20 @@
 Each translation unit under csrc/ compiles in parallel to an object under
 _build/, then nvcc links the shared library next to this file.  No fast-math
 and no FMA contraction: the kernels' results are defined bit for bit.
+
+A build is reused only when the digest recorded beside it (under _build/)
+matches the digest of what it was built from: the contents of every file under
+csrc/ and include/, the compiler command line, the nvcc binary and the host
+machine type.  A library copied in from elsewhere, or one older or newer than
+its sources by file time, is rebuilt rather than trusted.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 
@@ -30,16 +38,38 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _deps_mtime() -> float:
-    files = glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h"))
-    return max(os.path.getmtime(f) for f in files)
+def source_digest(cc: str, flags) -> str:
+    """Digest of everything the library is built from (see the module docstring)."""
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h")))
+    for f in files:
+        h.update(os.path.relpath(f, ROOT).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    h.update(" ".join([os.path.realpath(cc), *ARCH, *flags]).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
+def _digest_path(lib: str) -> str:
+    return os.path.join(BUILD, os.path.basename(lib) + ".digest")
+
+
+def _recorded_digest(lib: str):
+    try:
+        with open(_digest_path(lib)) as f:
+            return f.read().strip()
+    except OSError:
+        return None
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+    cc = nvcc()
+    digest = source_digest(cc, FLAGS)
+    if not force and os.path.exists(LIB) and _recorded_digest(LIB) == digest:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    cc = nvcc()
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 
@@ -62,6 +92,9 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(_digest_path(LIB) + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(_digest_path(LIB) + f".tmp{os.getpid()}", _digest_path(LIB))
     return LIB
 
 

@@ -41,6 +41,8 @@
 //  overlap the kernel before it on the stream.
 #pragma once
 
+#include <mutex>
+
 #include "rr_device.cuh"
 
 namespace rr {
@@ -813,15 +815,22 @@ inline cudaError_t launch_kernel(void (*k)(RingParams), const Launch &l, size_t 
 template <int OP, int DT, int WT, bool HD>
 cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s) {
   if (l.path == RR_PATH_BULK) {
-    static int smem_set[64] = {0};  // largest dynamic shared memory opted in, per device
+    // Largest dynamic shared memory opted in, per device.  The attribute is
+    // only ever raised, and the raise and its record happen under one lock, so
+    // a thread that finds a size recorded knows the attribute is at least that.
+    static std::mutex smem_mu;
+    static int smem_set[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (l.smem > 48 * 1024 && (dev >= 64 || smem_set[dev] < (int)l.smem)) {
-      e = cudaFuncSetAttribute(rr_bulk_kernel<OP, DT, WT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)l.smem);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) smem_set[dev] = (int)l.smem;
+    if (l.smem > 48 * 1024) {
+      std::lock_guard<std::mutex> lock(smem_mu);
+      if (dev >= 64 || smem_set[dev] < (int)l.smem) {
+        e = cudaFuncSetAttribute(rr_bulk_kernel<OP, DT, WT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)l.smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) smem_set[dev] = (int)l.smem;
+      }
     }
     return launch_kernel(rr_bulk_kernel<OP, DT, WT, HD>, l, l.smem, s, p);
   } else if (l.path == RR_PATH_DIRECT) {

@@ -507,3 +507,29 @@ def test_rank_buffers_layout():
         rr.rank_buffers(2, 8, torch.float32, "cpu", stagger_bytes=100)
     with pytest.raises(ValueError):
         rr.rank_buffers(3, [1, 2], torch.float32, "cpu")
+
+
+def test_binding_checks_host_buffer_sizes(L):
+    """The host-buffer entry points copy N elements per rank to and from raw
+    host addresses, which the C ABI cannot bound, so the binding checks every
+    list length and element count before it passes a pointer on."""
+    import torch
+
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    R, N = 4, 1000
+    hin = [torch.zeros(N) for _ in range(R)]
+    cases = [
+        (hin, [torch.zeros(N) for _ in range(R - 1)], "host_outs: 3 buffers for 4 ranks"),
+        (hin, [torch.zeros(N) for _ in range(R + 1)], "host_outs: 5 buffers for 4 ranks"),
+        (hin, [torch.zeros(N) for _ in range(R - 1)] + [torch.zeros(N - 1)], "host_outs[3]: 999 elements"),
+        (hin[:2] + [torch.zeros(N + 7)] + hin[3:], [torch.zeros(N) for _ in range(R)], "host_ins[2]: 1007"),
+        (hin, [torch.zeros(N) for _ in range(R - 1)] + [torch.zeros(N, dtype=torch.float64)], "host_outs[3]: dtype"),
+        (hin, [torch.zeros(N) for _ in range(R - 1)] + [torch.zeros(2 * N)[::2]], "host_outs[3]: every buffer"),
+        ([], [], "host_ins: need at least one rank"),
+    ]
+    for ins, outs, msg in cases:
+        with pytest.raises(ValueError, match=re.escape(msg)):
+            rr.allreduce_host_static(ins, outs)
+        with pytest.raises(ValueError, match=re.escape(msg)):
+            rr.allreduce_host(ins, host_outs=outs, workspace=torch.empty(16, dtype=torch.uint8))

@@ -104,3 +104,27 @@ def test_kernel_digest_ignores_comments_only():
     assert bench.code_only(src) == bench.code_only(same)
     assert bench.code_only(src) != bench.code_only(other)
     assert '"a//b /* c */"' in bench.code_only(src)
+
+
+def test_gpus_flag_launches_replicas_itself(tmp_path):
+    """`bench.py --gpus 2` started without a launcher starts two ranks under
+    torch.distributed.run by itself; rank 0 alone prints one JSON line, which
+    reports both ranks.  (The reference arm runs here: it needs no GPU.)"""
+    import subprocess
+
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3", "--ref-sample-mib", "1"],
+                       capture_output=True, text=True, env=env, timeout=600, cwd=str(tmp_path))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_replica_launch_command():
+    cmd = bench.replica_launch_command(4, ["--gpus", "4", "--steps", "5"], 29511)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--master-addr=127.0.0.1" in cmd and "--master-port=29511" in cmd
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "5"] and cmd[-5].endswith("bench.py")

@@ -3,9 +3,14 @@
 Every case runs through the C ABI (the Python binding only marshals) and is
 compared element by element with the oracle's literal ring simulation, or, at
 the full workload sizes, on sampled elements with the oracle's closed form
-plus size-independent properties.  The bar is bit-exact for every format:
-both sides follow the same accumulation order and rounding.
+plus size-independent properties, and then on every element against the
+oracle's closed form evaluated on all host cores.  The bar is bit-exact for
+every format: both sides follow the same accumulation order and rounding.
 """
+import collections
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -543,6 +548,62 @@ def check_sampled(rr, xs, outs, wire=None, group=0, what=""):
                 f"{what}: output {r} differs from output 0"
 
 
+def full_check_workers():
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def check_full(rr, xs, outs, wire=None, group=0, algo="ring", what="", piece=1 << 21):
+    """Every element of the AllReduce against the oracle's closed form.
+
+    Output 0 is compared element by element with the closed form over the
+    whole index range [0, N).  The range is split into disjoint pieces that the
+    host's cores evaluate at once: the closed form is element-wise (each
+    element's fold depends only on its own chunk), so the split cannot change
+    a bit, and ctypes releases the interpreter lock during the oracle call.
+    Inputs and output come back from the device one piece at a time, so host
+    memory stays bounded.  Every other output must equal output 0 bit for bit
+    (compared on the device)."""
+    R, N = len(xs), xs[0].numel()
+    dt = NAME[xs[0].dtype]
+    workers = full_check_workers()
+
+    def one(a, vals, got):
+        idx = np.arange(a, a + got.size, dtype=np.uint64)
+        if algo == "ring":
+            want = oracle.fold_gathered(vals, idx, N, dt, wire, group)
+        else:
+            want = oracle.fold_gathered_algo(vals, idx, N, dt, wire, algo)
+        g, w = bits(got), bits(want)
+        if np.array_equal(g, w):
+            return None
+        bad = np.flatnonzero(g != w)
+        k = int(bad[0])
+        return f"{bad.size} of {g.size} elements of [{a}, {a + g.size}) differ, first at {a + k}: " \
+               f"got {int(g[k]):#x} want {int(w[k]):#x}"
+
+    failures = []
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        pending = collections.deque()
+        for a in range(0, N, piece):
+            b = min(N, a + piece)
+            pending.append(ex.submit(one, a, [host(x[a:b]) for x in xs], host(outs[0][a:b])))
+            while len(pending) > workers + 2:
+                err = pending.popleft().result()
+                if err:
+                    failures.append(err)
+        while pending:
+            err = pending.popleft().result()
+            if err:
+                failures.append(err)
+    assert not failures, f"{what} rank 0: " + "; ".join(failures[:4])
+    iv = torch.int16 if outs[0].element_size() == 2 else torch.int32
+    for r in range(1, R):
+        assert torch.equal(outs[r].view(iv), outs[0].view(iv)), f"{what}: output {r} differs from output 0"
+
+
 def big_inputs(R, N, dtype, seed, piece=1 << 28):
     g = torch.Generator(device="cuda")
     g.manual_seed(seed)
@@ -612,21 +673,31 @@ def test_workload2_full_oracle(rr, wl, mib):
 
 
 @pytest.mark.parametrize("mib", [128, 512])
-def test_workload2_sampled(rr, wl, mib):
-    xs = wl.inputs(wl.config2(mib), "cuda")
-    outs = rr.allreduce(xs)
+def test_workload2_full_size(rr, wl, mib):
+    """The benchmark's workload in its launch configuration (staggered rank
+    buffers), every element of every output."""
+    w = wl.config2(mib)
+    xs = rr.rank_buffers(w.R, w.count, w.dtype, "cuda")
+    for r in range(w.R):
+        wl.rank_values(w.wid, r, w.count, w.dtype, w.dist, "cuda", out=xs[r])
+    outs = rr.rank_buffers(w.R, w.count, w.dtype, "cuda")
+    rr.allreduce(xs, outs=outs)
     torch.cuda.synchronize()
-    check_sampled(rr, xs, outs, what=f"workload 2 {mib} MiB")
+    check_sampled(rr, xs, outs, what=f"workload 2 {mib} MiB")  # quick pre-check
+    check_full(rr, xs, outs, what=f"workload 2 {mib} MiB")
     del outs, xs
     torch.cuda.empty_cache()
 
 
-def test_workload3_sampled_full_size(rr, wl):
+def test_workload3_full_size(rr, wl):
     w = wl.config3()
     xs = wl.inputs(w, "cuda")
     outs = rr.allreduce(xs, wire="bf16")
     torch.cuda.synchronize()
     check_sampled(rr, xs, outs, wire="bf16", what="workload 3")
+    check_full(rr, xs, outs, wire="bf16", what="workload 3")
+    del outs, xs
+    torch.cuda.empty_cache()
 
 
 def test_workload3_shape_full_oracle(rr):
@@ -645,12 +716,13 @@ def test_workload4_full_oracle(rr, wl):
 
 
 @pytest.mark.parametrize("bucket", [0, 48])
-def test_workload5_bucket_sampled(rr, wl, bucket):
+def test_workload5_bucket_full_size(rr, wl, bucket):
     w = wl.config5(bucket)
     xs = wl.inputs(w, "cuda", bucket=bucket)
     outs = rr.allreduce(xs)
     torch.cuda.synchronize()
     check_sampled(rr, xs, outs, what=f"workload 5 bucket {bucket}")
+    check_full(rr, xs, outs, what=f"workload 5 bucket {bucket}")
     del outs, xs
     torch.cuda.empty_cache()
 
@@ -781,7 +853,7 @@ def test_algorithm_occupancy_variants(rr, dtype, wire):
 
 
 @pytest.mark.parametrize("algo", ["hd", "naive"])
-def test_algorithm_full_size_sampled(rr, wl, algo):
+def test_algorithm_full_size(rr, wl, algo):
     xs = wl.inputs(wl.config2(512), "cuda")
     outs = rr.allreduce_algo(xs, algo=algo)
     torch.cuda.synchronize()
@@ -789,9 +861,9 @@ def test_algorithm_full_size_sampled(rr, wl, algo):
     idx = sample_indices(N, 8)
     ti = torch.from_numpy(idx).cuda()
     want = oracle.fold_gathered_algo([host(x[ti]) for x in xs], idx.astype(np.uint64), N, "f16", None, algo)
-    for r in range(8):
+    for r in range(8):  # quick pre-check on sampled elements
         assert_same(host(outs[r][ti]), want, f"{algo} 512 MiB sampled rank {r}")
-        assert torch.equal(outs[r].view(torch.int16), outs[0].view(torch.int16))
+    check_full(rr, xs, outs, algo=algo, what=f"{algo} 512 MiB")
     del outs, xs
     torch.cuda.empty_cache()
 

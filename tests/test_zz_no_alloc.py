@@ -58,13 +58,63 @@ def test_static_staging_matches_workspace_entry_point(rr, dtype, wire, R, L, N, 
             assert same_bits(got[r], want[r]), f"call {call}, rank {r}"
 
 
-def test_static_staging_rejects_pieces_beyond_its_size(rr):
-    R = 64
-    hin = host_inputs(R, 1024, torch.float32, seed=5)
-    out = [torch.empty_like(t) for t in hin]
-    largest = (32 << 20) // (3 * R * 4) // 256 * 256
+def static_scratch_bytes():
+    """RR_STATIC_SCRATCH_BYTES as the public header defines it."""
+    import os
+    import re
+
+    header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ringred.h")
+    with open(header) as f:
+        m = re.search(r"#define\s+RR_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", f.read())
+    assert m, "RR_STATIC_SCRATCH_BYTES not found in ringred.h"
+    return int(m.group(1)) << int(m.group(2))
+
+
+def largest_static_piece(rr, R, dtype):
+    """The largest piece_count whose three slots fit the staging array, found
+    through the ABI's own workspace rule (ring_allreduce_host_workspace) by
+    bisection, so the test follows the header's documented limit and not a
+    copy of the library's internal constants."""
+    limit = static_scratch_bytes()
+    lo, hi = 0, limit  # workspace(lo) fits (or lo = 0), workspace(hi) does not
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if rr.host_workspace_bytes(R, mid, dtype) <= limit:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+@pytest.mark.parametrize("R,dtype", [(64, torch.float32), (8, torch.float16)])
+def test_static_staging_rejects_pieces_beyond_its_size(rr, R, dtype):
+    largest = largest_static_piece(rr, R, dtype)
+    assert largest > 0
+    N = 2 * largest + 1000  # three pieces at the largest size, the last one ragged
+    hin = host_inputs(R, N, dtype, seed=5 + R)
+    got = [torch.full_like(t, 7).pin_memory() for t in hin]
     with pytest.raises(rr.RingError) as e:
-        rr.allreduce_host_static(hin, out, piece_count=largest + 1)
+        rr.allreduce_host_static(hin, got, piece_count=largest + 1)
     assert e.value.status == rr.ERR_INVALID_ARG
-    rr.allreduce_host_static(hin, out, piece_count=largest)  # the largest piece fits
+    assert all(torch.equal(t, torch.full_like(t, 7)) for t in got)  # rejected before anything was written
+    ws = torch.empty(rr.host_workspace_bytes(R, 1 << 16, dtype), dtype=torch.uint8, device="cuda")
+    want = [torch.empty_like(t).pin_memory() for t in hin]
+    rr.allreduce_host(hin, host_outs=want, workspace=ws)
+    rr.allreduce_host_static(hin, got, piece_count=largest)  # the largest piece fits
     torch.cuda.current_stream().synchronize()
+    for r in range(R):
+        assert same_bits(got[r], want[r]), f"largest piece, rank {r}"
+
+
+def test_static_staging_in_place(rr):
+    """host_outs may be host_ins: the result replaces the inputs."""
+    R, N, dtype = 8, 1_500_007, torch.bfloat16
+    ws = torch.empty(rr.host_workspace_bytes(R, 1 << 16, dtype), dtype=torch.uint8, device="cuda")
+    for call in range(2):
+        hin = host_inputs(R, N, dtype, seed=77 + call)
+        want = [torch.empty_like(t).pin_memory() for t in hin]
+        rr.allreduce_host([t.clone() for t in hin], host_outs=want, workspace=ws)
+        rr.allreduce_host_static(hin, hin, piece_count=65536 if call else 0)
+        torch.cuda.current_stream().synchronize()
+        for r in range(R):
+            assert same_bits(hin[r], want[r]), f"in place, call {call}, rank {r}"
