@@ -23,6 +23,8 @@ region, pipelined in pieces), the CPU oracle's throughput on a bounded sample, a
 sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --path-sweep [--sweep-ops ar,rs,ag] [--sweep-ranks ...] [--sweep-mib ...]
+                  [--sweep-off-grid no|only|both] [--sweep-variants]
 """
 from __future__ import annotations
 
@@ -307,6 +309,43 @@ def staggered_inputs(rr, wl, w, dev, in_lens=None, out_lens=None):
     return ins, rr.rank_buffers(w.R, out_lens, w.dtype, dev)
 
 
+REPLAYS, REPLAY_WARMUP = 20, 5
+
+
+def time_replays(dev, sets, call, launches):
+    """Per-call time (ms) of `call` by CUDA-graph replay: one graph of
+    `launches` back-to-back calls cycling through the buffer sets, REPLAY_WARMUP
+    untimed replays, then REPLAYS replays each timed with CUDA events on the
+    replay stream.  Returns (median, min, max) over the replays of the replay
+    time / launches (a replay's events sit on the stream replay() launches on)."""
+    import torch
+
+    for ins, outs in sets:  # warm up outside capture (first-call set-up)
+        call(ins, outs)
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.Stream(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for k in range(launches):
+                ins, outs = sets[k % len(sets)]
+                call(ins, outs, s)
+    for _ in range(REPLAY_WARMUP):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    cur = torch.cuda.current_stream(dev)  # replay() launches on the current stream
+    times = []
+    for _ in range(REPLAYS):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        g.replay()
+        b.record(cur)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b) / launches)
+    del g
+    return statistics.median(times), min(times), max(times)
+
+
 def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring", cfg=None):
     """Time workload w: CUDA-graph replay of `launches` back-to-back calls over
     rotating buffer sets (>= 3x L2 in total).  Returns one table row."""
@@ -336,36 +375,17 @@ def graph_row(rr, wl, w, dev, l2_bytes, peak, launches, algo="ring", cfg=None):
         else:
             rr.allreduce_algo(ins, outs, w.wire, algo, stream, cfg)
 
-    for ins, outs in sets:  # warm up outside capture
-        call(ins, outs)
-    torch.cuda.synchronize(dev)
-    s = torch.cuda.Stream(dev)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            for k in range(launches):
-                ins, outs = sets[k % nsets]
-                call(ins, outs, s)
-    g.replay()
-    torch.cuda.synchronize(dev)
-    times = []
-    for _ in range(3):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        g.replay()
-        b.record()
-        torch.cuda.synchronize(dev)
-        times.append(a.elapsed_time(b) / launches)
-    t_ms = min(times)
+    t_ms, t_min, t_max = time_replays(dev, sets, call, launches)
     alg = (2 * R_ if op == rr.OP_ALLREDUCE else R_ + 1) * msg
     busbw = msg / t_ms / 1e6 * ((2 if op == rr.OP_ALLREDUCE else 1) * (R_ - 1) / R_)
     row = {"workload": w.name if algo == "ring" else f"{w.name}, {algo} order", "op": w.op, "algo": algo,
            "R": R_, "group_size": w.group_size or R_, "count": N,
-           "msg_bytes": msg, "ms": round(t_ms, 5), "algbw_gbs": round(msg / t_ms / 1e6, 2),
+           "msg_bytes": msg, "ms": round(t_ms, 5), "ms_min": round(t_min, 5), "ms_max": round(t_max, 5),
+           "replays": REPLAYS, "algbw_gbs": round(msg / t_ms / 1e6, 2),
            "busbw_gbs": round(busbw, 2), "hbm_gbs": round(alg / t_ms / 1e6, 1),
            "roofline_frac": round(alg / t_ms / 1e6 / peak, 4), "buffer_sets": nsets,
            "plan": rr.plan(op, sets[0][0], sets[0][1], N, w.wire, w.group_size, cfg)}
-    del g, sets
+    del sets
     return row
 
 
@@ -412,12 +432,54 @@ def bucket_set_row(rr, wl, dev, peak):
     return row
 
 
-def overlap_row(rr, wl, dev, pieces=8, max_ctas=0):
+def host_link_speeds(dev, host_in, host_out, dev_src):
+    """The host link alone, on the e2e step's own page-locked buffers: the R
+    inputs copied to the device, the R results copied back, each alone and
+    both at once (one stream each way), median of 3.  Tells a slow host-buffer
+    pipeline from a slow link."""
+    import torch
+
+    nbytes = sum(t.numel() * t.element_size() for t in host_in)
+    dst = [torch.empty_like(t, device=dev) for t in host_in]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(h2d, d2h):
+        cur = torch.cuda.current_stream(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(cur)
+        up.wait_stream(cur)
+        down.wait_stream(cur)
+        if h2d:
+            with torch.cuda.stream(up):
+                for d, h in zip(dst, host_in):
+                    d.copy_(h, non_blocking=True)
+        if d2h:
+            with torch.cuda.stream(down):
+                for h, d in zip(host_out, dev_src):
+                    h.copy_(d, non_blocking=True)
+        cur.wait_stream(up)
+        cur.wait_stream(down)
+        t1.record(cur)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1)
+
+    def med(h2d, d2h):
+        run(h2d, d2h)
+        return statistics.median(run(h2d, d2h) for _ in range(3))
+
+    h, d, both = med(True, False), med(False, True), med(True, True)
+    del dst
+    return {"h2d_ms": round(h, 3), "d2h_ms": round(d, 3), "both_ms": round(both, 3),
+            "h2d_gbs": round(nbytes / h / 1e6, 1), "d2h_gbs": round(nbytes / d / 1e6, 1)}
+
+
+def overlap_row(rr, wl, dev, pieces=8, max_ctas=0, beside_compute=0):
     """Chunked AllReduce overlapped with compute (the pattern of the page
     bjdmk.com.cn/news/5966809, sections 4.2-4.3): `pieces` bf16 GEMMs run on the
     compute stream; after each one an event releases one range of a 512 MiB
     fp16 AllReduce (R = 8) on a communication stream.  Reports the two
-    streams alone and together."""
+    streams alone and together (median of 5 runs each); the AllReduce's grid
+    is uncapped, capped at max_ctas, or capped by the library (beside_compute)."""
     import torch
 
     w = wl.config2(512)
@@ -441,7 +503,7 @@ def overlap_row(rr, wl, dev, pieces=8, max_ctas=0):
             for _ in range(pieces):
                 torch.matmul(A, B, out=C)
 
-    cfg = rr.LaunchCfg(0, 0, 0, 0, 0, max_ctas)
+    cfg = rr.LaunchCfg(0, 0, 0, 0, 0, max_ctas, 0, 0, beside_compute)
 
     def comm_only():
         for k in range(pieces):
@@ -460,8 +522,8 @@ def overlap_row(rr, wl, dev, pieces=8, max_ctas=0):
     def timed(fn):
         fn()
         torch.cuda.synchronize(dev)
-        best = None
-        for _ in range(3):
+        runs = []
+        for _ in range(5):
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             cur = torch.cuda.current_stream(dev)
@@ -473,16 +535,17 @@ def overlap_row(rr, wl, dev, pieces=8, max_ctas=0):
             cur.wait_stream(comm)
             t1.record(cur)
             torch.cuda.synchronize(dev)
-            ms = t0.elapsed_time(t1)
-            best = ms if best is None else min(best, ms)
-        return best
+            runs.append(t0.elapsed_time(t1))
+        return statistics.median(runs)
 
     t_comp, t_comm, t_both = timed(compute_only), timed(comm_only), timed(both)
     hidden = (t_comp + t_comm - t_both) / min(t_comp, t_comm)
     del xs, outs, A, B, C
     torch.cuda.empty_cache()
+    grid = rr.plan(rr.OP_ALLREDUCE, [x[:step] for x in xs], [o[:step] for o in outs], step, cfg=cfg)["max_ctas"]
     return {"what": f"{pieces} bf16 GEMMs {n}^3 on a compute stream; after each, one of {pieces} ranges of the "
                     f"512 MiB R=8 fp16 AllReduce on a communication stream", "max_ctas": max_ctas,
+            "beside_compute": beside_compute, "allreduce_grid": grid,
             "compute_ms": round(t_comp, 3),
             "allreduce_ms": round(t_comm, 3), "together_ms": round(t_both, 3),
             "serial_ms": round(t_comp + t_comm, 3), "fraction_of_shorter_hidden": round(hidden, 3)}
@@ -595,7 +658,8 @@ def run_ours(args):
             del xs
             torch.cuda.empty_cache()
             table.append(bucket_set_row(rr, wl, dev, peak))
-            overlap = [overlap_row(rr, wl, dev, max_ctas=m) for m in (0, 128, 96)]
+            overlap = [overlap_row(rr, wl, dev, max_ctas=m) for m in (0, 128, 96, 64)]
+            overlap.append(overlap_row(rr, wl, dev, beside_compute=1))
             xs, outs = staggered_inputs(rr, wl, w, dev)
         else:
             outs = rr.rank_buffers(R, N, torch.float16, dev)
@@ -633,7 +697,8 @@ def run_ours(args):
         e2e = {"value": round(job_throughput(world, msg, e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": R * msg, "d2h_bytes_per_step": R * msg, "ms_per_step": round(e_ms, 4),
                "steps": args.e2e_steps, "api": "ring_allreduce_host",
-               "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity}
+               "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity,
+               "link": host_link_speeds(dev, host_in, host_out, xs)}
         del host_in, host_out, ws
         outs = rr.rank_buffers(R, N, torch.float16, dev)
 
@@ -665,6 +730,114 @@ def run_ours(args):
     if pg:
         pg.barrier()
         pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# path sweep: the measurements behind the planner's choices
+# --------------------------------------------------------------------------
+
+SWEEP_OPS = {"ar": 0, "rs": 1, "ag": 2}
+
+
+def sweep_variants(rr, op, wide, shifted, all_variants):
+    """(label, cfg) pairs to time at one point: the planner's choice, the tile
+    pipeline and the direct path (each forced), and with all_variants every
+    direct kernel the library builds (vectors a thread x register budget)."""
+    out = [("auto", None), ("bulk", rr.LaunchCfg(rr.PATH_BULK)), ("direct", rr.LaunchCfg(rr.PATH_DIRECT))]
+    if all_variants:
+        if shifted:
+            rows = (1, 2, 4) if op == 2 else ((1, 2) if wide else (1, 2, 3, 4))
+            pairs = [(u, 0) for u in rows]
+        elif op == 2:
+            pairs = [(1, 2), (2, 2), (4, 2)]
+        elif wide:
+            pairs = [(1, 2), (2, 2)]
+        else:
+            pairs = [(1, 2), (1, 3), (2, 2), (2, 3), (3, 2), (4, 2)]
+        for u, occ in pairs:
+            out.append((f"direct U={u} occ={occ or 'auto'}", rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, occ, 0, 0, 0, u)))
+    return out
+
+
+def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid, all_variants):
+    """Time every variant of one (collective, ranks, size) point.  Chunks are
+    whole multiples of the 16-byte vector (or, off_grid, one element more, so
+    chunk boundaries fall off the 16-byte grid).  Returns JSON rows."""
+    import torch
+
+    E = torch.tensor([], dtype=dtype).element_size()
+    V = 16 // E
+    base = max(V, (mib * MIB // E) // R_ // V * V) + (1 if off_grid else 0)
+    N = R_ * base
+    lens = [rr.chunk_count(N, R_, c) for c in range(R_)]
+    in_lens = lens if op == 2 else [N] * R_
+    out_lens = lens if op == 1 else [N] * R_
+    set_bytes = (sum(in_lens) + sum(out_lens)) * E
+    nsets = max(1, min(16, -(-3 * l2_bytes // set_bytes)))
+    sets = []
+    for k in range(nsets):
+        ins = rr.rank_buffers(R_, in_lens, dtype, dev)
+        for x in ins:
+            x.copy_(torch.randn(x.numel(), device=dev).mul_(1e-2).to(dtype))
+        sets.append((ins, rr.rank_buffers(R_, out_lens, dtype, dev)))
+    msg = N * E
+    alg = (2 * R_ if op == 0 else R_ + 1) * msg
+    # about 2 ms of work per replay, 4 to 40 launches
+    launches = max(4, min(40, int(2e-3 * 6.5e12 / alg) + 1))
+    wide = dtype != torch.float32 and wire == "f32"
+    shifted = off_grid and op != 0
+    rows = []
+    for label, cfg in sweep_variants(rr, op, wide, shifted, all_variants):
+        try:
+            plan = rr.plan(op, sets[0][0], sets[0][1], N, wire, 0, cfg)
+        except rr.RingError:
+            continue  # a path these buffers do not allow
+        if label != "auto" and plan["path"] == rr.PATH_SIMPLE:
+            continue
+
+        def call(ins, outs, stream=None, cfg=cfg):
+            rr.collective(op, ins, outs, N, wire, 0, stream, cfg)
+
+        med, lo, hi = time_replays(dev, sets, call, launches)
+        rows.append({"op": {0: "allreduce", 1: "reduce_scatter", 2: "allgather"}[op], "R": R_, "count": N,
+                     "msg_bytes": msg, "off_grid": off_grid, "variant": label,
+                     "path": {1: "bulk", 2: "simple", 3: "direct"}[plan["path"]], "vectors": plan["vectors"],
+                     "ctas_per_sm": plan["ctas_per_sm"], "grid": plan["max_ctas"],
+                     "us": round(med * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                     "frac": round(alg / (med * 1e-3) / 1e9 / peak, 4), "replays": REPLAYS, "launches": launches})
+    del sets
+    torch.cuda.empty_cache()
+    return rows
+
+
+def run_path_sweep(args):
+    """--path-sweep: one JSON line per (point, variant) on stdout; the planner's
+    rules in the library cite these measurements."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import ring_allreduce_reducescatter_gb300 as rr
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2_bytes = int(getattr(props, "L2_cache_size", 128 * MIB))
+    peak, _ = measured_hbm_peak()
+    dtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.sweep_dtype]
+    wire = args.sweep_wire or None
+    for op_name in args.sweep_ops.split(","):
+        op = SWEEP_OPS[op_name]
+        for R_ in (int(v) for v in args.sweep_ranks.split(",")):
+            for mib in (int(v) for v in args.sweep_mib.split(",")):
+                for off_grid in ((False, True) if args.sweep_off_grid == "both" else
+                                 ((True,) if args.sweep_off_grid == "only" else (False,))):
+                    if off_grid and op == 0:
+                        continue
+                    for row in path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid,
+                                                args.sweep_variants):
+                        print(json.dumps(row), flush=True)
 
 
 # --------------------------------------------------------------------------
@@ -721,6 +894,16 @@ def main():
     ap.add_argument("--no-workloads", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path-sweep", action="store_true",
+                    help="time the planner's choice against the forced tile pipeline and direct path instead")
+    ap.add_argument("--sweep-ops", default="ar,rs,ag")
+    ap.add_argument("--sweep-ranks", default="2,3,4,5,8,9,12,16,32")
+    ap.add_argument("--sweep-mib", default="1,4,16,64,256")
+    ap.add_argument("--sweep-dtype", default="f16", choices=["f32", "f16", "bf16"])
+    ap.add_argument("--sweep-wire", default="", choices=["", "f32", "f16", "bf16"])
+    ap.add_argument("--sweep-off-grid", default="no", choices=["no", "only", "both"],
+                    help="chunk boundaries off the 16-byte grid (ReduceScatter / AllGather)")
+    ap.add_argument("--sweep-variants", action="store_true", help="every direct kernel variant too")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.gpus < 1:
@@ -729,7 +912,9 @@ def main():
         ap.error(f"--gpus {args.gpus} but the launcher started WORLD_SIZE={os.environ['WORLD_SIZE']} ranks")
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
-    if args.impl == "reference":
+    if args.path_sweep:
+        run_path_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -81,7 +81,7 @@ extern "C" {
 typedef struct CUstream_st *cudaStream_t;
 
 #define RR_MAX_RANKS 64
-#define RR_ABI_VERSION 2
+#define RR_ABI_VERSION 3
 
 typedef enum { RR_FP32 = 0, RR_FP16 = 1, RR_BF16 = 2 } rr_dtype;
 
@@ -154,12 +154,17 @@ rr_status ring_allgather(const void *const *in_bufs, void *const *out_bufs, int 
  * thread with plain loads and stores (any alignment). */
 typedef enum { RR_PATH_AUTO = 0, RR_PATH_BULK = 1, RR_PATH_SIMPLE = 2, RR_PATH_DIRECT = 3 } rr_path;
 
-/* Optional launch configuration; zero fields mean "choose automatically". */
+/* Optional launch configuration; zero fields mean "choose automatically".
+ * A configuration never changes the result, only the speed. */
 typedef struct {
   int path;        /* rr_path */
   int tile_bytes;  /* bulk path: bytes per rank per tile, a multiple of 16 */
   int stages;      /* bulk path: tiles in flight per CTA, 2..16 */
-  int ctas_per_sm; /* bulk path: 1..4 */
+  int ctas_per_sm; /* bulk path: 1..4.  Direct path: 2 or 3, the 256-thread
+                      CTAs per SM its registers are budgeted for (3: at most
+                      85 registers a thread, more CTAs resident).  A value
+                      the direct kernel is not built for is ignored, or
+                      RR_ERR_UNSUPPORTED when path is RR_PATH_DIRECT. */
   int threads;     /* threads per CTA: 64..1024, a multiple of 32 */
   int max_ctas;    /* at most this many CTAs (0: no limit); a chunked AllReduce
                       that runs beside compute kernels can leave them SMs.
@@ -169,8 +174,21 @@ typedef struct {
                       while the previous kernel on the stream is still
                       running (programmatic dependent launch: it waits for that
                       kernel's completion and writes before touching memory);
-                      2: plain stream order.  Never changes the result. */
+                      2: plain stream order. */
+  int vectors;     /* direct path: 16-byte vectors a thread takes at once,
+                      1..4 (AllGather 1, 2 or 4; 16-bit storage summed in
+                      binary32 1 or 2); with chunk boundaries off the 16-byte
+                      grid, rows of 31-32 vectors a warp takes at once
+                      (ReduceScatter 1..4, AllGather 1, 2 or 4).  A value
+                      outside these is RR_ERR_UNSUPPORTED. */
+  int beside_compute; /* 1: the call runs beside compute kernels on other
+                      streams; unless max_ctas is given, the grid is capped at
+                      RR_BESIDE_COMPUTE_SM_EIGHTHS eighths of the SMs (one CTA each),
+                      leaving the rest to the compute.  0: the whole GPU. */
 } rr_launch_cfg;
+
+/* Share of the SMs (numerator / 8) a call with beside_compute = 1 takes. */
+#define RR_BESIDE_COMPUTE_SM_EIGHTHS 5
 
 /*
  * ring_collective -- every collective through one entry point with an

@@ -109,6 +109,8 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
       return RR_ERR_INVALID_ARG;
     if (cfg->max_ctas < 0) return RR_ERR_INVALID_ARG;
     if (cfg->early_launch < 0 || cfg->early_launch > 2) return RR_ERR_INVALID_ARG;
+    if (cfg->vectors < 0 || cfg->vectors > 4) return RR_ERR_INVALID_ARG;
+    if (cfg->beside_compute < 0 || cfg->beside_compute > 1) return RR_ERR_INVALID_ARG;
   }
   ck->op = op;
   ck->R = R;
@@ -204,12 +206,18 @@ bool prefer_direct(int op, int R, int L, unsigned long long msg_bytes, int max_c
 // vectors need it) and every shared-memory size fits the device.
 rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int smem_per_sm, int smem_optin,
                       rr::RingParams *p, rr::Launch *l) {
-  const rr_launch_cfg zero = {0, 0, 0, 0, 0, 0, 0};
-  const rr_launch_cfg &c = cfg ? *cfg : zero;
+  const rr_launch_cfg zero = {};
+  rr_launch_cfg c = cfg ? *cfg : zero;
   const size_t E = ck.E;
   const unsigned long long N = ck.n;  // elements of this launch
-  auto capped = [&](int grid) { return (c.max_ctas > 0 && grid > c.max_ctas) ? c.max_ctas : grid; };
   if (sms < 1 || smem_per_sm < 1 || smem_optin < 1) return RR_ERR_INVALID_ARG;
+  // beside compute kernels: a share of the SMs, one CTA each (a tile pipeline
+  // per SM), unless the caller gave the cap itself
+  if (c.beside_compute && c.max_ctas == 0) {
+    c.max_ctas = (int)((long long)sms * RR_BESIDE_COMPUTE_SM_EIGHTHS / 8);
+    if (c.max_ctas < 1) c.max_ctas = 1;
+  }
+  auto capped = [&](int grid) { return (c.max_ctas > 0 && grid > c.max_ctas) ? c.max_ctas : grid; };
 
   p->count = N;
   p->first = ck.first;
@@ -255,20 +263,28 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   l->early_launch = c.early_launch == 0 ? kEarlyLaunchDefault : c.early_launch == 1;
   if (path == RR_PATH_DIRECT) {  // U 16-byte vectors per thread
     if (l->threads > 256) return RR_ERR_UNSUPPORTED;
-    // eight loads in flight per thread: few ranks per group take several vectors
-    // (two vectors for up to four ranks per group: for two ranks, four vectors a
-    // thread reached 0.61 of the copy bandwidth and two vectors at three CTAs
-    // per SM 0.78, at 256 MiB)
+    const bool wide = ck.dtype != RR_FP32 && ck.wire == RR_FP32;  // eight binary32 accumulators: 128 registers
+    const unsigned long long msg_bytes = (unsigned long long)ck.count * E;
+    // About eight loads in flight per thread: few ranks per group take several
+    // vectors (two vectors for up to four ranks per group: for two ranks, four
+    // vectors a thread reached 0.61 of the copy bandwidth and two vectors at
+    // three CTAs per SM 0.78, at 256 MiB).
     int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 4 ? 2 : 1);
-    // ReduceScatter stores one vector per R loads, so nearly all its traffic is
-    // loads and it wants more of them in flight: two vectors a thread (batches
-    // of four ranks) from 64 MiB per rank.  Measured at 256 MiB per rank,
-    // binary32, of the copy bandwidth: R = 5 0.79 -> 0.90, R = 8 0.95 -> 1.04,
-    // R = 9 0.87 -> 1.00, R = 16 0.99 -> 1.04 (results bit-identical); R = 9 at
-    // 4 MiB lost 3 %.
-    if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && (unsigned long long)ck.count * E >= (64ull << 20))
-      U = 2;
-    if (p->shifted) U = 1;  // the shifted kernel: one vector a thread
+    if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING) {
+      // ReduceScatter stores one vector per R loads, so nearly all its traffic
+      // is loads and it wants more of them in flight: two vectors a thread
+      // (batches of four ranks) from 64 MiB per rank.  Measured at 256 MiB per
+      // rank, binary32, of the copy bandwidth: R = 5 0.79 -> 0.90, R = 8 0.95
+      // -> 1.04, R = 9 0.87 -> 1.00, R = 16 0.99 -> 1.04 (results
+      // bit-identical); R = 9 at 4 MiB lost 3 %.  Three ranks take the whole
+      // group at three vectors: nine loads.
+      if (msg_bytes >= (64ull << 20)) U = 2;
+      if (ck.L == 3) U = 3;
+    }
+    if (p->shifted)  // rows a warp takes at once: about eight loads a lane
+      U = ck.op == RR_OP_REDUCE_SCATTER ? (ck.L == 2 ? 4 : ck.L == 3 ? 3 : 2) : (ck.L <= 2 ? 4 : ck.L <= 4 ? 2 : 1);
+    if (wide && U > 2) U = 2;
+    if (c.vectors) U = c.vectors;
     p->direct_u = U;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
     // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5
@@ -280,17 +296,45 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // did better from 64 MiB (R = 8, 256 MiB: 1.006 against 0.991); flat rings
     // of three or four ranks (two vectors a thread) do not.
     const unsigned long long vecs = n_bulk * E / 16;
-    const unsigned long long msg_bytes = (unsigned long long)ck.count * E;
     const int batch = U * ck.L;  // loads of one group a thread issues together
     const bool full_batch = (batch == 7 || batch == 8) && msg_bytes >= (64ull << 20) && !(U == 2 && ck.L == ck.R);
-    const bool wide = ck.dtype != RR_FP32 && ck.wire == RR_FP32;  // eight binary32 accumulators: 128 registers
     const bool looping = vecs > (unsigned long long)sms * 512ull * (unsigned long long)U * (ck.L >= 16 ? 2ull : 1ull);
-    l->direct_occ = (U <= 2 && ck.op != RR_OP_ALLGATHER && looping && !full_batch && !wide) ? 3 : 2;
+    l->direct_occ = (U <= 3 && ck.op != RR_OP_ALLGATHER && looping && !full_batch && !wide) ? 3 : 2;
     // Halving-doubling loads a whole tree (up to 16 vectors) per batch: a third
     // CTA helped only below seven ranks (R = 5: 0.85 -> 1.00 at 256 MiB; R = 12:
     // 1.01 -> 0.99).
     if (ck.algo == RR_ALGO_HALVING_DOUBLING)
       l->direct_occ = (ck.R < 7 && looping && !wide) ? 3 : 2;
+    if (U >= 3 && !p->shifted) l->direct_occ = 2;  // three or four vectors: 128 registers
+    if (p->shifted) l->direct_occ = rr::shift_occupancy(U);  // fixed per row count
+    // ctas_per_sm asks for a register budget (2 or 3 CTAs per SM).  It applies
+    // when a kernel of that budget exists for this plan; otherwise (1 or 4,
+    // tile-pipeline shapes, or a budget the kernel is not built for) it is
+    // ignored, unless the direct path was forced.
+    if (c.ctas_per_sm != 0) {
+      const int want = c.ctas_per_sm;
+      bool ok = want == 2 || want == 3;
+      if (ok) {
+        if (ck.algo == RR_ALGO_HALVING_DOUBLING)
+          ok = want == 2 || (!wide && ck.R < 8);
+        else if (p->shifted)
+          ok = want == rr::shift_occupancy(U);
+        else
+          ok = rr::direct_variant_exists(ck.op, wide, U, want);
+      }
+      if (ok)
+        l->direct_occ = want;
+      else if (c.path == RR_PATH_DIRECT)
+        return RR_ERR_UNSUPPORTED;
+    }
+    // only kernels that exist (a forced configuration may ask for others)
+    if (ck.algo == RR_ALGO_HALVING_DOUBLING) {
+      if (U != 1 || (l->direct_occ != 2 && !(l->direct_occ == 3 && !wide && ck.R < 8))) return RR_ERR_UNSUPPORTED;
+    } else if (p->shifted) {
+      if (!rr::shift_variant_exists(ck.op, wide, U)) return RR_ERR_UNSUPPORTED;
+    } else if (!rr::direct_variant_exists(ck.op, wide, U, l->direct_occ)) {
+      return RR_ERR_UNSUPPORTED;
+    }
     const unsigned long long blocks = (vecs + (unsigned long long)l->threads * U - 1) / ((unsigned long long)l->threads * U);
     unsigned long long cap = (unsigned long long)sms * (2048 / l->threads);
     // ReduceScatter, and ring AllReduce over groups of at most three ranks, do
@@ -431,14 +475,17 @@ rr_status plan(const Checked &ck, const void *const *in, void *const *out, const
   return plan_launch(ck, cfg, dev.sms, dev.smem_per_sm, dev.smem_optin, p, l);
 }
 
-void export_plan(const rr::RingParams &p, const rr::Launch &l, size_t E, rr_launch_cfg *chosen) {
+void export_plan(const rr::RingParams &p, const rr::Launch &l, size_t E, bool beside_compute,
+                 rr_launch_cfg *chosen) {
   chosen->path = l.path;
   chosen->tile_bytes = l.path == RR_PATH_BULK ? p.tile_elems * (int)E : 0;
   chosen->stages = l.path == RR_PATH_BULK ? p.stages : 0;
-  chosen->ctas_per_sm = l.ctas_per_sm;
+  chosen->ctas_per_sm = l.path == RR_PATH_DIRECT ? l.direct_occ : l.ctas_per_sm;
   chosen->threads = l.threads;
   chosen->max_ctas = l.grid;
   chosen->early_launch = l.early_launch ? 1 : 2;
+  chosen->vectors = l.path == RR_PATH_DIRECT ? p.direct_u : 0;
+  chosen->beside_compute = beside_compute ? 1 : 0;
 }
 
 // Plan and launch a validated collective on the current device.
@@ -643,7 +690,8 @@ rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs,
   Checked ck;
   rr_status st = check_args(op, in_bufs, out_bufs, R, count, dtype, wire, group_size, cfg, &ck);
   if (st != RR_OK) return st;
-  *chosen = rr_launch_cfg{RR_PATH_SIMPLE, 0, 0, 0, 0, 0};
+  *chosen = rr_launch_cfg{};
+  chosen->path = RR_PATH_SIMPLE;
   if (count == 0) return RR_OK;
   DeviceInfo dev;
   st = current_device(&dev);
@@ -652,7 +700,7 @@ rr_status ring_plan(rr_op op, const void *const *in_bufs, void *const *out_bufs,
   rr::Launch l;
   st = plan(ck, in_bufs, out_bufs, cfg, dev, &p, &l);
   if (st != RR_OK) return st;
-  export_plan(p, l, ck.E, chosen);
+  export_plan(p, l, ck.E, cfg && cfg->beside_compute, chosen);
   return RR_OK;
 }
 
@@ -669,7 +717,7 @@ rr_status ring_plan_device(rr_op op, int R, size_t count, rr_dtype dtype, rr_dty
   rr::Launch l;
   st = plan_launch(ck, cfg, sm_count, smem_per_sm, smem_per_block_optin, &p, &l);
   if (st != RR_OK) return st;
-  export_plan(p, l, ck.E, chosen);
+  export_plan(p, l, ck.E, cfg && cfg->beside_compute, chosen);
   *grid = l.grid;
   *smem_bytes = l.smem;
   return RR_OK;

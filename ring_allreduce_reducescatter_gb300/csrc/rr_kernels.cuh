@@ -526,24 +526,33 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
   using W = typename VT::W;
   constexpr int V = VT::V;
   constexpr int E = Fmt<DT>::bytes;
-  constexpr int NB = 8 / U;  // ranks per batch of loads
+  constexpr int NB = direct_batch_ranks(U);  // ranks per batch of loads
   const unsigned long long nvec = p.n_bulk / V;
   const unsigned long long T = (unsigned long long)(gridDim.x - p.straddle_cta) * blockDim.x;
   for (unsigned long long v0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < nvec; v0 += T * U) {
     if constexpr (OP == kOpAllGather) {
+      // all U loads first, then the stores: U loads in flight per thread
+      uint4 val[U];
+      bool live[U];
 #pragma unroll
       for (int k = 0; k < U; ++k) {
         const unsigned long long v = v0 + (unsigned long long)k * T;
-        if (v >= nvec) break;
-        const unsigned long long i0 = v * V, g0 = p.first + i0, boff = i0 * E;
+        live[k] = v < nvec;
+        if (!live[k]) continue;
+        const unsigned long long i0 = v * V, g0 = p.first + i0;
         const int c = chunk_of(g0, p.base, p.L);
-        if (c != chunk_of(g0 + V - 1, p.base, p.L)) {
+        if (c != chunk_of(g0 + V - 1, p.base, p.L)) {  // over a chunk boundary: element by element
           for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, i0 + e);
+          live[k] = false;
           continue;
         }
-        const uint4 val =
-            ldg_stream(static_cast<const unsigned char *>(p.in[c]) + (i0 - (unsigned long long)c * p.base) * E);
-        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, val);
+        val[k] = ldg_stream(static_cast<const unsigned char *>(p.in[c]) + (i0 - (unsigned long long)c * p.base) * E);
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        if (!live[k]) continue;
+        const unsigned long long boff = (v0 + (unsigned long long)k * T) * V * E;
+        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, val[k]);
       }
     } else {  // ring / naive fold, AllReduce or ReduceScatter
       unsigned long long boff[U];
@@ -619,10 +628,11 @@ __global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long li
 // builds the matching bytes of the other side from two aligned loads.
 // --------------------------------------------------------------------------
 
-// US: rows of output vectors a warp takes at once (ReduceScatter; 2 for up to
-// four ranks, so that a lane keeps eight loads in flight).
+// US: rows of output vectors a warp takes at once (ReduceScatter, and
+// AllGather over at most four ranks) or vectors a thread takes at once
+// (AllGather over more ranks); more rows keep more loads in flight.
 template <int OP, int DT, int WT, int US>
-__global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __grid_constant__ RingParams p) {
+__global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_kernel(const __grid_constant__ RingParams p) {
   grid_dependency_wait();
   grid_dependents_launch();
   using VT = Vec<DT, WT>;
@@ -640,7 +650,7 @@ __global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __gri
     // (a shuffle); lane 31 only supplies that block.  A vector whose upper
     // block would pass the end of the rank vectors goes element by element,
     // and so do the elements past a chunk's last full vector.
-    constexpr int NB = 8 / US;  // ranks per batch: 8 loads in flight a lane
+    constexpr int NB = direct_batch_ranks(US);  // ranks per batch: 8 (US = 3: 9) loads in flight a lane
     const unsigned lane = threadIdx.x & 31u;
     const unsigned long long warp = tid >> 5, n_warps = T >> 5;
     const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
@@ -719,17 +729,20 @@ __global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __gri
   } else if (L <= 4) {
     // AllGather with few ranks, where the loads weigh most: rows of 32 output
     // vectors aligned to 32 vectors (512-byte store segments), clipped to one
-    // chunk and numbered across the chunks; lane t loads the aligned source
-    // block under vector t's start, which is also the upper block lane t - 1
-    // needs (a shuffle), and lane 31 loads its upper block itself.  Vectors
-    // over a chunk boundary (at most one per boundary, taken by the first
-    // boundary inside it), vectors whose upper block would pass the end of the
-    // chunk's buffer and the ragged end go element by element.
+    // chunk; a warp's work item is US consecutive rows of one chunk, items
+    // numbered across the chunks.  Lane t loads the aligned source block under
+    // vector t's start, which is also the upper block lane t - 1 needs (a
+    // shuffle), and lane 31 loads its upper block itself; every row's loads
+    // are issued before any store.  Vectors over a chunk boundary (at most one
+    // per boundary, taken by the first boundary inside it), vectors whose
+    // upper block would pass the end of the chunk's buffer and the ragged end
+    // go element by element.
     const unsigned lane = threadIdx.x & 31u;
     const unsigned long long warp = tid >> 5, n_warps = T >> 5;
     const unsigned long long nvec = p.n_bulk / V;  // output vectors wholly before the ragged end
     const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
-    const unsigned long long ipc = (base / V + 64) / 32, ipl = (len_last / V + 64) / 32;  // rows per chunk, at most
+    const unsigned long long rpc = (base / V + 64) / 32, rpl = (len_last / V + 64) / 32;  // rows per chunk, at most
+    const unsigned long long ipc = (rpc + US - 1) / US, ipl = (rpl + US - 1) / US;        // items per chunk
     const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
     for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
       int c;
@@ -745,22 +758,36 @@ __global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __gri
       const unsigned long long vf = (cb + V - 1) / V;  // first output vector wholly in the chunk
       const unsigned long long ve = (cb + len) / V < nvec ? (cb + len) / V : nvec;  // one past the last
       const int sh = (int)((vf * V - cb) % V) * E;     // where a vector's source starts in its aligned block
-      const unsigned long long v = (vf / 32 + item) * 32 + lane;
-      const bool act = v >= vf && v < ve;
-      // the aligned source block under vector v's start (o - oa = sh / E for every v of the chunk)
-      const unsigned long long o = v * V - cb, oa = o - (o % V);
-      const bool load = v >= vf && v <= ve && oa + V <= len;
-      const bool tail = act && sh != 0 && oa + 2 * V > len;
       const unsigned char *src = static_cast<const unsigned char *>(p.in[c]);
-      const uint4 blk = load ? ldg_stream(src + oa * E) : make_uint4(0u, 0u, 0u, 0u);
-      uint4 next = make_uint4(__shfl_down_sync(0xffffffffu, blk.x, 1), __shfl_down_sync(0xffffffffu, blk.y, 1),
-                              __shfl_down_sync(0xffffffffu, blk.z, 1), __shfl_down_sync(0xffffffffu, blk.w, 1));
-      if (lane == 31u && act && sh != 0 && !tail) next = ldg_stream(src + (oa + V) * E);
-      if (tail) {
-        for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
-      } else if (act) {
-        const uint4 x = sh ? funnel16(blk, next, sh) : blk;
-        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + v * V * E, x);
+      uint4 blk[US], nxt[US];
+      bool act[US], tail[US];
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const unsigned long long v = (vf / 32 + item * US + k) * 32 + lane;
+        act[k] = v >= vf && v < ve;
+        // the aligned source block under vector v's start (o - oa = sh / E for every v of the chunk)
+        const unsigned long long o = v * V - cb, oa = o - (o % V);
+        const bool load = v >= vf && v <= ve && oa + V <= len;
+        tail[k] = act[k] && sh != 0 && oa + 2 * V > len;
+        blk[k] = load ? ldg_stream(src + oa * E) : make_uint4(0u, 0u, 0u, 0u);
+        nxt[k] = (lane == 31u && act[k] && sh != 0 && !tail[k]) ? ldg_stream(src + (oa + V) * E)
+                                                               : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, blk[k].x, 1), __shfl_down_sync(0xffffffffu, blk[k].y, 1),
+                                    __shfl_down_sync(0xffffffffu, blk[k].z, 1), __shfl_down_sync(0xffffffffu, blk[k].w, 1));
+        if (lane != 31u) nxt[k] = up;
+      }
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const unsigned long long v = (vf / 32 + item * US + k) * 32 + lane;
+        if (tail[k]) {
+          for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
+        } else if (act[k]) {
+          const uint4 x = sh ? funnel16(blk[k], nxt[k], sh) : blk[k];
+          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + v * V * E, x);
+        }
       }
     }
     for (unsigned long long b = 1 + tid; b < (unsigned long long)L; b += T) {  // vectors over a boundary
@@ -770,22 +797,41 @@ __global__ void __launch_bounds__(kDirectThreads, 3) rr_shift_kernel(const __gri
       for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, vb * V + e);
     }
     for (unsigned long long i = p.n_bulk + tid; i < p.count; i += T) element_op<OP, DT, WT>(p, i);
-  } else {  // AllGather: each thread an output vector, two aligned loads of its source block pair
+  } else {
+    // AllGather: each thread takes US output vectors a grid-stride apart and
+    // builds each from the two aligned blocks of its chunk's input under it
+    // (the second served by L1); all loads before the stores
     const unsigned long long nvec = p.n_bulk / V;
-    for (unsigned long long v = tid; v < nvec; v += T) {
-      const unsigned long long gs = v * V;
-      const int c = chunk_of(gs, base, L);
-      const unsigned long long o = gs - (unsigned long long)c * base;  // offset in chunk c's buffer
-      const unsigned long long oa = o / V * V, len = chunk_end(c, base, L, N) - (unsigned long long)c * base;
-      const int sh = (int)(o - oa) * E;
-      if (c != chunk_of(gs + V - 1, base, L) || (sh != 0 && oa + 2 * V > len)) {
-        for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, gs + e);
-        continue;
+    for (unsigned long long v0 = tid; v0 < nvec; v0 += T * US) {
+      uint4 lo[US], hi[US];
+      int sh[US];
+      bool live[US];
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const unsigned long long v = v0 + (unsigned long long)k * T;
+        live[k] = v < nvec;
+        if (!live[k]) continue;
+        const unsigned long long gs = v * V;
+        const int c = chunk_of(gs, base, L);
+        const unsigned long long o = gs - (unsigned long long)c * base;  // offset in chunk c's buffer
+        const unsigned long long oa = o / V * V, len = chunk_end(c, base, L, N) - (unsigned long long)c * base;
+        sh[k] = (int)(o - oa) * E;
+        if (c != chunk_of(gs + V - 1, base, L) || (sh[k] != 0 && oa + 2 * V > len)) {
+          for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, gs + e);
+          live[k] = false;
+          continue;
+        }
+        const unsigned char *src = static_cast<const unsigned char *>(p.in[c]) + oa * E;
+        lo[k] = ldg_l1(src);
+        hi[k] = sh[k] ? ldg_l1(src + 16) : lo[k];
       }
-      const unsigned char *src = static_cast<const unsigned char *>(p.in[c]) + oa * E;
-      const uint4 lo = ldg_l1(src);
-      const uint4 x = sh ? funnel16(lo, ldg_l1(src + 16), sh) : lo;
-      for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + gs * E, x);
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        if (!live[k]) continue;
+        const uint4 x = sh[k] ? funnel16(lo[k], hi[k], sh[k]) : lo[k];
+        const unsigned long long gs = (v0 + (unsigned long long)k * T) * V;
+        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + gs * E, x);
+      }
     }
     for (unsigned long long i = p.n_bulk + tid; i < p.count; i += T) element_op<OP, DT, WT>(p, i);
   }
@@ -812,6 +858,51 @@ inline cudaError_t launch_kernel(void (*k)(RingParams), const Launch &l, size_t 
   return cudaLaunchKernelEx(&c, k, p);
 }
 
+// The direct kernel of the plan's (U, OCC); the planner picks only variants
+// for which direct_variant_exists holds.
+template <int OP, int DT, int WT>
+cudaError_t launch_direct(const RingParams &p, const Launch &l, cudaStream_t s) {
+  constexpr bool wide = DT != kF32 && WT == kF32;
+  const int U = p.direct_u, occ = l.direct_occ;
+  if constexpr (OP == kOpAllGather) {
+    switch (U) {
+      case 1: return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
+      case 2: return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
+      case 4: return launch_kernel(rr_direct_kernel<OP, DT, WT, 4, 2>, l, 0, s, p);
+    }
+  } else if constexpr (wide) {
+    if (U == 1) return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
+    if (U == 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
+  } else {
+    switch (U * 8 + occ) {
+      case 1 * 8 + 2: return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
+      case 1 * 8 + 3: return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 3>, l, 0, s, p);
+      case 2 * 8 + 2: return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
+      case 2 * 8 + 3: return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 3>, l, 0, s, p);
+      case 3 * 8 + 2: return launch_kernel(rr_direct_kernel<OP, DT, WT, 3, 2>, l, 0, s, p);
+      case 4 * 8 + 2: return launch_kernel(rr_direct_kernel<OP, DT, WT, 4, 2>, l, 0, s, p);
+    }
+  }
+  return cudaErrorInvalidConfiguration;  // not a variant the planner picks
+}
+
+// The shifted kernel of the plan's rows per work item (shift_variant_exists).
+template <int OP, int DT, int WT>
+cudaError_t launch_shift(const RingParams &p, const Launch &l, cudaStream_t s) {
+  constexpr bool wide = DT != kF32 && WT == kF32;
+  switch (p.direct_u) {
+    case 1: return launch_kernel(rr_shift_kernel<OP, DT, WT, 1>, l, 0, s, p);
+    case 2: return launch_kernel(rr_shift_kernel<OP, DT, WT, 2>, l, 0, s, p);
+    case 3:
+      if constexpr (OP == kOpReduceScatter && !wide) return launch_kernel(rr_shift_kernel<OP, DT, WT, 3>, l, 0, s, p);
+      break;
+    case 4:
+      if constexpr (!wide) return launch_kernel(rr_shift_kernel<OP, DT, WT, 4>, l, 0, s, p);
+      break;
+  }
+  return cudaErrorInvalidConfiguration;  // not a variant the planner picks
+}
+
 template <int OP, int DT, int WT, bool HD>
 cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s) {
   if (l.path == RR_PATH_BULK) {
@@ -836,28 +927,11 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
   } else if (l.path == RR_PATH_DIRECT) {
     if constexpr (HD) {
       return launch_hd_direct(DT, WT, p, l, s);
-    } else if constexpr (OP != kOpAllReduce) {
-      if (p.shifted) {
-        if constexpr (OP == kOpReduceScatter) {
-          if (p.L <= 4) return launch_kernel(rr_shift_kernel<OP, DT, WT, 2>, l, 0, s, p);
-        }
-        return launch_kernel(rr_shift_kernel<OP, DT, WT, 1>, l, 0, s, p);
+    } else {
+      if constexpr (OP != kOpAllReduce) {
+        if (p.shifted) return launch_shift<OP, DT, WT>(p, l, s);
       }
-    }
-    if constexpr (!HD) {
-      // vectors per thread: 1 for AllGather, 1 or 2 otherwise
-      constexpr bool multi = OP != kOpAllGather;
-      constexpr bool wide = DT != kF32 && WT == kF32;
-      if constexpr (multi && !wide) {
-        if (p.direct_u >= 2)
-          return l.direct_occ == 3 ? launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 3>, l, 0, s, p)
-                                   : launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
-        if (l.direct_occ == 3) return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 3>, l, 0, s, p);
-      }
-      if constexpr (multi) {
-        if (p.direct_u >= 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
-      }
-      return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
+      return launch_direct<OP, DT, WT>(p, l, s);
     }
   }
   return launch_kernel(rr_simple_kernel<OP, DT, WT, HD>, l, 0, s, p);

@@ -38,13 +38,40 @@ struct RingParams {
   int stages;                     // bulk path: pipeline depth
   int store_lag;                  // bulk path: store groups left in flight before a stage is refilled (1..8)
   int slots;                      // bulk path: tiles of one stage (R, or 1 for AllGather)
-  int direct_u;                   // direct path: vectors per thread and iteration (1 or 2)
+  int direct_u;                   // direct path: vectors per thread and iteration (1..4); shifted kernel: rows per warp item
   int algo;                       // AllReduce summation order: kAlgo*
   int hd_log2p;                   // halving-doubling: log2 of P, the largest power of two <= R
   int hd_extra;                   // halving-doubling: R - P ranks folded in pairs first
   int straddle_cta;               // direct AllReduce: 1 if the grid's last CTA folds the vectors over chunk boundaries
   int shifted;                    // direct ReduceScatter / AllGather: chunk boundaries off the 16-byte grid
 };
+
+// Loads a direct-path thread issues together for one group: U vectors of NB
+// ranks each.  Eight whatever U is (nine for U = 3, a three-rank group whole).
+__host__ __device__ constexpr int direct_batch_ranks(int U) { return U == 3 ? 3 : 8 / U; }
+
+// The direct-path kernels that exist: (collective, wide accumulators, U
+// vectors a thread, OCC 256-thread CTAs per SM the registers are budgeted
+// for).  Ring / naive AllReduce and ReduceScatter: U = 1, 2 at OCC 2 or 3,
+// U = 3, 4 at OCC 2 (at 85 registers a thread they spill); with binary32
+// accumulators of 16-bit storage ("wide", eight floats a vector): U = 1, 2 at
+// OCC 2; AllGather: U = 1, 2, 4 at OCC 2.  The planner picks only these and
+// rejects a forced launch configuration outside them.
+__host__ __device__ constexpr bool direct_variant_exists(int op, bool wide, int U, int occ) {
+  return op == kOpAllGather ? ((U == 1 || U == 2 || U == 4) && occ == 2)
+         : wide             ? ((U == 1 || U == 2) && occ == 2)
+                            : (((U == 1 || U == 2) && (occ == 2 || occ == 3)) || ((U == 3 || U == 4) && occ == 2));
+}
+
+// The shifted ReduceScatter / AllGather kernels (chunk boundaries off the
+// 16-byte grid): US rows of output vectors per warp work item.
+// ReduceScatter: US = 1..4 (wide: 1, 2); AllGather: US = 1, 2, 4.
+__host__ __device__ constexpr bool shift_variant_exists(int op, bool wide, int US) {
+  return op == kOpAllGather ? (US == 1 || US == 2 || US == 4) : wide ? (US == 1 || US == 2) : (US >= 1 && US <= 4);
+}
+
+// 256-thread CTAs per SM the shifted kernel of US rows is compiled for.
+__host__ __device__ constexpr int shift_occupancy(int US) { return US >= 3 ? 2 : 3; }
 
 // One launch, fully resolved by the planner.
 struct Launch {

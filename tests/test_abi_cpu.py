@@ -60,7 +60,7 @@ def test_header_is_c_and_links_from_c(L, tmp_path):
                     f"-Wl,-rpath,{libdir}"], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
     lines = dict(l.split(" ", 1) for l in out if l)
-    assert lines["abi"] == "2"
+    assert lines["abi"] == "3"
     assert out[1:5] == ["chunk 0 2 0", "chunk 1 2 2", "chunk 2 2 4", "chunk 3 4 6"]
     assert lines["bad_rank_count"] == str(EINVAL) and lines["bad_dtype"] == str(EINVAL)
     assert lines["unsupported_pair"] == str(EUNSUP) and lines["alias"] == str(EALIAS)
@@ -89,7 +89,7 @@ def test_last_cuda_error_is_recorded(L):
 
 
 def test_abi_version(L):
-    assert L.ring_abi_version() == 2
+    assert L.ring_abi_version() == 3
 
 
 def test_status_strings(L):
@@ -533,3 +533,68 @@ def test_binding_checks_host_buffer_sizes(L):
             rr.allreduce_host_static(ins, outs)
         with pytest.raises(ValueError, match=re.escape(msg)):
             rr.allreduce_host(ins, host_outs=outs, workspace=torch.empty(16, dtype=torch.uint8))
+
+
+def test_forced_vectors_and_register_budget(L):
+    """`vectors` and, on the direct path, `ctas_per_sm` select a kernel; only
+    kernels the library builds are accepted, and the plan reports the choice."""
+    D = 3  # RR_PATH_DIRECT
+    N = 1 << 24
+    built = {AR: {(1, 2), (1, 3), (2, 2), (2, 3), (3, 2), (4, 2)}, RS: {(1, 2), (1, 3), (2, 2), (2, 3), (3, 2), (4, 2)},
+             AG: {(1, 2), (2, 2), (4, 2)}}
+    for op, ok in built.items():
+        for u in (1, 2, 3, 4):
+            for occ in (2, 3):
+                st, ch, grid, _ = plan_dev(L, op, 8, N, F32, cfg=(D, 0, 0, occ, 0, 0, 0, u))
+                if (u, occ) in ok:
+                    assert st == OK and ch["vectors"] == u and ch["ctas_per_sm"] == occ, (op, u, occ, ch)
+                else:
+                    assert st == EUNSUP, (op, u, occ, st)
+    # binary32 accumulation of 16-bit storage: one or two vectors, two CTAs per SM
+    for u, occ, want in ((1, 2, OK), (2, 2, OK), (2, 3, EUNSUP), (3, 2, EUNSUP)):
+        assert plan_dev(L, AR, 8, N, F16, wire=F32, cfg=(D, 0, 0, occ, 0, 0, 0, u))[0] == want
+    # shifted kernels (chunk boundaries off the 16-byte grid): rows per warp,
+    # their register budget fixed by the row count
+    Ns = 4 * (8 * 1000 + 1)
+    for op, rows in ((RS, (1, 2, 3, 4)), (AG, (1, 2, 4))):
+        for u in (1, 2, 3, 4):
+            st, ch, _, _ = plan_dev(L, op, 4, Ns, F16, cfg=(D, 0, 0, 0, 0, 0, 0, u))
+            if u in rows:
+                assert st == OK and ch["vectors"] == u and ch["ctas_per_sm"] == (2 if u >= 3 else 3)
+            else:
+                assert st == EUNSUP
+    assert plan_dev(L, RS, 4, Ns, F16, cfg=(D, 0, 0, 2, 0, 0, 0, 1))[0] == EUNSUP  # one row: three CTAs only
+    assert plan_dev(L, RS, 4, Ns, F16, cfg=(0, 0, 0, 2, 0, 0, 0, 1))[0] == OK      # ignored on the automatic path
+    # out-of-range values are argument errors
+    assert plan_dev(L, AR, 8, N, F32, cfg=(0, 0, 0, 0, 0, 0, 0, 5))[0] == EINVAL
+    assert plan_dev(L, AR, 8, N, F32, cfg=(0, 0, 0, 0, 0, 0, 0, -1))[0] == EINVAL
+    assert plan_dev(L, AR, 8, N, F32, cfg=(0, 0, 0, 0, 0, 0, 0, 0, 2))[0] == EINVAL
+
+
+def test_planner_vectors_for_few_ranks(L):
+    """Few ranks take several vectors (rows) a thread so that about eight loads
+    are in flight: ReduceScatter over three ranks takes the whole group at three
+    vectors; the shifted ReduceScatter takes 4 / 3 / 2 rows for 2 / 3 / 4+
+    ranks, the shifted AllGather 4 / 2 / 1 rows for 2 / 3-4 / 5+ ranks."""
+    st, ch, _, _ = plan_dev(L, RS, 3, 3 * (1 << 22), F32)
+    assert st == OK and ch["path"] == 3 and ch["vectors"] == 3 and ch["ctas_per_sm"] == 2
+    for R, rows in ((2, 4), (3, 3), (4, 2), (8, 2), (16, 2)):
+        st, ch, _, _ = plan_dev(L, RS, R, R * (8 * 100_000 + 3), F16)
+        assert st == OK and ch["path"] == 3 and ch["vectors"] == rows, (R, ch)
+    for R, rows in ((2, 4), (3, 2), (4, 2), (5, 1), (8, 1)):
+        st, ch, _, _ = plan_dev(L, AG, R, R * (8 * 100_000 + 3), F16)
+        assert st == OK and ch["path"] == 3 and ch["vectors"] == rows, (R, ch)
+
+
+def test_beside_compute_caps_the_grid(L):
+    """beside_compute: the grid takes RR_BESIDE_COMPUTE_SM_EIGHTHS eighths of
+    the SMs, one tile pipeline each; an explicit max_ctas still wins."""
+    with open(HEADER) as f:
+        eighths = int(re.search(r"#define RR_BESIDE_COMPUTE_SM_EIGHTHS (\d+)", f.read()).group(1))
+    want = GB300["sms"] * eighths // 8
+    st, ch, grid, smem = plan_dev(L, AR, 8, 1 << 26, F16, cfg=(0, 0, 0, 0, 0, 0, 0, 0, 1))
+    assert st == OK and grid == want and ch["path"] == 1 and ch["ctas_per_sm"] == 1 and ch["beside_compute"] == 1
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 26, F16, cfg=(0, 0, 0, 0, 0, 40, 0, 0, 1))
+    assert st == OK and grid == 40
+    st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 26, F16)
+    assert st == OK and ch["beside_compute"] == 0 and grid == GB300["sms"] * 16

@@ -886,3 +886,85 @@ def test_capped_grids(rr):
             check_ar(rr, xs, cfg=rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 256, cap), what=f"direct R={R} cap={cap}")
             check_rs(rr, xs[:R], cfg=rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 64, cap), what=f"direct RS R={R} cap={cap}") \
                 if (300_007 // R * 2) % 16 == 0 else None
+
+
+# --------------------------------------------------------------------------
+# every direct-path kernel variant, forced through the launch configuration
+# --------------------------------------------------------------------------
+
+def direct_variants(op, wide, shifted):
+    """(vectors, register budget) of every direct-path kernel the library
+    builds for this collective (0 = the budget the planner gives it)."""
+    if shifted:
+        rows = (1, 2, 4) if op == "ag" else ((1, 2) if wide else (1, 2, 3, 4))
+        return [(u, 0) for u in rows]
+    if op == "ag":
+        return [(1, 2), (2, 2), (4, 2)]
+    if wide:
+        return [(1, 2), (2, 2)]
+    return [(1, 2), (1, 3), (2, 2), (2, 3), (3, 2), (4, 2)]
+
+
+@pytest.mark.parametrize("dtype,wire", PAIRS, ids=lambda v: str(v))
+def test_every_direct_variant(rr, dtype, wire):
+    """Each direct-path kernel (1-4 vectors a thread, both register budgets;
+    the shifted kernels at 1-4 rows a warp) on chunk boundaries on and off the
+    16-byte grid with a ragged last chunk, on the planner's grid and on a grid
+    of five CTAs whose threads loop many times; bit for bit against the oracle."""
+    E = torch.tensor([], dtype=dtype).element_size()
+    V = 16 // E
+    wide = dtype != torch.float32 and wire == "f32"
+    for R in (2, 3, 4, 5, 9):
+        for off_grid in (False, True):
+            base = V * 4001 + (1 if off_grid else 0)
+            N = R * base + (R - 1)
+            xs = gen(R, N, dtype, 1009 * R + base)
+            hx = [host(x) for x in xs]
+            ref_ar = oracle.allreduce(hx, NAME[dtype], wire)
+            ref_rs = oracle.reduce_scatter(hx, NAME[dtype], wire)
+            lens = [oracle.chunk_len(N, R, c) for c in range(R)]
+            chunks = gen(R, 0, dtype, 2003 * R + base, lengths=lens)
+            ref_ag = oracle.allgather([host(c) for c in chunks], N, NAME[dtype]) if wire is None else None
+            for cap in (0, 5):
+                for u, occ in direct_variants("ar", wide, False):
+                    cfg = rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, occ, 0, cap, 0, u)
+                    outs = run_ar(rr, xs, wire, cfg=cfg)
+                    torch.cuda.synchronize()
+                    for r in range(R):
+                        assert_same(host(outs[r]), ref_ar.outs[r], f"AR U={u} occ={occ} cap={cap} R={R} "
+                                                                   f"off_grid={off_grid} rank {r}")
+                for u, occ in direct_variants("rs", wide, off_grid):
+                    cfg = rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, occ, 0, cap, 0, u)
+                    parts = [torch.full((lens[c],), float("nan"), dtype=dtype, device="cuda") for c in range(R)]
+                    rr.collective(rr.OP_REDUCE_SCATTER, xs, parts, N, wire, 0, None, cfg)
+                    torch.cuda.synchronize()
+                    for c in range(R):
+                        assert_same(host(parts[c]), ref_rs.outs[c], f"RS U={u} occ={occ} cap={cap} R={R} "
+                                                                    f"off_grid={off_grid} chunk {c}")
+                if ref_ag is None:
+                    continue
+                for u, occ in direct_variants("ag", False, off_grid):
+                    cfg = rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, occ, 0, cap, 0, u)
+                    outs = [torch.full((N,), float("nan"), dtype=dtype, device="cuda") for _ in range(R)]
+                    rr.collective(rr.OP_ALLGATHER, chunks, outs, N, None, 0, None, cfg)
+                    torch.cuda.synchronize()
+                    for r in range(R):
+                        assert_same(host(outs[r]), ref_ag.outs[r], f"AG U={u} occ={occ} cap={cap} R={R} "
+                                                                   f"off_grid={off_grid} rank {r}")
+    assert rr.device_status() == 0
+
+
+def test_launch_config_rejects_kernels_not_built(rr):
+    """A forced direct path asking for a kernel the library does not build is
+    RR_ERR_UNSUPPORTED, before anything is launched."""
+    xs = gen(4, 4 * 8192, torch.float32, 3)
+    outs = [torch.empty_like(x) for x in xs]
+    for u, occ in ((3, 3), (4, 3)):
+        with pytest.raises(rr.RingError) as e:
+            rr.collective(rr.OP_ALLREDUCE, xs, outs, xs[0].numel(), None, 0, None,
+                          rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, occ, 0, 0, 0, u))
+        assert e.value.status == rr.ERR_UNSUPPORTED
+    with pytest.raises(rr.RingError) as e:  # AllGather: no three-vector kernel
+        rr.collective(rr.OP_ALLGATHER, [x[:8192] for x in xs], outs, xs[0].numel(), None, 0, None,
+                      rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, 0, 0, 3))
+    assert e.value.status == rr.ERR_UNSUPPORTED
