@@ -739,11 +739,15 @@ def run_ours(args):
 SWEEP_OPS = {"ar": 0, "rs": 1, "ag": 2}
 
 
-def sweep_variants(rr, op, wide, shifted, all_variants):
+def sweep_variants(rr, op, wide, shifted, all_variants, prefetch=False):
     """(label, cfg) pairs to time at one point: the planner's choice, the tile
-    pipeline and the direct path (each forced), and with all_variants every
-    direct kernel the library builds (vectors a thread x register budget)."""
+    pipeline and the direct path (each forced); with prefetch the direct path
+    under each L2-prefetch mode; with all_variants every direct kernel the
+    library builds (vectors a thread x register budget)."""
     out = [("auto", None), ("bulk", rr.LaunchCfg(rr.PATH_BULK)), ("direct", rr.LaunchCfg(rr.PATH_DIRECT))]
+    if prefetch and not shifted:
+        for pf, name in ((1, "none"), (2, "head"), (3, "ahead"), (4, "head+ahead")):
+            out.append((f"direct prefetch={name}", rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, 0, 0, 0, 0, pf)))
     if all_variants:
         if shifted:
             rows = (1, 2, 4) if op == 2 else ((1, 2) if wide else (1, 2, 3, 4))
@@ -759,7 +763,7 @@ def sweep_variants(rr, op, wide, shifted, all_variants):
     return out
 
 
-def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid, all_variants):
+def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid, all_variants, prefetch=False):
     """Time every variant of one (collective, ranks, size) point.  Chunks are
     whole multiples of the 16-byte vector (or, off_grid, one element more, so
     chunk boundaries fall off the 16-byte grid).  Returns JSON rows."""
@@ -787,7 +791,7 @@ def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid
     wide = dtype != torch.float32 and wire == "f32"
     shifted = off_grid and op != 0
     rows = []
-    for label, cfg in sweep_variants(rr, op, wide, shifted, all_variants):
+    for label, cfg in sweep_variants(rr, op, wide, shifted, all_variants, prefetch):
         try:
             plan = rr.plan(op, sets[0][0], sets[0][1], N, wire, 0, cfg)
         except rr.RingError:
@@ -802,7 +806,7 @@ def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid
         rows.append({"op": {0: "allreduce", 1: "reduce_scatter", 2: "allgather"}[op], "R": R_, "count": N,
                      "msg_bytes": msg, "off_grid": off_grid, "variant": label,
                      "path": {1: "bulk", 2: "simple", 3: "direct"}[plan["path"]], "vectors": plan["vectors"],
-                     "ctas_per_sm": plan["ctas_per_sm"], "grid": plan["max_ctas"],
+                     "ctas_per_sm": plan["ctas_per_sm"], "prefetch": plan["prefetch"], "grid": plan["max_ctas"],
                      "us": round(med * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
                      "frac": round(alg / (med * 1e-3) / 1e9 / peak, 4), "replays": REPLAYS, "launches": launches})
     del sets
@@ -836,7 +840,7 @@ def run_path_sweep(args):
                     if off_grid and op == 0:
                         continue
                     for row in path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid,
-                                                args.sweep_variants):
+                                                args.sweep_variants, args.sweep_prefetch):
                         print(json.dumps(row), flush=True)
 
 
@@ -904,6 +908,7 @@ def main():
     ap.add_argument("--sweep-off-grid", default="no", choices=["no", "only", "both"],
                     help="chunk boundaries off the 16-byte grid (ReduceScatter / AllGather)")
     ap.add_argument("--sweep-variants", action="store_true", help="every direct kernel variant too")
+    ap.add_argument("--sweep-prefetch", action="store_true", help="the direct path under each L2-prefetch mode too")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.gpus < 1:

@@ -78,7 +78,8 @@ class LaunchCfg(ctypes.Structure):
 
     _fields_ = [("path", ctypes.c_int), ("tile_bytes", ctypes.c_int), ("stages", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("threads", ctypes.c_int), ("max_ctas", ctypes.c_int),
-                ("early_launch", ctypes.c_int), ("vectors", ctypes.c_int), ("beside_compute", ctypes.c_int)]
+                ("early_launch", ctypes.c_int), ("vectors", ctypes.c_int), ("beside_compute", ctypes.c_int),
+                ("prefetch", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -111,6 +111,7 @@ rr_status check_scalars(int op, int R, size_t count, int dtype, int wire, int gr
     if (cfg->early_launch < 0 || cfg->early_launch > 2) return RR_ERR_INVALID_ARG;
     if (cfg->vectors < 0 || cfg->vectors > 4) return RR_ERR_INVALID_ARG;
     if (cfg->beside_compute < 0 || cfg->beside_compute > 1) return RR_ERR_INVALID_ARG;
+    if (cfg->prefetch < 0 || cfg->prefetch > 4) return RR_ERR_INVALID_ARG;
   }
   ck->op = op;
   ck->R = R;
@@ -270,22 +271,37 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // vectors a thread reached 0.61 of the copy bandwidth and two vectors at
     // three CTAs per SM 0.78, at 256 MiB).
     int U = (ck.op == RR_OP_ALLGATHER || ck.algo == RR_ALGO_HALVING_DOUBLING) ? 1 : (ck.L <= 4 ? 2 : 1);
-    if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING) {
-      // ReduceScatter stores one vector per R loads, so nearly all its traffic
-      // is loads and it wants more of them in flight: two vectors a thread
-      // (batches of four ranks) from 64 MiB per rank.  Measured at 256 MiB per
-      // rank, binary32, of the copy bandwidth: R = 5 0.79 -> 0.90, R = 8 0.95
-      // -> 1.04, R = 9 0.87 -> 1.00, R = 16 0.99 -> 1.04 (results
-      // bit-identical); R = 9 at 4 MiB lost 3 %.  Three ranks take the whole
-      // group at three vectors: nine loads.
-      if (msg_bytes >= (64ull << 20)) U = 2;
-      if (ck.L == 3) U = 3;
+    // ReduceScatter stores one vector per R loads, so nearly all its traffic
+    // is loads and it wants more of them in flight: two vectors a thread
+    // (batches of four ranks) from 64 MiB per rank.  Measured at 256 MiB per
+    // rank, binary32, of the copy bandwidth: R = 5 0.79 -> 0.90, R = 8 0.95 ->
+    // 1.04, R = 9 0.87 -> 1.00, R = 16 0.99 -> 1.04 (results bit-identical);
+    // R = 9 at 4 MiB lost 3 %.  (Three ranks at three vectors, nine loads but
+    // two CTAs per SM: 0.60 against 0.875 at 256 MiB, binary16.)
+    if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && msg_bytes >= (64ull << 20)) U = 2;
+    // AllGather over two ranks: two vectors a thread, both loads before the
+    // four stores (256 MiB binary16: 0.83 -> 0.94; 16 MiB: 0.70 -> 0.73)
+    if (ck.op == RR_OP_ALLGATHER && ck.R == 2) U = 2;
+    if (p->shifted) {
+      // rows a warp takes at once.  Measured, binary16, of the copy bandwidth
+      // at 16 / 256 MiB per rank: ReduceScatter R = 2 four rows 0.56 / 0.81
+      // (two: 0.55 / 0.72); R = 3 two rows 0.62 / 0.79, three 0.58 / 0.81;
+      // R = 4 two rows 0.68 / 0.83; R = 8 two rows 0.81 / 0.84, one 0.77 /
+      // 0.85.  AllGather R = 2 two rows 0.68 / 0.82, four 0.63 / 0.83; R = 3
+      // two rows 0.79 / 0.92; R = 4 two rows 0.84 / 0.94; R = 8 two vectors
+      // a thread 0.83 / 0.93, one 0.84 / 0.86.
+      if (ck.op == RR_OP_REDUCE_SCATTER)
+        U = ck.L == 2 ? 4 : (ck.L == 3 && msg_bytes >= (64ull << 20)) ? 3 : 2;
+      else
+        U = 2;
     }
-    if (p->shifted)  // rows a warp takes at once: about eight loads a lane
-      U = ck.op == RR_OP_REDUCE_SCATTER ? (ck.L == 2 ? 4 : ck.L == 3 ? 3 : 2) : (ck.L <= 2 ? 4 : ck.L <= 4 ? 2 : 1);
     if (wide && U > 2) U = 2;
     if (c.vectors) U = c.vectors;
     p->direct_u = U;
+    // L2 prefetch (kPrefetch* bits): none by default; only the ring / naive
+    // kernels on 16-byte chunk boundaries prefetch
+    p->prefetch = c.prefetch ? c.prefetch - 1 : 0;
+    if (p->shifted || ck.algo == RR_ALGO_HALVING_DOUBLING) p->prefetch = 0;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
     // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5
     // 0.88 -> 0.98, R = 9 0.93 -> 0.99, R = 3 0.85 -> 0.96).  A grid that
@@ -485,6 +501,7 @@ void export_plan(const rr::RingParams &p, const rr::Launch &l, size_t E, bool be
   chosen->max_ctas = l.grid;
   chosen->early_launch = l.early_launch ? 1 : 2;
   chosen->vectors = l.path == RR_PATH_DIRECT ? p.direct_u : 0;
+  chosen->prefetch = l.path == RR_PATH_DIRECT ? p.prefetch + 1 : 0;
   chosen->beside_compute = beside_compute ? 1 : 0;
 }
 

@@ -292,6 +292,9 @@ __device__ __forceinline__ uint4 funnel16(uint4 lo, uint4 hi, int sh) {
                     __funnelshift_r(a3, a4, b));
 }
 
+// Brings the line holding p into L2 (a hint: no data reaches the SM).
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 __device__ __forceinline__ void stg_stream(void *p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");

@@ -510,18 +510,28 @@ __device__ __forceinline__ void straddle_pass(const RingParams &p) {
 
 // OCC: 256-thread CTAs per SM the registers are budgeted for (2: up to 128
 // registers a thread, 3: up to 85).
-template <int OP, int DT, int WT, int U, int OCC>
-__global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __grid_constant__ RingParams p) {
-  // The next kernel may be scheduled at once: a large grid fills the SMs'
-  // registers or thread slots, so its CTAs take SMs only as this grid's leave.
-  grid_dependency_wait();
-  grid_dependents_launch();
-  if constexpr (OP == kOpAllReduce) {
-    if (p.straddle_cta && blockIdx.x == gridDim.x - 1) {
-      straddle_pass<DT, WT>(p);
-      return;
+// L2 prefetch of the inputs of the U vectors v0, v0 + T, ... (those below nvec).
+template <int OP, int DT, int U>
+__device__ __forceinline__ void prefetch_vectors(const RingParams &p, unsigned long long v0, unsigned long long T,
+                                                 unsigned long long nvec) {
+  constexpr int E = Fmt<DT>::bytes;
+  constexpr int V = 16 / E;
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const unsigned long long v = v0 + (unsigned long long)k * T;
+    if (v >= nvec) break;
+    if constexpr (OP == kOpAllGather) {
+      const unsigned long long g0 = v * V;
+      const int c = chunk_of(g0, p.base, p.L);
+      prefetch_l2(static_cast<const unsigned char *>(p.in[c]) + (g0 - (unsigned long long)c * p.base) * E);
+    } else {
+      for (int r = 0; r < p.R; ++r) prefetch_l2(static_cast<const unsigned char *>(p.in[r]) + v * 16);
     }
   }
+}
+
+template <int OP, int DT, int WT, int U, int OCC>
+__global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __grid_constant__ RingParams p) {
   using VT = Vec<DT, WT>;
   using W = typename VT::W;
   constexpr int V = VT::V;
@@ -529,7 +539,21 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
   constexpr int NB = direct_batch_ranks(U);  // ranks per batch of loads
   const unsigned long long nvec = p.n_bulk / V;
   const unsigned long long T = (unsigned long long)(gridDim.x - p.straddle_cta) * blockDim.x;
-  for (unsigned long long v0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < nvec; v0 += T * U) {
+  const unsigned long long first_v = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool main_cta = !(OP == kOpAllReduce && p.straddle_cta && blockIdx.x == gridDim.x - 1);
+  if ((p.prefetch & kPrefetchHead) && main_cta) prefetch_vectors<OP, DT, U>(p, first_v, T, nvec);
+  // The next kernel may be scheduled at once: a large grid fills the SMs'
+  // registers or thread slots, so its CTAs take SMs only as this grid's leave.
+  grid_dependency_wait();
+  grid_dependents_launch();
+  if constexpr (OP == kOpAllReduce) {
+    if (!main_cta) {
+      straddle_pass<DT, WT>(p);
+      return;
+    }
+  }
+  for (unsigned long long v0 = first_v; v0 < nvec; v0 += T * U) {
+    if (p.prefetch & kPrefetchAhead) prefetch_vectors<OP, DT, U>(p, v0 + T * U, T, nvec);
     if constexpr (OP == kOpAllGather) {
       // all U loads first, then the stores: U loads in flight per thread
       uint4 val[U];

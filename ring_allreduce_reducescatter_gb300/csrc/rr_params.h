@@ -44,7 +44,17 @@ struct RingParams {
   int hd_extra;                   // halving-doubling: R - P ranks folded in pairs first
   int straddle_cta;               // direct AllReduce: 1 if the grid's last CTA folds the vectors over chunk boundaries
   int shifted;                    // direct ReduceScatter / AllGather: chunk boundaries off the 16-byte grid
+  int prefetch;                   // direct path: kPrefetch* bits
 };
+
+// L2 prefetch of the direct path's inputs (no data reaches the SM, so no
+// registers are held): kPrefetchHead, a thread's first vectors before the
+// programmatic-launch wait (their DRAM latency overlaps the previous kernel's
+// tail; a prefetch has no effect on the values read after the wait, since L2
+// is where the previous kernel's writes land); kPrefetchAhead, the next
+// iteration's vectors while the current ones load (twice the requests in
+// flight per thread).
+enum : int { kPrefetchHead = 1, kPrefetchAhead = 2 };
 
 // Loads a direct-path thread issues together for one group: U vectors of NB
 // ranks each.  Eight whatever U is (nine for U = 3, a three-rank group whole).

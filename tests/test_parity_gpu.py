@@ -941,6 +941,17 @@ def test_every_direct_variant(rr, dtype, wire):
                     for c in range(R):
                         assert_same(host(parts[c]), ref_rs.outs[c], f"RS U={u} occ={occ} cap={cap} R={R} "
                                                                     f"off_grid={off_grid} chunk {c}")
+                for pf in (2, 3, 4):  # L2 prefetch before the wait, one iteration ahead, both
+                    cfg = rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, cap, 0, 0, 0, pf)
+                    outs = run_ar(rr, xs, wire, cfg=cfg)
+                    torch.cuda.synchronize()
+                    for r in range(R):
+                        assert_same(host(outs[r]), ref_ar.outs[r], f"AR prefetch={pf} cap={cap} R={R} rank {r}")
+                    parts = [torch.full((lens[c],), float("nan"), dtype=dtype, device="cuda") for c in range(R)]
+                    rr.collective(rr.OP_REDUCE_SCATTER, xs, parts, N, wire, 0, None, cfg)
+                    torch.cuda.synchronize()
+                    for c in range(R):
+                        assert_same(host(parts[c]), ref_rs.outs[c], f"RS prefetch={pf} cap={cap} R={R} chunk {c}")
                 if ref_ag is None:
                     continue
                 for u, occ in direct_variants("ag", False, off_grid):
@@ -951,6 +962,13 @@ def test_every_direct_variant(rr, dtype, wire):
                     for r in range(R):
                         assert_same(host(outs[r]), ref_ag.outs[r], f"AG U={u} occ={occ} cap={cap} R={R} "
                                                                    f"off_grid={off_grid} rank {r}")
+                for pf in (2, 3, 4):
+                    outs = [torch.full((N,), float("nan"), dtype=dtype, device="cuda") for _ in range(R)]
+                    rr.collective(rr.OP_ALLGATHER, chunks, outs, N, None, 0, None,
+                                  rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, cap, 0, 0, 0, pf))
+                    torch.cuda.synchronize()
+                    for r in range(R):
+                        assert_same(host(outs[r]), ref_ag.outs[r], f"AG prefetch={pf} cap={cap} R={R} rank {r}")
     assert rr.device_status() == 0
 
 
