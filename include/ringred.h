@@ -359,6 +359,23 @@ rr_status ring_device_status(unsigned int *flags);
  */
 rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t stream);
 
+/*
+ * Debug builds.  The library can be built with device-side bounds checks
+ * (the build script's debug mode, -DRR_DEBUG_CHECKS): every load, store,
+ * bulk copy and prefetch a kernel makes of a rank buffer is checked against
+ * that buffer's extent in the launch (count elements, or one chunk for a
+ * ReduceScatter output / AllGather input).  An access outside is skipped
+ * instead of made, and bit 1 (value 2) of the device status word is set
+ * (ring_device_status); nothing faults.  Results are otherwise bit-identical.
+ * ring_debug_checks returns 1 for such a build, 0 for a release build.
+ * ring_debug_set_margin(bytes) makes the checks treat every buffer as `bytes`
+ * shorter than it is (process-wide, for later launches), so a test can see
+ * the checks fire on accesses that are in fact valid; 0 restores the true
+ * extents.  A release build returns RR_ERR_UNSUPPORTED.
+ */
+int ring_debug_checks(void);
+rr_status ring_debug_set_margin(size_t bytes);
+
 /* RR_ABI_VERSION of the library. */
 int ring_abi_version(void);
 

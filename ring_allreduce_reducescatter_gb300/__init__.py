@@ -18,12 +18,15 @@ __all__ = [
     "RingError", "lib", "allreduce", "reduce_scatter", "allgather", "collective", "plan",
     "allreduce_range", "allreduce_host", "allreduce_host_static", "host_workspace_bytes", "allreduce_algo",
     "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg", "rank_buffers",
+    "debug_checks", "debug_set_margin",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
     "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE", "PATH_DIRECT",
 ]
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_DIR, "libringred.so")
+# RINGRED_LIBRARY names another build of the library to load instead (the
+# debug build with device-side bounds checks, libringred_debug.so)
+LIB_PATH = os.environ.get("RINGRED_LIBRARY") or os.path.join(_DIR, "libringred.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT = range(6)
 OP_ALLREDUCE, OP_REDUCE_SCATTER, OP_ALLGATHER = 0, 1, 2
@@ -134,6 +137,10 @@ def lib() -> ctypes.CDLL:
         L.ring_last_cuda_error.restype = i
         L.ring_last_cuda_error_string.argtypes = []
         L.ring_last_cuda_error_string.restype = ctypes.c_char_p
+        L.ring_debug_checks.argtypes = []
+        L.ring_debug_checks.restype = i
+        L.ring_debug_set_margin.argtypes = [sz]
+        L.ring_debug_set_margin.restype = i
         _lib = L
     return _lib
 
@@ -360,6 +367,18 @@ def allreduce_host_static(host_ins, host_outs, wire=None, group_size: int = 0, p
                                           _stream_handle(stream))
     if st != OK:
         raise RingError(st, "ring_allreduce_host_static")
+
+
+def debug_checks() -> bool:
+    """True when the loaded library is the debug build (device-side bounds checks)."""
+    return bool(lib().ring_debug_checks())
+
+
+def debug_set_margin(nbytes: int) -> None:
+    """Debug build: the checks treat every buffer as nbytes shorter (0 restores)."""
+    st = lib().ring_debug_set_margin(nbytes)
+    if st != OK:
+        raise RingError(st, "ring_debug_set_margin")
 
 
 def device_status() -> int:

@@ -26,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libringred.so")
+# the same library with device-side bounds checks (RR_DEBUG_CHECKS)
+DEBUG_LIB = os.path.join(PKG, "libringred_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",
          "-I", INCLUDE, "-I", CSRC]
@@ -64,18 +66,24 @@ def _recorded_digest(lib: str):
         return None
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    """Build libringred.so (or, debug=True, libringred_debug.so with every
+    device access of a rank buffer checked against its extent) unless the
+    recorded digest shows it is current.  Returns the library's path."""
     cc = nvcc()
-    digest = source_digest(cc, FLAGS)
-    if not force and os.path.exists(LIB) and _recorded_digest(LIB) == digest:
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    lib = DEBUG_LIB if debug else LIB
+    flags = FLAGS + (["-DRR_DEBUG_CHECKS=1"] if debug else [])
+    objdir = os.path.join(BUILD, "debug") if debug else BUILD
+    digest = source_digest(cc, flags)
+    if not force and os.path.exists(lib) and _recorded_digest(lib) == digest:
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        cmd = [cc, *ARCH, *flags, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -86,19 +94,19 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if verbose_ptxas:
         for _, log in results:
             print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(_digest_path(LIB) + f".tmp{os.getpid()}", "w") as f:
+    os.replace(tmp, lib)
+    with open(_digest_path(lib) + f".tmp{os.getpid()}", "w") as f:
         f.write(digest + "\n")
-    os.replace(_digest_path(LIB) + f".tmp{os.getpid()}", _digest_path(LIB))
-    return LIB
+    os.replace(_digest_path(lib) + f".tmp{os.getpid()}", _digest_path(lib))
+    return lib
 
 
 if __name__ == "__main__":
     import sys
 
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -6,12 +6,17 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ringred.h"
 #include "rr_params.h"
 
 namespace {
+
+// Debug builds: bytes the device-side bounds checks take off every buffer's
+// extent (ring_debug_set_margin); 0 checks the true extents.
+std::atomic<unsigned long long> g_debug_margin{0};
 
 // Sticky device status word (bit rr::kStatusWaitTimeout).  Kernels get its
 // device address, taken with cudaGetSymbolAddress for each device.
@@ -488,6 +493,7 @@ rr_status plan(const Checked &ck, const void *const *in, void *const *out, const
     p->out[r] = out[r];
   }
   p->status = dev.status;
+  p->debug_margin = g_debug_margin.load(std::memory_order_relaxed);
   return plan_launch(ck, cfg, dev.sms, dev.smem_per_sm, dev.smem_optin, p, l);
 }
 
@@ -795,6 +801,24 @@ rr_status ring_selftest_bounded_wait(unsigned long long limit_ns, cudaStream_t s
 }
 
 int ring_abi_version(void) { return RR_ABI_VERSION; }
+
+int ring_debug_checks(void) {
+#ifdef RR_DEBUG_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+rr_status ring_debug_set_margin(size_t bytes) {
+#ifdef RR_DEBUG_CHECKS
+  g_debug_margin.store((unsigned long long)bytes, std::memory_order_relaxed);
+  return RR_OK;
+#else
+  (void)bytes;
+  return RR_ERR_UNSUPPORTED;
+#endif
+}
 
 int ring_last_cuda_error(void) { return g_last_cuda_error; }
 

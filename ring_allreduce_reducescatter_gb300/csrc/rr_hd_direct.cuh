@@ -18,7 +18,7 @@ namespace hd {
 // The 2^LOG2N leaves v0 + m * stride (m < 2^LOG2N), loaded together (two
 // ranks for a leaf v < E when EXTRA, one otherwise) and combined by the tree
 // whose first level pairs m and m + 2^LOG2N / 2.
-template <class VT, int LOG2N, bool EXTRA>
+template <class VT, int E, int LOG2N, bool EXTRA>
 __device__ __forceinline__ typename VT::W hd_batch(const RingParams &p, unsigned long long boff, int v0, int stride) {
   using W = typename VT::W;
   constexpr int N = 1 << LOG2N;
@@ -28,9 +28,9 @@ __device__ __forceinline__ typename VT::W hd_batch(const RingParams &p, unsigned
   for (int m = 0; m < N; ++m) {
     const int v = v0 + m * stride;
     const bool pair = EXTRA && v < Ex;
-    xa[m] = ldg_stream(static_cast<const unsigned char *>(p.in[pair ? 2 * v : v + Ex]) + boff);
+    xa[m] = load_in<false, E>(p, pair ? 2 * v : v + Ex, boff);
     if constexpr (EXTRA) {
-      xb[m] = pair ? ldg_stream(static_cast<const unsigned char *>(p.in[2 * v + 1]) + boff) : make_uint4(0, 0, 0, 0);
+      xb[m] = pair ? load_in<false, E>(p, 2 * v + 1, boff) : make_uint4(0, 0, 0, 0);
     }
   }
   auto leaf = [&](int m) {
@@ -47,14 +47,14 @@ __device__ __forceinline__ typename VT::W hd_batch(const RingParams &p, unsigned
 // and P/8 apart) only combine leaves of one coset {v + m Q : m < 8}, Q = P/8,
 // so for P > 8 it is the tree over the Q coset sums (partners Q/2, ..., 1
 // apart) of 8-leaf trees: one batch of at most 16 loads per coset.
-template <class VT, int LOG2P, bool EXTRA>
+template <class VT, int E, int LOG2P, bool EXTRA>
 __device__ __forceinline__ typename VT::W hd_vec(const RingParams &p, unsigned long long boff) {
   using W = typename VT::W;
   if constexpr (LOG2P <= 3) {
-    return hd_batch<VT, LOG2P, EXTRA>(p, boff, 0, 1);
+    return hd_batch<VT, E, LOG2P, EXTRA>(p, boff, 0, 1);
   } else {
     constexpr int Q = 1 << (LOG2P - 3);
-    auto coset = [&](int v) { return hd_batch<VT, 3, EXTRA>(p, boff, v, Q); };
+    auto coset = [&](int v) { return hd_batch<VT, E, 3, EXTRA>(p, boff, v, Q); };
     auto add = [](W a, W b) { return VT::hop(a, b); };
     return hd_tree<LOG2P - 3, W>(coset, add);
   }
@@ -67,7 +67,7 @@ __device__ __forceinline__ typename Fmt<DT>::type hd_scalar(const RingParams &p,
   using SC = Scalar<DT, WT>;
   using W = typename SC::W;
   const int Ex = EXTRA ? p.hd_extra : 0;
-  auto x = [&](int r) { return SC::in(static_cast<const S *>(p.in[r])[i]); };
+  auto x = [&](int r) { return SC::in(load_elem<false, S>(p, r, i)); };
   auto leaf = [&](int v) {
     if constexpr (EXTRA) {
       if (v < Ex) return hop(x(2 * v), x(2 * v + 1));
@@ -91,14 +91,14 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_hd_direct_kernel(const
   const unsigned long long T = (unsigned long long)gridDim.x * blockDim.x;
   for (unsigned long long v = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += T) {
     const unsigned long long boff = v * V * E;
-    const uint4 res = VT::out(hd_vec<VT, LOG2P, EXTRA>(p, boff));
-    for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, res);
+    const uint4 res = VT::out(hd_vec<VT, E, LOG2P, EXTRA>(p, boff));
+    for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, boff, res);
   }
   // the ragged end (under 16 bytes per rank)
   for (unsigned long long i = p.n_bulk + (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count;
        i += T) {
     const typename Fmt<DT>::type y = hd_scalar<DT, WT, LOG2P, EXTRA>(p, i);
-    for (int r = 0; r < p.R; ++r) static_cast<typename Fmt<DT>::type *>(p.out[r])[i] = y;
+    for (int r = 0; r < p.R; ++r) store_elem<false, typename Fmt<DT>::type>(p, r, i, y);
   }
 }
 

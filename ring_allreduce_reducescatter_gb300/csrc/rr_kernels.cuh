@@ -48,6 +48,98 @@
 namespace rr {
 
 // --------------------------------------------------------------------------
+// accesses to the rank buffers.  Every load, store, bulk copy and prefetch of
+// a rank buffer goes through these.  A debug build (RR_DEBUG_CHECKS) checks
+// each against the buffer's extent in this launch; an access outside it is
+// skipped (a load reads zeros, a skipped bulk load's bytes are retired from
+// its barrier) and sets kStatusIndexFault in the status word, so an index
+// error shows as a status bit, not a fault.  A release build compiles each to
+// the plain access.  CH: the buffer holds one chunk (a ReduceScatter output, an
+// AllGather input); otherwise the launch's `count` elements.
+// --------------------------------------------------------------------------
+
+#ifdef RR_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+__device__ __forceinline__ unsigned long long extent_bytes(const RingParams &p, int r, bool chunk, int E) {
+  const unsigned long long n =
+      chunk ? (r < p.L - 1 ? p.base : p.total - (unsigned long long)(p.L - 1) * p.base) : p.count;
+  return n * (unsigned long long)E;
+}
+
+// [off, off + bytes) of buffer r lies inside its extent (always, in a release build).
+template <bool CH, int E>
+__device__ __forceinline__ bool access_ok(const RingParams &p, int r, unsigned long long off,
+                                          unsigned long long bytes) {
+  if constexpr (kDebugChecks) {
+    if (r < 0 || r >= p.R) {
+      atomicOr(p.status, kStatusIndexFault);
+      return false;
+    }
+    const unsigned long long ext = extent_bytes(p, r, CH, E);
+    const unsigned long long lim = ext > p.debug_margin ? ext - p.debug_margin : 0;
+    if (off > lim || bytes > lim - off) {
+      atomicOr(p.status, kStatusIndexFault);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <bool CH, int E>
+__device__ __forceinline__ uint4 load_in(const RingParams &p, int r, unsigned long long off) {
+  if (!access_ok<CH, E>(p, r, off, 16)) return make_uint4(0u, 0u, 0u, 0u);
+  return ldg_stream(static_cast<const unsigned char *>(p.in[r]) + off);
+}
+
+template <bool CH, int E>
+__device__ __forceinline__ uint4 load_in_l1(const RingParams &p, int r, unsigned long long off) {
+  if (!access_ok<CH, E>(p, r, off, 16)) return make_uint4(0u, 0u, 0u, 0u);
+  return ldg_l1(static_cast<const unsigned char *>(p.in[r]) + off);
+}
+
+template <bool CH, int E>
+__device__ __forceinline__ void store_out(const RingParams &p, int r, unsigned long long off, uint4 v) {
+  if (access_ok<CH, E>(p, r, off, 16)) stg_stream(static_cast<unsigned char *>(p.out[r]) + off, v);
+}
+
+template <bool CH, int E>
+__device__ __forceinline__ void prefetch_in(const RingParams &p, int r, unsigned long long off) {
+  if (access_ok<CH, E>(p, r, off, 16)) prefetch_l2(static_cast<const unsigned char *>(p.in[r]) + off);
+}
+
+// One element (index i of the buffer).
+template <bool CH, class S>
+__device__ __forceinline__ S load_elem(const RingParams &p, int r, unsigned long long i) {
+  if (!access_ok<CH, (int)sizeof(S)>(p, r, i * sizeof(S), sizeof(S))) return S{};
+  return static_cast<const S *>(p.in[r])[i];
+}
+
+template <bool CH, class S>
+__device__ __forceinline__ void store_elem(const RingParams &p, int r, unsigned long long i, S v) {
+  if (access_ok<CH, (int)sizeof(S)>(p, r, i * sizeof(S), sizeof(S))) static_cast<S *>(p.out[r])[i] = v;
+}
+
+// Bulk copy of `bytes` from input r at `off` into shared memory (completion on bar).
+template <bool CH, int E>
+__device__ __forceinline__ void bulk_load_in(const RingParams &p, int r, unsigned long long off, void *smem_dst,
+                                             uint32_t bytes, uint64_t *bar, uint64_t pol) {
+  if (access_ok<CH, E>(p, r, off, bytes))
+    bulk_load(smem_dst, static_cast<const unsigned char *>(p.in[r]) + off, bytes, bar, pol);
+  else
+    mbar_complete_tx(bar, bytes);
+}
+
+template <bool CH, int E>
+__device__ __forceinline__ void bulk_store_out(const RingParams &p, int r, unsigned long long off,
+                                               const void *smem_src, uint32_t bytes, uint64_t pol) {
+  if (access_ok<CH, E>(p, r, off, bytes)) bulk_store(static_cast<unsigned char *>(p.out[r]) + off, smem_src, bytes, pol);
+}
+
+// --------------------------------------------------------------------------
 // summation orders of the other AllReduce algorithms (page
 // ai6s.net/6a0dd5b5662f9a54cb75ef90.html, TpAllReduceOp::Execute)
 // --------------------------------------------------------------------------
@@ -124,10 +216,10 @@ __device__ __forceinline__ typename Scalar<DT, WT>::W fold_group_global(const Ri
   using SC = Scalar<DT, WT>;
   const int L = p.L;
   int r = c;
-  typename SC::W acc = SC::in(static_cast<const S *>(p.in[g * L + r])[i]);
+  typename SC::W acc = SC::in(load_elem<false, S>(p, g * L + r, i));
   for (int k = 1; k < L; ++k) {
     r = (r + 1 == L) ? 0 : r + 1;
-    acc = hop(acc, SC::in(static_cast<const S *>(p.in[g * L + r])[i]));
+    acc = hop(acc, SC::in(load_elem<false, S>(p, g * L + r, i)));
   }
   return acc;
 }
@@ -147,7 +239,7 @@ __device__ __forceinline__ typename Fmt<DT>::type hd_elem_global(const RingParam
   using SC = Scalar<DT, WT>;
   using W = typename SC::W;
   const int E = p.hd_extra;
-  auto x = [&](int r) { return SC::in(static_cast<const S *>(p.in[r])[i]); };
+  auto x = [&](int r) { return SC::in(load_elem<false, S>(p, r, i)); };
   auto leaf = [&](int v) { return v < E ? hop(x(2 * v), x(2 * v + 1)) : x(v + E); };
   auto add = [](W a, W b) { return hop(a, b); };
   return SC::out(hd_fold<W>(p.hd_log2p, leaf, add));
@@ -165,13 +257,13 @@ __device__ __forceinline__ void element_op(const RingParams &p, unsigned long lo
       v = hd_elem_global<DT, WT>(p, i);
     else
       v = fold_elem_global<DT, WT>(p, i, c);
-    for (int r = 0; r < p.R; ++r) static_cast<S *>(p.out[r])[i] = v;
+    for (int r = 0; r < p.R; ++r) store_elem<false, S>(p, r, i, v);
   } else if (OP == kOpReduceScatter) {
     const S v = fold_elem_global<DT, WT>(p, i, c);
-    static_cast<S *>(p.out[c])[i - (unsigned long long)c * p.base] = v;
+    store_elem<true, S>(p, c, i - (unsigned long long)c * p.base, v);
   } else {
-    const S v = static_cast<const S *>(p.in[c])[i - (unsigned long long)c * p.base];
-    for (int r = 0; r < p.R; ++r) static_cast<S *>(p.out[r])[i] = v;
+    const S v = load_elem<true, S>(p, c, i - (unsigned long long)c * p.base);
+    for (int r = 0; r < p.R; ++r) store_elem<false, S>(p, r, i, v);
   }
 }
 
@@ -301,8 +393,7 @@ __device__ __forceinline__ void issue_loads(const RingParams &p, unsigned char *
   const uint32_t bytes = (uint32_t)((t1 - t0) * E);
   if (OP != kOpAllGather) {
     mbar_arrive_expect_tx(bar, bytes * (uint32_t)p.R);
-    for (int r = 0; r < p.R; ++r)
-      bulk_load(stage + (size_t)r * slot_bytes, static_cast<const unsigned char *>(p.in[r]) + t0 * E, bytes, bar, pol);
+    for (int r = 0; r < p.R; ++r) bulk_load_in<false, E>(p, r, t0 * E, stage + (size_t)r * slot_bytes, bytes, bar, pol);
   } else {
     mbar_arrive_expect_tx(bar, bytes);
     const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
@@ -310,9 +401,7 @@ __device__ __forceinline__ void issue_loads(const RingParams &p, unsigned char *
       const unsigned long long off = (unsigned long long)c * p.base;
       const unsigned long long end = chunk_end(c, p.base, p.L, p.total);
       const unsigned long long s0 = t0 > off ? t0 : off, s1 = t1 < end ? t1 : end;
-      if (s1 > s0)
-        bulk_load(stage + (s0 - t0) * E, static_cast<const unsigned char *>(p.in[c]) + (s0 - off) * E,
-                  (uint32_t)((s1 - s0) * E), bar, pol);
+      if (s1 > s0) bulk_load_in<true, E>(p, c, (s0 - off) * E, stage + (s0 - t0) * E, (uint32_t)((s1 - s0) * E), bar, pol);
     }
   }
 }
@@ -326,16 +415,14 @@ __device__ __forceinline__ void issue_stores(const RingParams &p, const unsigned
   const unsigned long long t0 = tile_begin(p, t), t1 = tile_end(p, t);
   const uint32_t bytes = (uint32_t)((t1 - t0) * E);
   if (OP != kOpReduceScatter) {
-    for (int r = 0; r < p.R; ++r) bulk_store(static_cast<unsigned char *>(p.out[r]) + t0 * E, stage, bytes, pol);
+    for (int r = 0; r < p.R; ++r) bulk_store_out<false, E>(p, r, t0 * E, stage, bytes, pol);
   } else {
     const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
     for (int c = c_lo; c <= c_hi; ++c) {
       const unsigned long long off = (unsigned long long)c * p.base;
       const unsigned long long end = chunk_end(c, p.base, p.L, p.total);
       const unsigned long long s0 = t0 > off ? t0 : off, s1 = t1 < end ? t1 : end;
-      if (s1 > s0)
-        bulk_store(static_cast<unsigned char *>(p.out[c]) + (s0 - off) * E, stage + (s0 - t0) * E,
-                   (uint32_t)((s1 - s0) * E), pol);
+      if (s1 > s0) bulk_store_out<true, E>(p, c, (s0 - off) * E, stage + (s0 - t0) * E, (uint32_t)((s1 - s0) * E), pol);
     }
   }
 }
@@ -467,7 +554,7 @@ __device__ __forceinline__ void straddle_vec(const RingParams &p, unsigned long 
         if (k0 + j < L) {
           int r = c0 + k0 + j;
           r -= (r >= L) ? L : 0;
-          x[j] = ldg_stream(static_cast<const unsigned char *>(p.in[g * L + r]) + boff);
+          x[j] = load_in<false, E>(p, g * L + r, boff);
         }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -488,7 +575,7 @@ __device__ __forceinline__ void straddle_vec(const RingParams &p, unsigned long 
     total_b = (g == 0) ? b : VT::hop(total_b, b);
   }
   const uint4 res = blend_bytes(VT::out(total_a), VT::out(total_b), split * E);
-  for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, res);
+  for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, boff, res);
 }
 
 // The AllReduce vectors that straddle a chunk boundary, done by one extra CTA
@@ -523,9 +610,9 @@ __device__ __forceinline__ void prefetch_vectors(const RingParams &p, unsigned l
     if constexpr (OP == kOpAllGather) {
       const unsigned long long g0 = v * V;
       const int c = chunk_of(g0, p.base, p.L);
-      prefetch_l2(static_cast<const unsigned char *>(p.in[c]) + (g0 - (unsigned long long)c * p.base) * E);
+      if (c == chunk_of(g0 + V - 1, p.base, p.L)) prefetch_in<true, E>(p, c, (g0 - (unsigned long long)c * p.base) * E);
     } else {
-      for (int r = 0; r < p.R; ++r) prefetch_l2(static_cast<const unsigned char *>(p.in[r]) + v * 16);
+      for (int r = 0; r < p.R; ++r) prefetch_in<false, E>(p, r, v * 16);
     }
   }
 }
@@ -570,13 +657,13 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
           live[k] = false;
           continue;
         }
-        val[k] = ldg_stream(static_cast<const unsigned char *>(p.in[c]) + (i0 - (unsigned long long)c * p.base) * E);
+        val[k] = load_in<true, E>(p, c, (i0 - (unsigned long long)c * p.base) * E);
       }
 #pragma unroll
       for (int k = 0; k < U; ++k) {
         if (!live[k]) continue;
         const unsigned long long boff = (v0 + (unsigned long long)k * T) * V * E;
-        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff, val[k]);
+        for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, boff, val[k]);
       }
     } else {  // ring / naive fold, AllReduce or ReduceScatter
       unsigned long long boff[U];
@@ -611,7 +698,7 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
               if (live[k] && k0 + j < L) {
                 int r = c[k] + k0 + j;
                 r -= (r >= L) ? L : 0;
-                x[k][j] = ldg_stream(static_cast<const unsigned char *>(p.in[g * L + r]) + boff[k]);
+                x[k][j] = load_in<false, E>(p, g * L + r, boff[k]);
               }
 #pragma unroll
           for (int k = 0; k < U; ++k)
@@ -627,10 +714,10 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         if (!live[k]) continue;
         const uint4 res = VT::out(total[k]);
         if constexpr (OP == kOpAllReduce) {
-          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + boff[k], res);
+          for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, boff[k], res);
         } else {  // ReduceScatter: the vector lies in chunk c[k]
           const unsigned long long i0 = boff[k] / E;
-          stg_stream(static_cast<unsigned char *>(p.out[c[k]]) + (i0 - (unsigned long long)c[k] * p.base) * E, res);
+          store_out<true, E>(p, c[k], (i0 - (unsigned long long)c[k] * p.base) * E, res);
         }
       }
     }
@@ -719,8 +806,7 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
               if (k0 + j < L) {
                 int r = c + k0 + j;
                 r -= (r >= L) ? L : 0;
-                blk[k][j] = load[k] ? ldg_stream(static_cast<const unsigned char *>(p.in[r]) + ga[k] * E)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+                blk[k][j] = load[k] ? load_in<false, E>(p, r, ga[k] * E) : make_uint4(0u, 0u, 0u, 0u);
               }
 #pragma unroll
           for (int k = 0; k < US; ++k)
@@ -740,7 +826,7 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
           if (tail[k]) {
             for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, g0 + u[k] * V + e);
           } else if (act[k]) {
-            stg_stream(static_cast<unsigned char *>(p.out[c]) + u[k] * V * E, VT::out(acc[k]));
+            store_out<true, E>(p, c, u[k] * V * E, VT::out(acc[k]));
           }
         }
       }
@@ -782,7 +868,6 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
       const unsigned long long vf = (cb + V - 1) / V;  // first output vector wholly in the chunk
       const unsigned long long ve = (cb + len) / V < nvec ? (cb + len) / V : nvec;  // one past the last
       const int sh = (int)((vf * V - cb) % V) * E;     // where a vector's source starts in its aligned block
-      const unsigned char *src = static_cast<const unsigned char *>(p.in[c]);
       uint4 blk[US], nxt[US];
       bool act[US], tail[US];
 #pragma unroll
@@ -793,8 +878,8 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
         const unsigned long long o = v * V - cb, oa = o - (o % V);
         const bool load = v >= vf && v <= ve && oa + V <= len;
         tail[k] = act[k] && sh != 0 && oa + 2 * V > len;
-        blk[k] = load ? ldg_stream(src + oa * E) : make_uint4(0u, 0u, 0u, 0u);
-        nxt[k] = (lane == 31u && act[k] && sh != 0 && !tail[k]) ? ldg_stream(src + (oa + V) * E)
+        blk[k] = load ? load_in<true, E>(p, c, oa * E) : make_uint4(0u, 0u, 0u, 0u);
+        nxt[k] = (lane == 31u && act[k] && sh != 0 && !tail[k]) ? load_in<true, E>(p, c, (oa + V) * E)
                                                                : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
@@ -810,7 +895,7 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
           for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
         } else if (act[k]) {
           const uint4 x = sh ? funnel16(blk[k], nxt[k], sh) : blk[k];
-          for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + v * V * E, x);
+          for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, v * V * E, x);
         }
       }
     }
@@ -845,16 +930,15 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
           live[k] = false;
           continue;
         }
-        const unsigned char *src = static_cast<const unsigned char *>(p.in[c]) + oa * E;
-        lo[k] = ldg_l1(src);
-        hi[k] = sh[k] ? ldg_l1(src + 16) : lo[k];
+        lo[k] = load_in_l1<true, E>(p, c, oa * E);
+        hi[k] = sh[k] ? load_in_l1<true, E>(p, c, oa * E + 16) : lo[k];
       }
 #pragma unroll
       for (int k = 0; k < US; ++k) {
         if (!live[k]) continue;
         const uint4 x = sh[k] ? funnel16(lo[k], hi[k], sh[k]) : lo[k];
         const unsigned long long gs = (v0 + (unsigned long long)k * T) * V;
-        for (int r = 0; r < p.R; ++r) stg_stream(static_cast<unsigned char *>(p.out[r]) + gs * E, x);
+        for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, gs * E, x);
       }
     }
     for (unsigned long long i = p.n_bulk + tid; i < p.count; i += T) element_op<OP, DT, WT>(p, i);

@@ -14,8 +14,10 @@ enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 enum : int { kOpAllReduce = 0, kOpReduceScatter = 1, kOpAllGather = 2 };
 enum : int { kAlgoRing = 0, kAlgoHalvingDoubling = 1, kAlgoNaive = 2 };
 
-// Device status bits (the word lives in rr_api.cu).
-enum : unsigned int { kStatusWaitTimeout = 1u };
+// Device status bits (the word lives in rr_api.cu).  kStatusIndexFault is
+// only ever set by a debug build (RR_DEBUG_CHECKS): an access outside its
+// buffer was skipped.
+enum : unsigned int { kStatusWaitTimeout = 1u, kStatusIndexFault = 2u };
 
 // Limit of one bounded wait inside a kernel.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -45,6 +47,7 @@ struct RingParams {
   int straddle_cta;               // direct AllReduce: 1 if the grid's last CTA folds the vectors over chunk boundaries
   int shifted;                    // direct ReduceScatter / AllGather: chunk boundaries off the 16-byte grid
   int prefetch;                   // direct path: kPrefetch* bits
+  unsigned long long debug_margin;  // debug build: bytes taken off every buffer's extent by the checks
 };
 
 // L2 prefetch of the direct path's inputs (no data reaches the SM, so no

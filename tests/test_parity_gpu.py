@@ -37,6 +37,15 @@ def rr():
     return mod
 
 
+@pytest.fixture(autouse=True)
+def device_status_stays_clear(request):
+    """After every test: no kernel recorded a bounded-wait timeout or (in the
+    debug build) an access outside its buffer."""
+    yield
+    if "rr" in request.fixturenames:
+        assert request.getfixturevalue("rr").device_status() == 0, "a kernel set the device status word"
+
+
 @pytest.fixture(scope="module")
 def wl():
     from ring_allreduce_reducescatter_gb300 import workloads
