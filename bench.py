@@ -640,7 +640,7 @@ def run_ours(args):
     # the size sweep and the other workloads: CUDA-graph replay of back-to-back
     # launches over rotating buffer sets at least 3x the L2 size, so every
     # launch reads inputs that are not in L2 and no host time is included
-    sweep, table, overlap = [], [], None
+    sweep, table, overlap, rsag = [], [], None, []
     if not args.no_sweep and world == 1:  # per-GPU tables: every replica would measure the same
         del outs
         torch.cuda.empty_cache()
@@ -658,6 +658,14 @@ def run_ours(args):
             del xs
             torch.cuda.empty_cache()
             table.append(bucket_set_row(rr, wl, dev, peak))
+            # ReduceScatter / AllGather over few ranks, chunk boundaries on and off
+            # the 16-byte grid (binary16, the planner's choice)
+            for op_ in (1, 2):
+                for R_ in (2, 3, 4, 8):
+                    for mib in (16, 256):
+                        for off in (False, True):
+                            rsag.extend(path_sweep_point(rr, dev, l2_bytes, peak, op_, R_, mib, torch.float16, None,
+                                                         off, False, only_auto=True))
             overlap = [overlap_row(rr, wl, dev, max_ctas=m) for m in (0, 128, 96, 64)]
             overlap.append(overlap_row(rr, wl, dev, beside_compute=1))
             xs, outs = staggered_inputs(rr, wl, w, dev)
@@ -724,7 +732,8 @@ def run_ours(args):
                          "kernel_ms": round(kern_ms, 5), "algorithmic_bytes_per_launch": 2 * R * msg},
             "busbw_gbs": round(value / world * 2 * (R - 1) / R, 3),
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": gpu_launches,
-            "sweep": sweep, "workloads": table, "overlap": overlap, "kernel_sources": digest,
+            "sweep": sweep, "workloads": table, "reduce_scatter_allgather": rsag, "overlap": overlap,
+            "kernel_sources": digest,
         }
         print(json.dumps(line), flush=True)
     if pg:
@@ -739,12 +748,19 @@ def run_ours(args):
 SWEEP_OPS = {"ar": 0, "rs": 1, "ag": 2}
 
 
-def sweep_variants(rr, op, wide, shifted, all_variants, prefetch=False):
+def sweep_variants(rr, op, wide, shifted, all_variants, prefetch=False, explicit=""):
     """(label, cfg) pairs to time at one point: the planner's choice, the tile
     pipeline and the direct path (each forced); with prefetch the direct path
     under each L2-prefetch mode; with all_variants every direct kernel the
     library builds (vectors a thread x register budget)."""
     out = [("auto", None), ("bulk", rr.LaunchCfg(rr.PATH_BULK)), ("direct", rr.LaunchCfg(rr.PATH_DIRECT))]
+    if explicit:
+        out = [("auto", None)]
+        for item in explicit.split(";"):
+            path, u, occ, pf = (int(v) for v in item.split(","))
+            out.append((f"path={path} U={u} occ={occ} prefetch={pf}",
+                        rr.LaunchCfg(path, 0, 0, occ, 0, 0, 0, u, 0, pf)))
+        return out
     if prefetch and not shifted:
         for pf, name in ((1, "none"), (2, "head"), (3, "ahead"), (4, "head+ahead")):
             out.append((f"direct prefetch={name}", rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, 0, 0, 0, 0, pf)))
@@ -763,10 +779,38 @@ def sweep_variants(rr, op, wide, shifted, all_variants, prefetch=False):
     return out
 
 
-def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid, all_variants, prefetch=False):
+SWEEP_STAGGERS = ((2 << 20), (2 << 20) + (640 << 10) + 256, (5 << 20) + 4096, (1 << 20) + (320 << 10) + 768)
+
+
+def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid, all_variants, prefetch=False,
+                     only_auto=False, layouts=1, explicit=""):
     """Time every variant of one (collective, ranks, size) point.  Chunks are
     whole multiples of the 16-byte vector (or, off_grid, one element more, so
-    chunk boundaries fall off the 16-byte grid).  Returns JSON rows."""
+    chunk boundaries fall off the 16-byte grid).  With layouts > 1 every
+    variant is timed on that many buffer layouts (rank vectors staggered by
+    different distances; where the ranks sit in HBM moves some points by up
+    to ~10 %) and the row reports the median over layouts.  Returns JSON rows."""
+    rows = None
+    for j in range(layouts):
+        part = path_sweep_layout(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid, all_variants, prefetch,
+                                 only_auto, SWEEP_STAGGERS[j % len(SWEEP_STAGGERS)], explicit)
+        if rows is None:
+            rows = part
+            for r in rows:
+                r["us_layouts"] = [r["us"]]
+        else:
+            for r, q in zip(rows, part):
+                r["us_layouts"].append(q["us"])
+    for r in rows or []:
+        if layouts > 1:
+            med = statistics.median(r["us_layouts"])
+            r["frac"] = round(r["frac"] * r["us"] / med, 4)
+            r["us"] = round(med, 3)
+    return rows or []
+
+
+def path_sweep_layout(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid, all_variants, prefetch, only_auto,
+                      stagger, explicit=""):
     import torch
 
     E = torch.tensor([], dtype=dtype).element_size()
@@ -780,10 +824,10 @@ def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid
     nsets = max(1, min(16, -(-3 * l2_bytes // set_bytes)))
     sets = []
     for k in range(nsets):
-        ins = rr.rank_buffers(R_, in_lens, dtype, dev)
+        ins = rr.rank_buffers(R_, in_lens, dtype, dev, stagger_bytes=stagger)
         for x in ins:
             x.copy_(torch.randn(x.numel(), device=dev).mul_(1e-2).to(dtype))
-        sets.append((ins, rr.rank_buffers(R_, out_lens, dtype, dev)))
+        sets.append((ins, rr.rank_buffers(R_, out_lens, dtype, dev, stagger_bytes=stagger)))
     msg = N * E
     alg = (2 * R_ if op == 0 else R_ + 1) * msg
     # about 2 ms of work per replay, 4 to 40 launches
@@ -791,7 +835,9 @@ def path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid
     wide = dtype != torch.float32 and wire == "f32"
     shifted = off_grid and op != 0
     rows = []
-    for label, cfg in sweep_variants(rr, op, wide, shifted, all_variants, prefetch):
+    variants = [("auto", None)] if only_auto else sweep_variants(rr, op, wide, shifted, all_variants, prefetch,
+                                                                 explicit)
+    for label, cfg in variants:
         try:
             plan = rr.plan(op, sets[0][0], sets[0][1], N, wire, 0, cfg)
         except rr.RingError:
@@ -840,7 +886,8 @@ def run_path_sweep(args):
                     if off_grid and op == 0:
                         continue
                     for row in path_sweep_point(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_grid,
-                                                args.sweep_variants, args.sweep_prefetch):
+                                                args.sweep_variants, args.sweep_prefetch,
+                                                layouts=args.sweep_layouts, explicit=args.sweep_cfg):
                         print(json.dumps(row), flush=True)
 
 
@@ -909,6 +956,9 @@ def main():
                     help="chunk boundaries off the 16-byte grid (ReduceScatter / AllGather)")
     ap.add_argument("--sweep-variants", action="store_true", help="every direct kernel variant too")
     ap.add_argument("--sweep-prefetch", action="store_true", help="the direct path under each L2-prefetch mode too")
+    ap.add_argument("--sweep-layouts", type=int, default=1, help="buffer layouts per point (median reported)")
+    ap.add_argument("--sweep-cfg", default="",
+                    help="explicit launch configurations 'path,vectors,ctas_per_sm,prefetch;...' (with auto)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.gpus < 1:

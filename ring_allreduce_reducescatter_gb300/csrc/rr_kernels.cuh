@@ -144,6 +144,25 @@ __device__ __forceinline__ void bulk_store_out(const RingParams &p, int r, unsig
 // ai6s.net/6a0dd5b5662f9a54cb75ef90.html, TpAllReduceOp::Execute)
 // --------------------------------------------------------------------------
 
+// The chunk of global element i through a one-entry cache of the chunk last
+// looked up: a direct-path thread's vectors advance by a fixed stride, so the
+// 64-bit division of chunk_of runs only when one leaves the cached chunk.
+// [lo, hi) is the cached chunk's index range (the last chunk's reaches the
+// end of the index space, as chunk_of clamps); lo == hi is empty.
+struct ChunkCache {
+  unsigned long long lo = 0, hi = 0;
+  int c = 0;
+};
+
+__device__ __forceinline__ int cached_chunk(ChunkCache &cc, const RingParams &p, unsigned long long i) {
+  if (i - cc.lo < cc.hi - cc.lo) return cc.c;  // lo <= i < hi
+  const int c = chunk_of(i, p.base, p.L);
+  cc.c = c;
+  cc.lo = (unsigned long long)c * p.base;
+  cc.hi = c == p.L - 1 ? ~0ull : (unsigned long long)(c + 1) * p.base;
+  return c;
+}
+
 // Naive (Reduce + Broadcast): the collector adds ranks 0, 1, ..., R-1 in order,
 // which is the ring fold started at rank 0 for every element.
 __device__ __forceinline__ int start_rank(const RingParams &p, unsigned long long global_index) {
@@ -639,6 +658,8 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
       return;
     }
   }
+  ChunkCache cc;
+  const bool naive = p.algo == kAlgoNaive;
   for (unsigned long long v0 = first_v; v0 < nvec; v0 += T * U) {
     if (p.prefetch & kPrefetchAhead) prefetch_vectors<OP, DT, U>(p, v0 + T * U, T, nvec);
     if constexpr (OP == kOpAllGather) {
@@ -651,8 +672,8 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         live[k] = v < nvec;
         if (!live[k]) continue;
         const unsigned long long i0 = v * V, g0 = p.first + i0;
-        const int c = chunk_of(g0, p.base, p.L);
-        if (c != chunk_of(g0 + V - 1, p.base, p.L)) {  // over a chunk boundary: element by element
+        const int c = cached_chunk(cc, p, g0);
+        if (g0 + V - 1 >= cc.hi) {  // over a chunk boundary: element by element
           for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, i0 + e);
           live[k] = false;
           continue;
@@ -675,10 +696,10 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         live[k] = v < nvec;
         boff[k] = v * V * E;
         c[k] = 0;
-        if (live[k]) {
+        if (live[k] && !naive) {  // the naive order starts every element at rank 0
           const unsigned long long g0 = p.first + v * V;
-          c[k] = start_rank(p, g0);
-          if (c[k] != start_rank(p, g0 + V - 1)) {  // straddles a chunk boundary
+          c[k] = cached_chunk(cc, p, g0);
+          if (g0 + V - 1 >= cc.hi) {  // straddles a chunk boundary
             if (!p.straddle_cta)
               for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
             live[k] = false;
