@@ -877,6 +877,7 @@ def run_path_sweep(args):
     peak, _ = measured_hbm_peak()
     dtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.sweep_dtype]
     wire = args.sweep_wire or None
+    all_rows = []
     for op_name in args.sweep_ops.split(","):
         op = SWEEP_OPS[op_name]
         for R_ in (int(v) for v in args.sweep_ranks.split(",")):
@@ -889,6 +890,42 @@ def run_path_sweep(args):
                                                 args.sweep_variants, args.sweep_prefetch,
                                                 layouts=args.sweep_layouts, explicit=args.sweep_cfg):
                         print(json.dumps(row), flush=True)
+                        all_rows.append(row)
+    if args.sweep_table:
+        with open(args.sweep_table, "w") as f:
+            f.write(path_choice_table(all_rows, args))
+
+
+def path_choice_table(rows, args):
+    """Markdown table of the tile pipeline against the direct path at every
+    point (the planner's path and whether it is within 5 % of the faster),
+    from path-sweep rows; tests/test_abi_cpu.py checks the planner against
+    the committed copy."""
+    pts = {}
+    for r in rows:
+        pts.setdefault((r["op"], r["R"], r["count"], r["msg_bytes"], r["off_grid"]), {})[r["variant"]] = r
+    cmd = "python bench.py --path-sweep " + " ".join(
+        f"--{k.replace('_', '-')} {v}" for k, v in (("sweep_ops", args.sweep_ops), ("sweep_ranks", args.sweep_ranks),
+                                                   ("sweep_mib", args.sweep_mib), ("sweep_dtype", args.sweep_dtype),
+                                                   ("sweep_layouts", args.sweep_layouts),
+                                                   ("sweep_off_grid", args.sweep_off_grid))) + " --sweep-table FILE"
+    out = ["# Path choice: tile pipeline against direct path", "",
+           "Made by (one GB300; microseconds per call, CUDA-graph replay over buffer sets of at least 3x the",
+           f"L2, median of {REPLAYS} replays; with several layouts the median over layouts):", "", "```", cmd, "```",
+           "", "| op | R | count | msg bytes | off grid | bulk us | direct us | planner | planner ok |",
+           "|---|---|---|---|---|---|---|---|---|"]
+    for (op, R_, count, msg, off), v in pts.items():
+        if "auto" not in v or "direct" not in v:
+            continue
+        b = v["bulk"]["us"] if "bulk" in v else None
+        d = v["direct"]["us"]
+        planner = v["auto"]["path"]
+        best = min(x for x in (b, d) if x is not None)
+        mine = b if planner == "bulk" else d if planner == "direct" else None
+        ok = mine is not None and mine <= 1.05 * best
+        out.append(f"| {op} | {R_} | {count} | {msg} | {int(off)} | {b if b is not None else '-'} | {d} | {planner} | "
+                   f"{'yes' if ok else 'NO'} |")
+    return "\n".join(out) + "\n"
 
 
 # --------------------------------------------------------------------------
@@ -957,6 +994,7 @@ def main():
     ap.add_argument("--sweep-variants", action="store_true", help="every direct kernel variant too")
     ap.add_argument("--sweep-prefetch", action="store_true", help="the direct path under each L2-prefetch mode too")
     ap.add_argument("--sweep-layouts", type=int, default=1, help="buffer layouts per point (median reported)")
+    ap.add_argument("--sweep-table", default="", help="also write the tile-vs-direct table (markdown) to this file")
     ap.add_argument("--sweep-cfg", default="",
                     help="explicit launch configurations 'path,vectors,ctas_per_sm,prefetch;...' (with auto)")
     args = ap.parse_args()

@@ -186,10 +186,12 @@ typedef struct {
                       RR_BESIDE_COMPUTE_SM_EIGHTHS eighths of the SMs (one CTA each),
                       leaving the rest to the compute.  0: the whole GPU. */
   int prefetch;    /* direct path, L2 prefetch of the inputs: 0 the library's
-                      choice; 1 none; 2 each thread's first vectors before the
-                      wait for the previous kernel (safe: a prefetch never
-                      changes what is read after the wait); 3 the next
-                      iteration's vectors while the current ones load; 4 both */
+                      choice (by message size and ranks); 1 none; 2 each
+                      thread's first vectors before the wait for the previous
+                      kernel (safe: a prefetch never changes what is read after
+                      the wait); 3 the next iteration's vectors while the
+                      current ones load; 4 both.  Ignored by the halving-
+                      doubling order and off-grid ReduceScatter / AllGather. */
 } rr_launch_cfg;
 
 /* Share of the SMs (numerator / 8) a call with beside_compute = 1 takes. */

@@ -186,22 +186,20 @@ int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 unsigned round16_down(unsigned long long x) { return (unsigned)(x & ~15ull); }
 
 // Which of the two 16-byte-aligned paths is faster, from a measured sweep of
-// both (R = 2 .. 32, 256 KiB .. 512 MiB per rank, every collective; CUDA-graph
-// replay over inputs colder than L2).  The direct path keeps eight loads in
-// flight per thread and needs no barriers: it wins for every AllGather, every
-// ReduceScatter with R >= 3, every two-level ring and every flat AllReduce of
-// 3..32 ranks but one case.  The tile pipeline wins for one or two ranks from
-// 4 MiB per rank, for
-// a flat ring of 16 ranks from 64 MiB per rank (two CTAs of three 32 KiB
-// stages fit an SM exactly), and for capped grids (each CTA then owns an SM
-// and moves 8 KB per bulk copy).
+// both (bench.py --path-sweep; CUDA-graph replay over inputs colder than L2).
+// The direct path keeps about eight loads in flight per thread (plus its L2
+// prefetches) and needs no barriers: it wins for every AllGather, every
+// ReduceScatter, every two-level ring and every flat AllReduce but one case.
+// (Two ranks moved to it once the chunk lookup lost its 64-bit division: at
+// 256 MiB per rank, binary16, 0.94 of the copy bandwidth against the tile
+// pipeline's 0.90; ReduceScatter 0.89 against 0.78.)  The tile pipeline wins
+// for a flat ring of 16 ranks from 64 MiB per rank (two CTAs of three 32 KiB
+// stages fit an SM exactly), and for capped grids (each CTA then owns an SM and
+// moves 8 KB per bulk copy).
 bool prefer_direct(int op, int R, int L, unsigned long long msg_bytes, int max_ctas) {
   const unsigned long long MiB = 1ull << 20;
   if (max_ctas > 0) return false;                       // capped grids: one tile pipeline per SM
-  if (op == RR_OP_ALLGATHER) return true;
-  if (op == RR_OP_REDUCE_SCATTER) return R >= 3;
-  if (R <= 2) return msg_bytes <= MiB;                  // the tile pipeline from 4 MiB (0.90 against 0.78)
-  if (L < R) return true;                               // two-level
+  if (op != RR_OP_ALLREDUCE || L < R) return true;      // ReduceScatter, AllGather, two-level
   if (R == 16) return msg_bytes < 64 * MiB;             // two CTAs of three 32 KiB stages per SM
   return true;
 }
@@ -232,6 +230,12 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   p->L = ck.L;
   p->G = ck.R / ck.L;
   p->base = (unsigned long long)ck.count / (unsigned long long)ck.L;
+  if (p->base > 0) {  // the chunk lookup's division by base, as a multiply
+    const rr::ChunkDivisor dv = rr::make_chunk_divisor(p->base);
+    p->div_magic = dv.magic;
+    p->div_shift1 = dv.shift1;
+    p->div_shift2 = dv.shift2;
+  }
   p->algo = ck.algo;
   int P = 1, log2p = 0;
   while (P * 2 <= ck.R) {
@@ -284,9 +288,6 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // R = 9 at 4 MiB lost 3 %.  (Three ranks at three vectors, nine loads but
     // two CTAs per SM: 0.60 against 0.875 at 256 MiB, binary16.)
     if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && msg_bytes >= (64ull << 20)) U = 2;
-    // AllGather over two ranks: two vectors a thread, both loads before the
-    // four stores (256 MiB binary16: 0.83 -> 0.94; 16 MiB: 0.70 -> 0.73)
-    if (ck.op == RR_OP_ALLGATHER && ck.R == 2) U = 2;
     if (p->shifted) {
       // rows a warp takes at once.  Measured, binary16, of the copy bandwidth
       // at 16 / 256 MiB per rank: ReduceScatter R = 2 four rows 0.56 / 0.81
@@ -303,9 +304,30 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     if (wide && U > 2) U = 2;
     if (c.vectors) U = c.vectors;
     p->direct_u = U;
-    // L2 prefetch (kPrefetch* bits): none by default; only the ring / naive
-    // kernels on 16-byte chunk boundaries prefetch
-    p->prefetch = c.prefetch ? c.prefetch - 1 : 0;
+    // L2 prefetch (kPrefetch* bits; only the ring / naive kernels on 16-byte
+    // chunk boundaries prefetch).  Measured, binary16, of the copy bandwidth,
+    // median over buffer layouts:
+    //  - before the launch wait (its DRAM latency overlaps the previous
+    //    kernel): AllReduce R = 8 1 MiB 0.55 -> 0.64, 4 MiB 0.84 -> 0.87;
+    //    R = 4 binary32 ReduceScatter 4 MiB 0.51 -> 0.58; little effect from
+    //    64 MiB, where R = 8 lost 1 % and groups of up to four ranks gained
+    //    0-3 %: below 64 MiB, or up to four ranks a group;
+    //  - one iteration ahead (twice the requests in flight): where threads
+    //    have few loads each, R = 2 (AllReduce 256 MiB 0.90 -> 0.94), every
+    //    AllGather (R = 2 256 MiB 0.88 -> 0.93), ReduceScatter over three
+    //    ranks (0.94 -> 1.00); and from 8 to 64 MiB (AllReduce R = 3 / 4 / 8
+    //    at 16 MiB 0.82 / 0.88 / 0.96 -> 0.91 / 0.94 / 0.99 with both); not
+    //    for ReduceScatter over five or more ranks (R = 8, 16 MiB: 0.99 -> 0.91)
+    //    nor above 64 MiB otherwise (AllReduce R = 8 256 MiB: 0.99 -> 0.95).
+    {
+      const bool small = msg_bytes < (64ull << 20), mid = small && msg_bytes >= (8ull << 20);
+      const bool rs_many = ck.op == RR_OP_REDUCE_SCATTER && ck.L >= 5;
+      int pf = 0;
+      if (small || ck.L <= 4) pf |= rr::kPrefetchHead;
+      if (ck.R == 2 || ck.op == RR_OP_ALLGATHER || (ck.op == RR_OP_REDUCE_SCATTER && ck.L == 3) || (mid && !rs_many))
+        pf |= rr::kPrefetchAhead;
+      p->prefetch = c.prefetch ? c.prefetch - 1 : pf;
+    }
     if (p->shifted || ck.algo == RR_ALGO_HALVING_DOUBLING) p->prefetch = 0;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
     // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5

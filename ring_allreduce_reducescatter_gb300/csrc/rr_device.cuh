@@ -236,10 +236,12 @@ struct Vec<kBF16, kF32> {
 // chunk table of (N, L): chunk c covers [c*base, c*base + len_c)
 // --------------------------------------------------------------------------
 
-__device__ __forceinline__ int chunk_of(unsigned long long i, unsigned long long base, int L) {
-  if (base == 0) return L - 1;  // N < L: chunks 0..L-2 are empty
-  unsigned long long c = i / base;
-  return c >= (unsigned long long)(L - 1) ? L - 1 : (int)c;
+// The chunk holding element i (p.base = floor(N / L); the quotient through the
+// launch's precomputed divisor, see ChunkDivisor).
+__device__ __forceinline__ int chunk_of(const RingParams &p, unsigned long long i) {
+  if (p.base == 0) return p.L - 1;  // N < L: chunks 0..L-2 are empty
+  const unsigned long long c = divide_by_chunk(i, p.div_magic, p.div_shift1, p.div_shift2);
+  return c >= (unsigned long long)(p.L - 1) ? p.L - 1 : (int)c;
 }
 
 __device__ __forceinline__ unsigned long long chunk_end(int c, unsigned long long base, int L,

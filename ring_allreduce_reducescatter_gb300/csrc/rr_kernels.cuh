@@ -144,29 +144,10 @@ __device__ __forceinline__ void bulk_store_out(const RingParams &p, int r, unsig
 // ai6s.net/6a0dd5b5662f9a54cb75ef90.html, TpAllReduceOp::Execute)
 // --------------------------------------------------------------------------
 
-// The chunk of global element i through a one-entry cache of the chunk last
-// looked up: a direct-path thread's vectors advance by a fixed stride, so the
-// 64-bit division of chunk_of runs only when one leaves the cached chunk.
-// [lo, hi) is the cached chunk's index range (the last chunk's reaches the
-// end of the index space, as chunk_of clamps); lo == hi is empty.
-struct ChunkCache {
-  unsigned long long lo = 0, hi = 0;
-  int c = 0;
-};
-
-__device__ __forceinline__ int cached_chunk(ChunkCache &cc, const RingParams &p, unsigned long long i) {
-  if (i - cc.lo < cc.hi - cc.lo) return cc.c;  // lo <= i < hi
-  const int c = chunk_of(i, p.base, p.L);
-  cc.c = c;
-  cc.lo = (unsigned long long)c * p.base;
-  cc.hi = c == p.L - 1 ? ~0ull : (unsigned long long)(c + 1) * p.base;
-  return c;
-}
-
 // Naive (Reduce + Broadcast): the collector adds ranks 0, 1, ..., R-1 in order,
 // which is the ring fold started at rank 0 for every element.
 __device__ __forceinline__ int start_rank(const RingParams &p, unsigned long long global_index) {
-  return p.algo == kAlgoNaive ? 0 : chunk_of(global_index, p.base, p.L);
+  return p.algo == kAlgoNaive ? 0 : chunk_of(p, global_index);
 }
 
 __host__ __device__ constexpr int bit_reverse(int u, int bits) {
@@ -332,7 +313,7 @@ __device__ __noinline__ uint4 fold_ragged_smem(const RingParams &p, const unsign
   S res[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) {
-    const int c = chunk_of(i0 + e, p.base, L);
+    const int c = chunk_of(p, i0 + e);
     const uint32_t eo = off + (uint32_t)(e * sizeof(S));
     typename SC::W total;
     for (int g = 0; g < p.G; ++g) {
@@ -389,8 +370,8 @@ __device__ __forceinline__ void compute_tile(const RingParams &p, unsigned char 
     int c = c_first, c1 = c_last;
     if (c != c1) {
       const unsigned long long i0 = g0 + (unsigned long long)v * V;
-      c = chunk_of(i0, p.base, L);
-      c1 = chunk_of(i0 + V - 1, p.base, L);
+      c = chunk_of(p, i0);
+      c1 = chunk_of(p, i0 + V - 1);
     }
     uint4 res;
     if (c == c1)
@@ -415,7 +396,7 @@ __device__ __forceinline__ void issue_loads(const RingParams &p, unsigned char *
     for (int r = 0; r < p.R; ++r) bulk_load_in<false, E>(p, r, t0 * E, stage + (size_t)r * slot_bytes, bytes, bar, pol);
   } else {
     mbar_arrive_expect_tx(bar, bytes);
-    const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
+    const int c_lo = chunk_of(p, t0), c_hi = chunk_of(p, t1 - 1);
     for (int c = c_lo; c <= c_hi; ++c) {
       const unsigned long long off = (unsigned long long)c * p.base;
       const unsigned long long end = chunk_end(c, p.base, p.L, p.total);
@@ -436,7 +417,7 @@ __device__ __forceinline__ void issue_stores(const RingParams &p, const unsigned
   if (OP != kOpReduceScatter) {
     for (int r = 0; r < p.R; ++r) bulk_store_out<false, E>(p, r, t0 * E, stage, bytes, pol);
   } else {
-    const int c_lo = chunk_of(t0, p.base, p.L), c_hi = chunk_of(t1 - 1, p.base, p.L);
+    const int c_lo = chunk_of(p, t0), c_hi = chunk_of(p, t1 - 1);
     for (int c = c_lo; c <= c_hi; ++c) {
       const unsigned long long off = (unsigned long long)c * p.base;
       const unsigned long long end = chunk_end(c, p.base, p.L, p.total);
@@ -628,8 +609,8 @@ __device__ __forceinline__ void prefetch_vectors(const RingParams &p, unsigned l
     if (v >= nvec) break;
     if constexpr (OP == kOpAllGather) {
       const unsigned long long g0 = v * V;
-      const int c = chunk_of(g0, p.base, p.L);
-      if (c == chunk_of(g0 + V - 1, p.base, p.L)) prefetch_in<true, E>(p, c, (g0 - (unsigned long long)c * p.base) * E);
+      const int c = chunk_of(p, g0);
+      if (c == chunk_of(p, g0 + V - 1)) prefetch_in<true, E>(p, c, (g0 - (unsigned long long)c * p.base) * E);
     } else {
       for (int r = 0; r < p.R; ++r) prefetch_in<false, E>(p, r, v * 16);
     }
@@ -658,7 +639,6 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
       return;
     }
   }
-  ChunkCache cc;
   const bool naive = p.algo == kAlgoNaive;
   for (unsigned long long v0 = first_v; v0 < nvec; v0 += T * U) {
     if (p.prefetch & kPrefetchAhead) prefetch_vectors<OP, DT, U>(p, v0 + T * U, T, nvec);
@@ -672,8 +652,8 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         live[k] = v < nvec;
         if (!live[k]) continue;
         const unsigned long long i0 = v * V, g0 = p.first + i0;
-        const int c = cached_chunk(cc, p, g0);
-        if (g0 + V - 1 >= cc.hi) {  // over a chunk boundary: element by element
+        const int c = chunk_of(p, g0);
+        if (c != chunk_of(p, g0 + V - 1)) {  // over a chunk boundary: element by element
           for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, i0 + e);
           live[k] = false;
           continue;
@@ -698,8 +678,8 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         c[k] = 0;
         if (live[k] && !naive) {  // the naive order starts every element at rank 0
           const unsigned long long g0 = p.first + v * V;
-          c[k] = cached_chunk(cc, p, g0);
-          if (g0 + V - 1 >= cc.hi) {  // straddles a chunk boundary
+          c[k] = chunk_of(p, g0);
+          if (c[k] != chunk_of(p, g0 + V - 1)) {  // straddles a chunk boundary
             if (!p.straddle_cta)
               for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
             live[k] = false;
@@ -942,11 +922,11 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
         live[k] = v < nvec;
         if (!live[k]) continue;
         const unsigned long long gs = v * V;
-        const int c = chunk_of(gs, base, L);
+        const int c = chunk_of(p, gs);
         const unsigned long long o = gs - (unsigned long long)c * base;  // offset in chunk c's buffer
         const unsigned long long oa = o / V * V, len = chunk_end(c, base, L, N) - (unsigned long long)c * base;
         sh[k] = (int)(o - oa) * E;
-        if (c != chunk_of(gs + V - 1, base, L) || (sh[k] != 0 && oa + 2 * V > len)) {
+        if (c != chunk_of(p, gs + V - 1) || (sh[k] != 0 && oa + 2 * V > len)) {
           for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, gs + e);
           live[k] = false;
           continue;

@@ -315,7 +315,8 @@ def test_planner_paths(L):
     # the measured choice between the two aligned paths
     assert plan_dev(L, AR, 8, 1 << 28, F16)[1]["path"] == DIRECT
     assert plan_dev(L, AR, 32, 1 << 20, F16)[1]["path"] == DIRECT
-    assert plan_dev(L, AR, 2, 1 << 28, F16)[1]["path"] == BULK
+    assert plan_dev(L, AR, 2, 1 << 28, F16)[1]["path"] == DIRECT
+    assert plan_dev(L, RS, 2, 1 << 28, F16)[1]["path"] == DIRECT
     for R in (3, 4, 5, 6, 7, 9, 12, 24, 32):
         assert plan_dev(L, AR, R, 1 << 26, F32)[1]["path"] == DIRECT
     assert plan_dev(L, AR, 16, 1 << 22, F32)[1]["path"] == DIRECT     # 16 MiB per rank
@@ -573,13 +574,14 @@ def test_forced_vectors_and_register_budget(L):
 
 def test_planner_vectors_for_few_ranks(L):
     """The measured choices of vectors (rows) a thread: ReduceScatter over three
-    ranks two vectors at three CTAs per SM; AllGather over two ranks two
-    vectors; the shifted ReduceScatter 4 rows for two ranks, 3 for three from
-    64 MiB per rank, else 2; the shifted AllGather 2."""
+    ranks two vectors at three CTAs per SM; AllGather one vector (the L2
+    prefetch keeps its loads in flight); the shifted ReduceScatter 4 rows for
+    two ranks, 3 for three from 64 MiB per rank, else 2; the shifted
+    AllGather 2."""
     st, ch, _, _ = plan_dev(L, RS, 3, 3 * (1 << 22), F32)
     assert st == OK and ch["path"] == 3 and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
     st, ch, _, _ = plan_dev(L, AG, 2, 2 * (1 << 22), F32)
-    assert st == OK and ch["path"] == 3 and ch["vectors"] == 2
+    assert st == OK and ch["path"] == 3 and ch["vectors"] == 1
     for R, n, rows in ((2, 100_000, 4), (3, 100_000, 2), (3, 2_000_000, 3), (4, 100_000, 2), (8, 100_000, 2),
                        (16, 100_000, 2)):
         st, ch, _, _ = plan_dev(L, RS, R, R * (8 * n + 3), F16)
@@ -601,3 +603,51 @@ def test_beside_compute_caps_the_grid(L):
     assert st == OK and grid == 40
     st, ch, grid, _ = plan_dev(L, AR, 8, 1 << 26, F16)
     assert st == OK and ch["beside_compute"] == 0 and grid == GB300["sms"] * 16
+
+
+def test_chunk_divisor_is_exact(tmp_path):
+    """The kernels find an element's chunk (its ring start rank) by dividing
+    its index by the chunk length with a multiply and shifts; the quotient
+    must be exact for every 64-bit index.  Compiled for the host from the
+    library's own header and checked against the exact quotient."""
+    import shutil
+    import subprocess
+
+    cuda_inc = next((d for d in ("/usr/local/cuda/include",) if os.path.exists(os.path.join(d, "cuda_runtime.h"))),
+                    None)
+    if cuda_inc is None or shutil.which("g++") is None:
+        pytest.skip("needs g++ and the CUDA runtime headers")
+    exe = tmp_path / "chunk_divisor_check"
+    csrc = os.path.join(ROOT, "ring_allreduce_reducescatter_gb300", "csrc")
+    subprocess.run(["g++", "-O2", "-std=c++17", "-I", cuda_inc, "-I", os.path.join(ROOT, "include"), "-I", csrc,
+                    os.path.join(ROOT, "tests", "csrc", "chunk_divisor_check.cpp"), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout
+    checked = int(out.stdout.split()[-3])
+    assert checked > 500_000, out.stdout
+
+
+def test_planner_prefetch_policy(L):
+    """L2 prefetch by size and ranks: before the launch wait below 64 MiB per
+    rank or for up to four ranks a group; one iteration ahead for two ranks,
+    AllGather, ReduceScatter over three ranks, and 8-64 MiB messages other
+    than ReduceScatter over five or more ranks; never on the shifted or
+    halving-doubling kernels (prefetch reported as 1 + the bits)."""
+    MiB = 1 << 20
+    def pf(op, R, mib, dt=F16, E=2, **kw):
+        st, ch, _, _ = plan_dev(L, op, R, R * (mib * MiB // E // R // 8 * 8), dt, **kw)
+        assert st == OK and ch["path"] == 3, (op, R, mib, ch)
+        return ch["prefetch"] - 1
+    HEAD, AHEAD = 1, 2
+    assert pf(AR, 8, 1) == HEAD
+    assert pf(AR, 8, 16) == HEAD | AHEAD
+    assert pf(AR, 8, 256) == 0
+    assert pf(AR, 4, 256) == HEAD
+    assert pf(AR, 2, 256) == HEAD | AHEAD
+    assert pf(RS, 8, 16) == HEAD
+    assert pf(RS, 3, 256) == HEAD | AHEAD
+    assert pf(AG, 8, 256) == AHEAD
+    assert pf(AR, 4, 4, F32, 4) == HEAD
+    assert pf(AR, 16, 64, group=8) == 0
+    st, ch, _, _ = plan_dev(L, RS, 8, 8 * 1001, F16)  # shifted
+    assert st == OK and ch["prefetch"] == 1

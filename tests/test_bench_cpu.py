@@ -128,3 +128,21 @@ def test_replica_launch_command():
     assert cmd[1:3] == ["-m", "torch.distributed.run"]
     assert "--nproc-per-node=4" in cmd and "--master-addr=127.0.0.1" in cmd and "--master-port=29511" in cmd
     assert cmd[-4:] == ["--gpus", "4", "--steps", "5"] and cmd[-5].endswith("bench.py")
+
+
+def test_path_choice_table_marks_the_planner():
+    """The sweep's table lists both paths per point and whether the planner's
+    pick is within 5 % of the faster."""
+    def row(variant, path, us, R=4):
+        return {"op": "allreduce", "R": R, "count": 1 << 20, "msg_bytes": 2 << 20, "off_grid": False,
+                "variant": variant, "path": path, "us": us}
+
+    rows = [row("auto", "direct", 10.0), row("bulk", "bulk", 12.0), row("direct", "direct", 10.0),
+            row("auto", "bulk", 20.0, R=2), row("bulk", "bulk", 20.0, R=2), row("direct", "direct", 15.0, R=2)]
+    args = type("A", (), dict(sweep_ops="ar", sweep_ranks="2,4", sweep_mib="2", sweep_dtype="f16", sweep_layouts=1,
+                              sweep_off_grid="no"))()
+    text = bench.path_choice_table(rows, args)
+    lines = [ln for ln in text.splitlines() if ln.startswith("| allreduce")]
+    assert lines[0].split("|")[6:10] == [" 12.0 ", " 10.0 ", " direct ", " yes "]
+    assert lines[1].split("|")[6:10] == [" 20.0 ", " 15.0 ", " bulk ", " NO "]
+    assert "--sweep-table FILE" in text
