@@ -540,9 +540,9 @@ def overlap_row(rr, wl, dev, pieces=8, max_ctas=0, beside_compute=0):
 
     t_comp, t_comm, t_both = timed(compute_only), timed(comm_only), timed(both)
     hidden = (t_comp + t_comm - t_both) / min(t_comp, t_comm)
+    grid = rr.plan(rr.OP_ALLREDUCE, [x[:step] for x in xs], [o[:step] for o in outs], step, cfg=cfg)["max_ctas"]
     del xs, outs, A, B, C
     torch.cuda.empty_cache()
-    grid = rr.plan(rr.OP_ALLREDUCE, [x[:step] for x in xs], [o[:step] for o in outs], step, cfg=cfg)["max_ctas"]
     return {"what": f"{pieces} bf16 GEMMs {n}^3 on a compute stream; after each, one of {pieces} ranges of the "
                     f"512 MiB R=8 fp16 AllReduce on a communication stream", "max_ctas": max_ctas,
             "beside_compute": beside_compute, "allreduce_grid": grid,

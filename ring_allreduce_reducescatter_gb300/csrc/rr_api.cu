@@ -328,7 +328,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
         pf |= rr::kPrefetchAhead;
       p->prefetch = c.prefetch ? c.prefetch - 1 : pf;
     }
-    if (p->shifted || ck.algo == RR_ALGO_HALVING_DOUBLING) p->prefetch = 0;
+    if (ck.algo == RR_ALGO_HALVING_DOUBLING || (p->shifted && c.prefetch == 0)) p->prefetch = 0;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
     // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5
     // 0.88 -> 0.98, R = 9 0.93 -> 0.99, R = 3 0.85 -> 0.96).  A grid that

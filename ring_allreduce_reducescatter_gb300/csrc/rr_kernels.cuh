@@ -745,8 +745,6 @@ __global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long li
 // (AllGather over more ranks); more rows keep more loads in flight.
 template <int OP, int DT, int WT, int US>
 __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_kernel(const __grid_constant__ RingParams p) {
-  grid_dependency_wait();
-  grid_dependents_launch();
   using VT = Vec<DT, WT>;
   using W = typename VT::W;
   constexpr int V = VT::V;
@@ -772,9 +770,8 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     const unsigned long long ipc = (base / V + per_item - 1) / per_item;      // items in chunks 0..L-2
     const unsigned long long ipl = (len_last / V + per_item - 1) / per_item;  // items in the last chunk
     const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
-    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
-      int c;
-      unsigned long long item;
+    // work item w: its chunk and its index among the chunk's items
+    auto locate = [&](unsigned long long w, int &c, unsigned long long &item) {
       if (w < (unsigned long long)(L - 1) * ipc) {
         c = (int)(w / ipc);
         item = w - (unsigned long long)c * ipc;
@@ -782,6 +779,30 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
         c = L - 1;
         item = w - (unsigned long long)(L - 1) * ipc;
       }
+    };
+    // L2 prefetch of the blocks lane `lane` loads for item w
+    auto prefetch_item = [&](unsigned long long w) {
+      if (w >= n_items) return;
+      int c;
+      unsigned long long item;
+      locate(w, c, item);
+      const unsigned long long len = c < L - 1 ? base : len_last, nv = len / V, g0 = (unsigned long long)c * base;
+      const unsigned long long shift = g0 % V;
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const unsigned long long u = item * per_item + 31ull * k + lane, ga = g0 + u * V - shift;
+        if (u <= nv && ga + V <= N)
+          for (int r = 0; r < L; ++r) prefetch_in<false, E>(p, r, ga * E);
+      }
+    };
+    if (p.prefetch & kPrefetchHead) prefetch_item(warp);
+    grid_dependency_wait();
+    grid_dependents_launch();
+    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
+      if (p.prefetch & kPrefetchAhead) prefetch_item(w + n_warps);
+      int c;
+      unsigned long long item;
+      locate(w, c, item);
       const unsigned long long len = c < L - 1 ? base : len_last, nv = len / V, g0 = (unsigned long long)c * base;
       const int shift = (int)(g0 % V);  // elements
       const int sh = shift * E;         // bytes
@@ -855,9 +876,7 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     const unsigned long long rpc = (base / V + 64) / 32, rpl = (len_last / V + 64) / 32;  // rows per chunk, at most
     const unsigned long long ipc = (rpc + US - 1) / US, ipl = (rpl + US - 1) / US;        // items per chunk
     const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
-    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
-      int c;
-      unsigned long long item;
+    auto locate = [&](unsigned long long w, int &c, unsigned long long &item) {
       if (w < (unsigned long long)(L - 1) * ipc) {
         c = (int)(w / ipc);
         item = w - (unsigned long long)c * ipc;
@@ -865,6 +884,33 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
         c = L - 1;
         item = w - (unsigned long long)(L - 1) * ipc;
       }
+    };
+    // L2 prefetch of the source block lane `lane` loads for item w
+    auto prefetch_item = [&](unsigned long long w) {
+      if (w >= n_items) return;
+      int c;
+      unsigned long long item;
+      locate(w, c, item);
+      const unsigned long long cb = (unsigned long long)c * base, len = c < L - 1 ? base : len_last;
+      const unsigned long long vf = (cb + V - 1) / V;
+      const unsigned long long ve = (cb + len) / V < nvec ? (cb + len) / V : nvec;
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const unsigned long long v = (vf / 32 + item * US + k) * 32 + lane;
+        if (v >= vf && v <= ve) {
+          const unsigned long long o = v * V - cb, oa = o - (o % V);
+          if (oa + V <= len) prefetch_in<true, E>(p, c, oa * E);
+        }
+      }
+    };
+    if (p.prefetch & kPrefetchHead) prefetch_item(warp);
+    grid_dependency_wait();
+    grid_dependents_launch();
+    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
+      if (p.prefetch & kPrefetchAhead) prefetch_item(w + n_warps);
+      int c;
+      unsigned long long item;
+      locate(w, c, item);
       const unsigned long long cb = (unsigned long long)c * base, len = c < L - 1 ? base : len_last;
       const unsigned long long vf = (cb + V - 1) / V;  // first output vector wholly in the chunk
       const unsigned long long ve = (cb + len) / V < nvec ? (cb + len) / V : nvec;  // one past the last
@@ -912,7 +958,23 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     // builds each from the two aligned blocks of its chunk's input under it
     // (the second served by L1); all loads before the stores
     const unsigned long long nvec = p.n_bulk / V;
+    // L2 prefetch of the lower source blocks of vectors v0, v0 + T, ...
+    auto prefetch_vecs = [&](unsigned long long v0) {
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const unsigned long long v = v0 + (unsigned long long)k * T;
+        if (v >= nvec) break;
+        const unsigned long long gs = v * V;
+        const int c = chunk_of(p, gs);
+        const unsigned long long o = gs - (unsigned long long)c * base, oa = o / V * V;
+        if (oa + V <= chunk_end(c, base, L, N) - (unsigned long long)c * base) prefetch_in<true, E>(p, c, oa * E);
+      }
+    };
+    if (p.prefetch & kPrefetchHead) prefetch_vecs(tid);
+    grid_dependency_wait();
+    grid_dependents_launch();
     for (unsigned long long v0 = tid; v0 < nvec; v0 += T * US) {
+      if (p.prefetch & kPrefetchAhead) prefetch_vecs(v0 + T * US);
       uint4 lo[US], hi[US];
       int sh[US];
       bool live[US];
