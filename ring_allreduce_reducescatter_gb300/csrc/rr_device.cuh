@@ -236,11 +236,10 @@ struct Vec<kBF16, kF32> {
 // chunk table of (N, L): chunk c covers [c*base, c*base + len_c)
 // --------------------------------------------------------------------------
 
-// The chunk holding element i (p.base = floor(N / L); the quotient through the
-// launch's precomputed divisor, see ChunkDivisor).
+// The chunk holding element i (p.base = floor(N / L)).
 __device__ __forceinline__ int chunk_of(const RingParams &p, unsigned long long i) {
   if (p.base == 0) return p.L - 1;  // N < L: chunks 0..L-2 are empty
-  const unsigned long long c = divide_by_chunk(i, p.div_magic, p.div_shift1, p.div_shift2);
+  const unsigned long long c = i / p.base;
   return c >= (unsigned long long)(p.L - 1) ? p.L - 1 : (int)c;
 }
 

@@ -48,44 +48,9 @@ struct RingParams {
   int shifted;                    // direct ReduceScatter / AllGather: chunk boundaries off the 16-byte grid
   int prefetch;                   // direct path: kPrefetch* bits
   unsigned long long debug_margin;  // debug build: bytes taken off every buffer's extent by the checks
-  unsigned long long div_magic;   // i / base as a multiply and shifts (ChunkDivisor)
-  int div_shift1, div_shift2;
+  int chunks_on_grid;             // every chunk boundary of this launch falls on the 16-byte vector grid
+  int head_span;                  // direct path, kPrefetchHead: CTAs resident at once (0: own vectors only)
 };
-
-// Division of 64-bit indices by the invariant chunk length `base` (>= 1) as a
-// high multiply and two shifts: the round-up method of T. Granlund and P.
-// Montgomery, "Division by Invariant Integers using Multiplication" (PLDI
-// 1994).  With l = ceil(log2 d) and m = floor(2^64 (2^l - d) / d) + 1 (a
-// 64-bit value since 2^l - d < d), t = floor(m n / 2^64) gives
-// floor(n / d) = (t + ((n - t) >> 1)) >> (l - 1) for every 64-bit n (l >= 1);
-// d = 1 takes m = 1, t = 0 and shifts 0, 0.  Exact, so the chunk of every
-// element is the one the chunk table defines.
-struct ChunkDivisor {
-  unsigned long long magic;
-  int shift1, shift2;
-};
-
-inline ChunkDivisor make_chunk_divisor(unsigned long long d) {
-  int l = 0;
-  while (l < 64 && (1ull << l) < d) ++l;
-  const unsigned __int128 two_l = (unsigned __int128)1 << l;
-  const unsigned __int128 m = ((two_l - d) << 64) / d + 1;
-  return ChunkDivisor{(unsigned long long)m, l > 0 ? 1 : 0, l > 0 ? l - 1 : 0};
-}
-
-__host__ __device__ __forceinline__ unsigned long long mul_high_u64(unsigned long long a, unsigned long long b) {
-#ifdef __CUDA_ARCH__
-  return __umul64hi(a, b);
-#else
-  return (unsigned long long)(((unsigned __int128)a * b) >> 64);
-#endif
-}
-
-__host__ __device__ __forceinline__ unsigned long long divide_by_chunk(unsigned long long n, unsigned long long magic,
-                                                                       int shift1, int shift2) {
-  const unsigned long long t = mul_high_u64(magic, n);
-  return (t + ((n - t) >> shift1)) >> shift2;
-}
 
 // L2 prefetch of the direct path's inputs (no data reaches the SM, so no
 // registers are held): kPrefetchHead, a thread's first vectors before the
