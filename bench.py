@@ -120,7 +120,10 @@ def recorded_traffic(digest):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples (200 ms) with host timestamps."""
+    """nvidia-smi clock / throttle samples (every PERIOD_MS) with host
+    timestamps; short timed regions (tens of milliseconds) still get samples."""
+
+    PERIOD_MS = 25
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -132,7 +135,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
@@ -473,13 +476,17 @@ def host_link_speeds(dev, host_in, host_out, dev_src):
             "h2d_gbs": round(nbytes / h / 1e6, 1), "d2h_gbs": round(nbytes / d / 1e6, 1)}
 
 
-def overlap_row(rr, wl, dev, pieces=8, max_ctas=0, beside_compute=0):
+def overlap_rows(rr, wl, dev, pieces=8, rounds=5):
     """Chunked AllReduce overlapped with compute (the pattern of the page
     bjdmk.com.cn/news/5966809, sections 4.2-4.3): `pieces` bf16 GEMMs run on the
     compute stream; after each one an event releases one range of a 512 MiB
-    fp16 AllReduce (R = 8) on a communication stream.  Reports the two
-    streams alone and together (median of 5 runs each); the AllReduce's grid
-    is uncapped, capped at max_ctas, or capped by the library (beside_compute)."""
+    fp16 AllReduce (R = 8) on a communication stream.  For each grid setting
+    of the AllReduce (uncapped; capped at a share of the SMs; the library's
+    own cap, beside_compute) the two streams are timed alone and together;
+    the settings take turns over `rounds` rounds and each row reports medians.
+    On one GPU the "communication" is itself HBM traffic that SMs drive, so
+    the figure of merit is the time together against the time one after the
+    other."""
     import torch
 
     w = wl.config2(512)
@@ -492,25 +499,27 @@ def overlap_row(rr, wl, dev, pieces=8, max_ctas=0, beside_compute=0):
     C = torch.empty(n, n, device=dev, dtype=torch.bfloat16)
     comp, comm = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     evs = [torch.cuda.Event() for _ in range(pieces)]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    settings = [("uncapped", rr.LaunchCfg())]
+    for eighths in (7, 6, 5, 4, 3):
+        settings.append((f"max_ctas={sms * eighths // 8}", rr.LaunchCfg(0, 0, 0, 0, 0, sms * eighths // 8)))
+    settings.append(("beside_compute", rr.LaunchCfg(0, 0, 0, 0, 0, 0, 0, 0, 1)))
 
     def ranges(k):
         a = k * step
-        b = min(N, a + step)
-        return a, b
+        return a, min(N, a + step)
 
-    def compute_only():
+    def compute_only(cfg):
         with torch.cuda.stream(comp):
             for _ in range(pieces):
                 torch.matmul(A, B, out=C)
 
-    cfg = rr.LaunchCfg(0, 0, 0, 0, 0, max_ctas, 0, 0, beside_compute)
-
-    def comm_only():
+    def comm_only(cfg):
         for k in range(pieces):
             a, b = ranges(k)
             rr.allreduce_range([x[a:b] for x in xs], [o[a:b] for o in outs], N, a, stream=comm, cfg=cfg)
 
-    def both():
+    def both(cfg):
         for k in range(pieces):
             with torch.cuda.stream(comp):
                 torch.matmul(A, B, out=C)
@@ -519,36 +528,42 @@ def overlap_row(rr, wl, dev, pieces=8, max_ctas=0, beside_compute=0):
             a, b = ranges(k)
             rr.allreduce_range([x[a:b] for x in xs], [o[a:b] for o in outs], N, a, stream=comm, cfg=cfg)
 
-    def timed(fn):
-        fn()
+    def timed(fn, cfg):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        t0.record(cur)
+        comp.wait_stream(cur)
+        comm.wait_stream(cur)
+        fn(cfg)
+        cur.wait_stream(comp)
+        cur.wait_stream(comm)
+        t1.record(cur)
         torch.cuda.synchronize(dev)
-        runs = []
-        for _ in range(5):
-            t0 = torch.cuda.Event(enable_timing=True)
-            t1 = torch.cuda.Event(enable_timing=True)
-            cur = torch.cuda.current_stream(dev)
-            t0.record(cur)
-            comp.wait_stream(cur)
-            comm.wait_stream(cur)
-            fn()
-            cur.wait_stream(comp)
-            cur.wait_stream(comm)
-            t1.record(cur)
-            torch.cuda.synchronize(dev)
-            runs.append(t0.elapsed_time(t1))
-        return statistics.median(runs)
+        return t0.elapsed_time(t1)
 
-    t_comp, t_comm, t_both = timed(compute_only), timed(comm_only), timed(both)
-    hidden = (t_comp + t_comm - t_both) / min(t_comp, t_comm)
-    grid = rr.plan(rr.OP_ALLREDUCE, [x[:step] for x in xs], [o[:step] for o in outs], step, cfg=cfg)["max_ctas"]
+    for _, cfg in settings:  # warm up every setting
+        timed(both, cfg)
+    times = {name: {"compute": [], "allreduce": [], "together": []} for name, _ in settings}
+    for _ in range(rounds):
+        for name, cfg in settings:
+            times[name]["compute"].append(timed(compute_only, cfg))
+            times[name]["allreduce"].append(timed(comm_only, cfg))
+            times[name]["together"].append(timed(both, cfg))
+    rows = []
+    for name, cfg in settings:
+        t = {k: statistics.median(v) for k, v in times[name].items()}
+        serial = t["compute"] + t["allreduce"]
+        grid = rr.plan(rr.OP_ALLREDUCE, [x[:step] for x in xs], [o[:step] for o in outs], step, cfg=cfg)["max_ctas"]
+        rows.append({"what": f"{pieces} bf16 GEMMs {n}^3 on a compute stream; after each, one of {pieces} ranges "
+                             f"of the 512 MiB R=8 fp16 AllReduce on a communication stream", "setting": name,
+                     "allreduce_grid": grid, "compute_ms": round(t["compute"], 3),
+                     "allreduce_ms": round(t["allreduce"], 3), "together_ms": round(t["together"], 3),
+                     "serial_ms": round(serial, 3), "saved_of_serial": round((serial - t["together"]) / serial, 3),
+                     "rounds": rounds})
     del xs, outs, A, B, C
     torch.cuda.empty_cache()
-    return {"what": f"{pieces} bf16 GEMMs {n}^3 on a compute stream; after each, one of {pieces} ranges of the "
-                    f"512 MiB R=8 fp16 AllReduce on a communication stream", "max_ctas": max_ctas,
-            "beside_compute": beside_compute, "allreduce_grid": grid,
-            "compute_ms": round(t_comp, 3),
-            "allreduce_ms": round(t_comm, 3), "together_ms": round(t_both, 3),
-            "serial_ms": round(t_comp + t_comm, 3), "fraction_of_shorter_hidden": round(hidden, 3)}
+    return rows
 
 
 # --------------------------------------------------------------------------
@@ -666,8 +681,7 @@ def run_ours(args):
                         for off in (False, True):
                             rsag.extend(path_sweep_point(rr, dev, l2_bytes, peak, op_, R_, mib, torch.float16, None,
                                                          off, False, only_auto=True))
-            overlap = [overlap_row(rr, wl, dev, max_ctas=m) for m in (0, 128, 96, 64)]
-            overlap.append(overlap_row(rr, wl, dev, beside_compute=1))
+            overlap = overlap_rows(rr, wl, dev)
             xs, outs = staggered_inputs(rr, wl, w, dev)
         else:
             outs = rr.rank_buffers(R, N, torch.float16, dev)
@@ -982,6 +996,8 @@ def main():
     ap.add_argument("--no-workloads", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap-only", action="store_true",
+                    help="print only the compute-overlap table (JSON lines) of the chunked AllReduce")
     ap.add_argument("--path-sweep", action="store_true",
                     help="time the planner's choice against the forced tile pipeline and direct path instead")
     ap.add_argument("--sweep-ops", default="ar,rs,ag")
@@ -1005,7 +1021,20 @@ def main():
         ap.error(f"--gpus {args.gpus} but the launcher started WORLD_SIZE={os.environ['WORLD_SIZE']} ranks")
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
-    if args.path_sweep:
+    if args.overlap_only:
+        import torch
+
+        import __graft_entry__
+
+        __graft_entry__.build()
+        import ring_allreduce_reducescatter_gb300 as rr
+        from ring_allreduce_reducescatter_gb300 import workloads as wl
+
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        for row in overlap_rows(rr, wl, dev):
+            print(json.dumps(row), flush=True)
+    elif args.path_sweep:
         run_path_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

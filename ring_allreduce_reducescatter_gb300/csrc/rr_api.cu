@@ -396,18 +396,6 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
                           ? 1
                           : 0;
     l->grid = capped((int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap));
-    // The head prefetch of a small message (inputs of at most 64 MiB, half the
-    // L2) also covers the CTAs of later waves: the span is the number of CTAs
-    // resident at once (registers: OCC 256-thread CTAs' worth per SM).
-    {
-      const unsigned long long in_bytes = (ck.op == RR_OP_ALLGATHER ? 1ull : (unsigned long long)ck.R) * N * E;
-      const unsigned long long resident =
-          (unsigned long long)sms * (unsigned long long)l->direct_occ * (256ull / (unsigned long long)l->threads);
-      p->head_span = ((p->prefetch & rr::kPrefetchHead) && !p->shifted && in_bytes <= (64ull << 20) &&
-                      resident < (unsigned long long)l->grid)
-                         ? (int)resident
-                         : 0;
-    }
     if (p->straddle_cta) {
       if (!(c.max_ctas > 0 && l->grid >= c.max_ctas))
         l->grid += 1;                      // one more CTA

@@ -651,15 +651,7 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
   const unsigned long long T = (unsigned long long)(gridDim.x - p.straddle_cta) * blockDim.x;
   const unsigned long long first_v = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
   const bool main_cta = !(OP == kOpAllReduce && p.straddle_cta && blockIdx.x == gridDim.x - 1);
-  if ((p.prefetch & kPrefetchHead) && main_cta) {
-    prefetch_vectors<OP, DT, U>(p, first_v, T, nvec);
-    // small messages: also the first vectors of the CTAs that will take this
-    // CTA's place in later waves (blockIdx.x + span, + 2 span, ...), so the
-    // whole input is on its way to L2 from the start
-    if (p.head_span > 0)
-      for (unsigned long long b = blockIdx.x + p.head_span; b < gridDim.x - p.straddle_cta; b += p.head_span)
-        prefetch_vectors<OP, DT, U>(p, b * blockDim.x + threadIdx.x, T, nvec);
-  }
+  if ((p.prefetch & kPrefetchHead) && main_cta) prefetch_vectors<OP, DT, U>(p, first_v, T, nvec);
   // The next kernel may be scheduled at once: a large grid fills the SMs'
   // registers or thread slots, so its CTAs take SMs only as this grid's leave.
   grid_dependency_wait();
@@ -710,8 +702,10 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         c[k] = 0;
         if (live[k] && !naive) {  // the naive order starts every element at rank 0
           const unsigned long long g0 = p.first + v * V;
-          c[k] = cached_chunk(cc, p, g0);
-          if (!p.chunks_on_grid && g0 + V - 1 >= cc.hi) {  // straddles a chunk boundary
+          // one vector a thread (five or more ranks a group): the plain lookup
+          // measured faster than the cache, whose state costs registers
+          c[k] = U == 1 ? chunk_of(p, g0) : cached_chunk(cc, p, g0);
+          if (!p.chunks_on_grid && (U == 1 ? c[k] != chunk_of(p, g0 + V - 1) : g0 + V - 1 >= cc.hi)) {
             if (!p.straddle_cta)
               for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
             live[k] = false;
