@@ -771,9 +771,11 @@ def sweep_variants(rr, op, wide, shifted, all_variants, prefetch=False, explicit
     if explicit:
         out = [("auto", None)]
         for item in explicit.split(";"):
-            path, u, occ, pf = (int(v) for v in item.split(","))
-            out.append((f"path={path} U={u} occ={occ} prefetch={pf}",
-                        rr.LaunchCfg(path, 0, 0, occ, 0, 0, 0, u, 0, pf)))
+            vals = [int(v) for v in item.split(",")]
+            path, u, occ, pf = vals[:4]
+            cap = vals[4] if len(vals) > 4 else 0
+            out.append((f"path={path} U={u} occ={occ} prefetch={pf}" + (f" max_ctas={cap}" if cap else ""),
+                        rr.LaunchCfg(path, 0, 0, occ, 0, cap, 0, u, 0, pf)))
         return out
     if prefetch and not shifted:
         for pf, name in ((1, "none"), (2, "head"), (3, "ahead"), (4, "head+ahead")):
@@ -1012,7 +1014,8 @@ def main():
     ap.add_argument("--sweep-layouts", type=int, default=1, help="buffer layouts per point (median reported)")
     ap.add_argument("--sweep-table", default="", help="also write the tile-vs-direct table (markdown) to this file")
     ap.add_argument("--sweep-cfg", default="",
-                    help="explicit launch configurations 'path,vectors,ctas_per_sm,prefetch;...' (with auto)")
+                    help="explicit launch configurations 'path,vectors,ctas_per_sm,prefetch[,max_ctas];...' "
+                         "(with auto)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.gpus < 1:

@@ -191,11 +191,13 @@ typedef struct {
                       kernel (safe: a prefetch never changes what is read after
                       the wait); 3 the next iteration's vectors while the
                       current ones load; 4 both.  Ignored by the halving-
-                      doubling order and off-grid ReduceScatter / AllGather. */
+                      doubling order. */
 } rr_launch_cfg;
 
-/* Share of the SMs (numerator / 8) a call with beside_compute = 1 takes. */
-#define RR_BESIDE_COMPUTE_SM_EIGHTHS 5
+/* Share of the SMs (numerator / 8) a call with beside_compute = 1 takes
+ * (measured: eight binary16 GEMMs of 8192^3 with the ranges of a 512 MiB
+ * eight-rank AllReduce between them took least time together at 7/8). */
+#define RR_BESIDE_COMPUTE_SM_EIGHTHS 7
 
 /*
  * ring_collective -- every collective through one entry point with an

@@ -326,7 +326,13 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
         pf |= rr::kPrefetchAhead;
       p->prefetch = c.prefetch ? c.prefetch - 1 : pf;
     }
-    if (ck.algo == RR_ALGO_HALVING_DOUBLING || (p->shifted && c.prefetch == 0)) p->prefetch = 0;
+    // The shifted kernels: the AllGather prefetches its first work item and
+    // the next one (binary16, of the copy bandwidth: R = 2 at 256 MiB 0.80 ->
+    // 0.86, R = 8 at 16 MiB 0.83 -> 0.88); the ReduceScatter does not (one
+    // item ahead lost 10-17 %, the first item alone 0-1 % either way).
+    if (p->shifted && c.prefetch == 0)
+      p->prefetch = ck.op == RR_OP_ALLGATHER ? (rr::kPrefetchHead | rr::kPrefetchAhead) : 0;
+    if (ck.algo == RR_ALGO_HALVING_DOUBLING) p->prefetch = 0;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
     // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5
     // 0.88 -> 0.98, R = 9 0.93 -> 0.99, R = 3 0.85 -> 0.96).  A grid that

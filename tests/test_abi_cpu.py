@@ -609,8 +609,9 @@ def test_planner_prefetch_policy(L):
     """L2 prefetch by size and ranks: before the launch wait below 64 MiB per
     rank or for up to four ranks a group; one iteration ahead for two ranks,
     AllGather, ReduceScatter over three ranks, and 8-64 MiB messages other
-    than ReduceScatter over five or more ranks; never on the shifted or
-    halving-doubling kernels (prefetch reported as 1 + the bits)."""
+    than ReduceScatter over five or more ranks; never on the halving-doubling
+    kernels; the shifted AllGather both, the shifted ReduceScatter none
+    (prefetch reported as 1 + the bits)."""
     MiB = 1 << 20
     def pf(op, R, mib, dt=F16, E=2, **kw):
         st, ch, _, _ = plan_dev(L, op, R, R * (mib * MiB // E // R // 8 * 8), dt, **kw)
@@ -627,5 +628,32 @@ def test_planner_prefetch_policy(L):
     assert pf(AG, 8, 256) == AHEAD
     assert pf(AR, 4, 4, F32, 4) == HEAD
     assert pf(AR, 16, 64, group=8) == 0
-    st, ch, _, _ = plan_dev(L, RS, 8, 8 * 1001, F16)  # shifted
+    st, ch, _, _ = plan_dev(L, RS, 8, 8 * 1001, F16)  # shifted ReduceScatter: none
     assert st == OK and ch["prefetch"] == 1
+    st, ch, _, _ = plan_dev(L, AG, 8, 8 * 1001, F16)  # shifted AllGather: both
+    assert st == OK and ch["prefetch"] == 1 + (HEAD | AHEAD)
+
+
+def test_planner_matches_the_measured_path_table(L):
+    """The planner's choice between the tile pipeline and the direct path is
+    within 5 % of the faster one at every point of the committed sweep
+    (profiles/path_choice_sweep_f16.md, written by bench.py --path-sweep
+    --sweep-table on a GB300: AllReduce, ReduceScatter and AllGather over 2-32
+    ranks at 1-256 MiB per rank, binary16)."""
+    path = os.path.join(ROOT, "profiles", "path_choice_sweep_f16.md")
+    rows = []
+    with open(path) as f:
+        for line in f:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) == 9 and cells[0] in ("allreduce", "reduce_scatter", "allgather"):
+                rows.append(cells)
+    assert len(rows) >= 100
+    ops = {"allreduce": AR, "reduce_scatter": RS, "allgather": AG}
+    names = {1: "bulk", 3: "direct"}
+    for op, R, count, _, off, bulk, direct, _, _ in rows:
+        st, ch, _, _ = plan_dev(L, ops[op], int(R), int(count), F16)
+        assert st == OK and ch["path"] in names, (op, R, count, ch)
+        t = {"bulk": float(bulk) if bulk != "-" else None, "direct": float(direct)}
+        best = min(v for v in t.values() if v is not None)
+        mine = t[names[ch["path"]]]
+        assert mine is not None and mine <= 1.05 * best, (op, R, count, names[ch["path"]], t)
