@@ -781,11 +781,16 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
   const unsigned long long tid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
   if constexpr (OP == kOpReduceScatter) {
     // Chunk by chunk (the shift is the chunk's), each warp takes US rows of
-    // 31 consecutive output vectors: in a row, lane t loads the aligned block
-    // under vector t's start, which is also the upper block lane t - 1 needs
-    // (a shuffle); lane 31 only supplies that block.  A vector whose upper
-    // block would pass the end of the rank vectors goes element by element,
-    // and so do the elements past a chunk's last full vector.
+    // 31 consecutive output vectors.  In a row, lane t loads every rank's
+    // aligned block under output vector t's start and folds them as they are,
+    // in the ring order of the chunk (the fold is element-wise, and every
+    // element of the chunk starts at rank c; the block's elements outside the
+    // chunk are folded too and dropped); the folded block is also the upper
+    // half lane t - 1 needs, so one shuffle and one funnel shift of the
+    // result build each output vector, whatever R is.  Lane 31 only supplies
+    // its block.  A vector whose upper block would pass the end of the rank
+    // vectors goes element by element, and so do the elements past a chunk's
+    // last full vector.
     constexpr int NB = direct_batch_ranks(US);  // ranks per batch: 8 (US = 3: 9) loads in flight a lane
     const unsigned lane = threadIdx.x & 31u;
     const unsigned long long warp = tid >> 5, n_warps = T >> 5;
@@ -861,20 +866,19 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
 #pragma unroll
             for (int j = 0; j < NB; ++j)
               if (k0 + j < L) {
-                const uint4 next = make_uint4(__shfl_down_sync(0xffffffffu, blk[k][j].x, 1),
-                                              __shfl_down_sync(0xffffffffu, blk[k][j].y, 1),
-                                              __shfl_down_sync(0xffffffffu, blk[k][j].z, 1),
-                                              __shfl_down_sync(0xffffffffu, blk[k][j].w, 1));
-                const W x = VT::in(sh ? funnel16(blk[k][j], next, sh) : blk[k][j]);
+                const W x = VT::in(blk[k][j]);
                 acc[k] = (k0 + j == 0) ? x : VT::hop(acc[k], x);
               }
         }
 #pragma unroll
         for (int k = 0; k < US; ++k) {
+          const uint4 res = VT::out(acc[k]);  // the folded block under output vector u[k]'s start
+          const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, res.x, 1), __shfl_down_sync(0xffffffffu, res.y, 1),
+                                      __shfl_down_sync(0xffffffffu, res.z, 1), __shfl_down_sync(0xffffffffu, res.w, 1));
           if (tail[k]) {
             for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, g0 + u[k] * V + e);
           } else if (act[k]) {
-            store_out<true, E>(p, c, u[k] * V * E, VT::out(acc[k]));
+            store_out<true, E>(p, c, u[k] * V * E, sh ? funnel16(res, up, sh) : res);
           }
         }
       }
