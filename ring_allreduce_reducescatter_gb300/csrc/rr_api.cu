@@ -300,6 +300,21 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
         U = 2;
     }
     if (wide && U > 2) U = 2;
+    // Flat rings of up to four ranks under 32 MiB per rank (ring order,
+    // AllReduce / ReduceScatter, chunks on the grid): one wave of resident
+    // CTAs whose threads loop, with the L2 prefetch of the first and the next
+    // iteration, instead of several waves with a partial last one.  One vector
+    // a thread where two would leave SMs idle (under two vectors per thread of
+    // a wave of two 256-thread CTAs per SM); two CTAs per SM up to 8 MiB, three
+    // above.  Measured (binary16 unless stated, of the copy bandwidth, median of
+    // two buffer layouts): 1 MiB AllReduce R = 2 / 3 / 4 0.24 / 0.34 / 0.41 ->
+    // 0.29 / 0.40 / 0.48; 4 MiB AllReduce R = 4 binary32 0.67 -> 0.76,
+    // ReduceScatter 0.57 -> 0.60; 16 MiB AllReduce R = 2 / 3 0.78 / 0.91 ->
+    // 0.81 / 0.94, ReduceScatter R = 3 / 4 0.79 / 0.83 -> 0.87 / 0.92.
+    const unsigned long long vecs_here = n_bulk * E / 16;
+    const bool one_wave = ck.algo == RR_ALGO_RING && !p->shifted && ck.op != RR_OP_ALLGATHER && ck.L == ck.R &&
+                          ck.L <= 4 && msg_bytes < (32ull << 20) && !wide && c.max_ctas == 0;
+    if (one_wave) U = vecs_here < 2ull * 128ull * 4ull * (unsigned long long)sms ? 1 : 2;
     if (c.vectors) U = c.vectors;
     p->direct_u = U;
     // L2 prefetch (kPrefetch* bits; only the ring / naive kernels on 16-byte
@@ -324,6 +339,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
       if (small || ck.L <= 4) pf |= rr::kPrefetchHead;
       if (ck.R == 2 || ck.op == RR_OP_ALLGATHER || (ck.op == RR_OP_REDUCE_SCATTER && ck.L == 3) || (mid && !rs_many))
         pf |= rr::kPrefetchAhead;
+      if (one_wave) pf = rr::kPrefetchHead | rr::kPrefetchAhead;
       p->prefetch = c.prefetch ? c.prefetch - 1 : pf;
     }
     // The shifted kernels: the AllGather prefetches its first work item and
@@ -352,6 +368,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // 1.01 -> 0.99).
     if (ck.algo == RR_ALGO_HALVING_DOUBLING)
       l->direct_occ = (ck.R < 7 && looping && !wide) ? 3 : 2;
+    if (one_wave) l->direct_occ = (U == 1 || msg_bytes <= (8ull << 20)) ? 2 : 3;
     if (U >= 3 && !p->shifted) l->direct_occ = 2;  // three or four vectors: 128 registers
     if (p->shifted) l->direct_occ = rr::shift_occupancy(U);  // fixed per row count
     // ctas_per_sm asks for a register budget (2 or 3 CTAs per SM).  It applies
@@ -394,6 +411,8 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     if (ck.algo == RR_ALGO_RING && !p->shifted &&
         (ck.op == RR_OP_REDUCE_SCATTER || (ck.op == RR_OP_ALLREDUCE && ck.L <= 3)))
       cap = (unsigned long long)sms * (unsigned long long)l->direct_occ * (256ull / l->threads) * 2ull;
+    if (one_wave)  // one wave of the CTAs the registers let reside
+      cap = (unsigned long long)sms * (unsigned long long)l->direct_occ * (256ull / l->threads);
     // Vectors over a chunk boundary (ring order, boundaries off the 16-byte
     // grid): one extra CTA folds them, so the main loop stays lean.
     const unsigned long long V = 16 / E;

@@ -477,8 +477,33 @@ def test_direct_grid_waves(L):
     assert plan_dev(L, RS, 8, n, F32)[2] == sms * 6 * 2
     # chunk boundaries off the 16-byte grid: the shifted kernel keeps sixteen
     assert plan_dev(L, RS, 8, (64 << 20) // 4 - 8, F32)[2] == sms * 16
-    # a grid that fits under the cap is not changed
-    assert plan_dev(L, RS, 4, 1 << 20, F32)[2] == (1 << 20) * 4 // 16 // 256
+    # a grid that fits under the cap is not changed (five ranks: no one-wave rule)
+    assert plan_dev(L, RS, 5, 5 * (1 << 16), F32)[2] == 5 * (1 << 16) * 4 // 16 // 128  # one vector a thread
+
+
+def test_one_wave_for_small_flat_rings(L):
+    """Flat AllReduce / ReduceScatter over up to four ranks under 32 MiB per
+    rank: one wave of resident CTAs (128 threads; two 256-thread CTAs' worth of
+    registers per SM up to 8 MiB, three above), one vector a thread when two
+    would leave SMs idle, both L2 prefetches; not for AllGather, five or more
+    ranks, two-level rings or 32 MiB and up."""
+    sms = GB300["sms"]
+    MiB = 1 << 20
+    def plan(op, R, mib, dt=F16, E=2, **kw):
+        st, ch, grid, _ = plan_dev(L, op, R, R * (mib * MiB // E // R // 8 * 8), dt, **kw)
+        assert st == OK and ch["path"] == 3, (op, R, mib, ch)
+        return ch["vectors"], ch["ctas_per_sm"], grid, ch["prefetch"] - 1
+    assert plan(AR, 4, 4, F32, 4) == (2, 2, sms * 4, 3)      # workload 1
+    assert plan(RS, 4, 4, F32, 4) == (2, 2, sms * 4, 3)
+    assert plan(AR, 2, 16) == (2, 3, sms * 6, 3)
+    assert plan(RS, 3, 16) == (2, 3, sms * 6, 3)
+    v, occ, grid, pf = plan(AR, 4, 1)                         # 1 MiB: one vector, the grid under a wave
+    assert (v, occ, pf) == (1, 2, 3) and grid <= sms * 4
+    assert plan(AR, 4, 64)[2] == sms * 6 * 2 or plan(AR, 4, 64)[2] == sms * 16   # the usual rules from 32 MiB
+    vecs = 4 * MiB // 16
+    assert plan(AG, 4, 4)[0] == 1 and plan(AG, 4, 4)[2] == vecs // 128         # AllGather keeps its grid
+    assert plan(AR, 8, 4)[2] == vecs // 128                                     # five or more ranks too
+    assert plan(AR, 8, 4, group=4)[2] == vecs // 256                            # two-level rings too
 
 
 def test_rank_buffers_layout():
@@ -626,7 +651,7 @@ def test_planner_prefetch_policy(L):
     assert pf(RS, 8, 16) == HEAD
     assert pf(RS, 3, 256) == HEAD | AHEAD
     assert pf(AG, 8, 256) == AHEAD
-    assert pf(AR, 4, 4, F32, 4) == HEAD
+    assert pf(AR, 4, 4, F32, 4) == HEAD | AHEAD  # a small flat ring of four: one wave, both
     assert pf(AR, 16, 64, group=8) == 0
     st, ch, _, _ = plan_dev(L, RS, 8, 8 * 1001, F16)  # shifted ReduceScatter: none
     assert st == OK and ch["prefetch"] == 1
