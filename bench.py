@@ -17,10 +17,11 @@ CUDA-event time against the measured HBM copy bandwidth), the sweep over 1,
 ReduceScatter / AllGather at R = 4, the bfloat16 wire, the two-level ring, a
 fusion bucket), each timed by CUDA-graph replay over rotating buffer sets of
 at least 3x the L2 size so no launch finds its inputs in L2, an end-to-end
-figure through the C ABI's host-buffer entry point (ring_allreduce_host:
+figure through the C ABI's host-buffer entry point (ring_allreduce_host_ex:
 page-locked inputs copied in and all R outputs copied back inside the timed
-region, pipelined in pieces), the CPU oracle's throughput on a bounded sample, and the SM clocks
-sampled during the timed region.
+region, pipelined in pieces, with the copy schedule the link measured just
+before favours), the CPU oracle's throughput on a bounded sample, and the SM
+clocks sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --path-sweep [--sweep-ops ar,rs,ag] [--sweep-ranks ...] [--sweep-mib ...]
@@ -700,9 +701,14 @@ def run_ours(args):
             host_in[r].copy_(xs[r])
         piece = args.e2e_piece_mib * MIB // 2
         ws = torch.empty(rr.host_workspace_bytes(R, piece, torch.float16), dtype=torch.uint8, device=dev)
+        # the host link on these buffers: where both directions at once are
+        # slower than one after the other, the copies take turns
+        link = host_link_speeds(dev, host_in, host_out, xs)
+        one_way = link["both_ms"] > link["h2d_ms"] + link["d2h_ms"]
+        mode = rr.HOST_COPIES_ONE_WAY if one_way else rr.HOST_COPIES_OVERLAP
 
         def e2e_step():
-            rr.allreduce_host(host_in, host_outs=host_out, workspace=ws)
+            rr.allreduce_host(host_in, host_outs=host_out, workspace=ws, copy_mode=mode)
 
         for _ in range(2):
             e2e_step()
@@ -718,9 +724,9 @@ def run_ours(args):
         e_ms = combine_ranks(pg, [a.elapsed_time(b) / args.e2e_steps], dev)[0]
         e2e = {"value": round(job_throughput(world, msg, e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": R * msg, "d2h_bytes_per_step": R * msg, "ms_per_step": round(e_ms, 4),
-               "steps": args.e2e_steps, "api": "ring_allreduce_host",
-               "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity,
-               "link": host_link_speeds(dev, host_in, host_out, xs)}
+               "steps": args.e2e_steps, "api": "ring_allreduce_host_ex",
+               "copy_mode": "one_way" if one_way else "overlap",
+               "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity, "link": link}
         del host_in, host_out, ws
         outs = rr.rank_buffers(R, N, torch.float16, dev)
 

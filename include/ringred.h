@@ -276,6 +276,25 @@ rr_status ring_allreduce_host(const void *const *host_in, void *const *host_out,
                               rr_dtype dtype, rr_dtype wire, int group_size, void *dev_workspace,
                               size_t workspace_bytes, cudaStream_t stream);
 
+/* How ring_allreduce_host_ex schedules its copies.  OVERLAP (what
+ * ring_allreduce_host does): piece k+1 is copied in while piece k-1 is copied
+ * out, so the host link carries both directions at once.  ONE_WAY: both
+ * directions take turns on one internal stream (copy-in k+1, copy-out k) and
+ * only the reduction overlaps them.  Which is faster depends on the machine:
+ * on one GB300 node 4 GiB each way took 25 ms with both directions at once,
+ * on others 58-104 ms, against 42.5 ms one after the other; time both on the
+ * caller's own buffers and keep the faster. */
+typedef enum { RR_HOST_COPIES_OVERLAP = 0, RR_HOST_COPIES_ONE_WAY = 1 } rr_host_copies;
+
+/*
+ * ring_allreduce_host_ex -- ring_allreduce_host with the copy schedule
+ * chosen by the caller (copy_mode, above).  Same arguments, result, ordering
+ * and errors otherwise; an unknown copy_mode is RR_ERR_INVALID_ARG.
+ */
+rr_status ring_allreduce_host_ex(const void *const *host_in, void *const *host_out, int R, size_t count,
+                                 rr_dtype dtype, rr_dtype wire, int group_size, void *dev_workspace,
+                                 size_t workspace_bytes, rr_host_copies copy_mode, cudaStream_t stream);
+
 /* Workspace bytes ring_allreduce_host needs for pieces of piece_count
  * elements (rounded up to 256); 0 for invalid arguments. */
 size_t ring_allreduce_host_workspace(int R, size_t piece_count, rr_dtype dtype);

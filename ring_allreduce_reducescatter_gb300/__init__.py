@@ -18,7 +18,7 @@ __all__ = [
     "RingError", "lib", "allreduce", "reduce_scatter", "allgather", "collective", "plan",
     "allreduce_range", "allreduce_host", "allreduce_host_static", "host_workspace_bytes", "allreduce_algo",
     "chunk_count", "chunk_offset", "device_status", "selftest_bounded_wait", "LaunchCfg", "rank_buffers",
-    "debug_checks", "debug_set_margin",
+    "debug_checks", "debug_set_margin", "HOST_COPIES_OVERLAP", "HOST_COPIES_ONE_WAY",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_ALIAS", "ERR_CUDA", "ERR_TIMEOUT",
     "OP_ALLREDUCE", "OP_REDUCE_SCATTER", "OP_ALLGATHER", "PATH_AUTO", "PATH_BULK", "PATH_SIMPLE", "PATH_DIRECT",
 ]
@@ -119,6 +119,8 @@ def lib() -> ctypes.CDLL:
         L.ring_allreduce_range.restype = i
         L.ring_allreduce_host.argtypes = [vpp, vpp, i, sz, i, i, i, vp, sz, vp]
         L.ring_allreduce_host.restype = i
+        L.ring_allreduce_host_ex.argtypes = [vpp, vpp, i, sz, i, i, i, vp, sz, i, vp]
+        L.ring_allreduce_host_ex.restype = i
         L.ring_allreduce_host_static.argtypes = [vpp, vpp, i, sz, i, i, i, sz, vp]
         L.ring_allreduce_host_static.restype = i
         L.ring_allreduce_host_workspace.argtypes = [i, sz, i]
@@ -327,10 +329,15 @@ def _check_host_buffers(host_ins, host_outs):
     return R, N
 
 
+HOST_COPIES_OVERLAP, HOST_COPIES_ONE_WAY = 0, 1
+
+
 def allreduce_host(host_ins, host_outs=None, workspace: Optional[torch.Tensor] = None, wire=None,
-                   group_size: int = 0, stream=None, piece_count: int = 1 << 24):
+                   group_size: int = 0, stream=None, piece_count: int = 1 << 24, copy_mode: Optional[int] = None):
     """ring_allreduce_host: CPU tensors in and out (page-locked for overlap),
-    pipelined through a device workspace (allocated here if not given)."""
+    pipelined through a device workspace (allocated here if not given).
+    copy_mode (HOST_COPIES_OVERLAP / HOST_COPIES_ONE_WAY) calls
+    ring_allreduce_host_ex with that copy schedule."""
     host_ins = list(host_ins)
     if host_outs is None:
         host_outs = [torch.empty_like(t, pin_memory=t.is_pinned()) for t in host_ins]
@@ -344,10 +351,14 @@ def allreduce_host(host_ins, host_outs=None, workspace: Optional[torch.Tensor] =
     wt = dt if wire is None else _code(wire)
     hin = (ctypes.c_void_p * R)(*[t.data_ptr() for t in host_ins])
     hout = (ctypes.c_void_p * R)(*[t.data_ptr() for t in host_outs])
-    st = lib().ring_allreduce_host(hin, hout, R, N, dt, wt, group_size, workspace.data_ptr(), workspace.numel(),
-                                   _stream_handle(stream))
+    if copy_mode is None:
+        st = lib().ring_allreduce_host(hin, hout, R, N, dt, wt, group_size, workspace.data_ptr(), workspace.numel(),
+                                       _stream_handle(stream))
+    else:
+        st = lib().ring_allreduce_host_ex(hin, hout, R, N, dt, wt, group_size, workspace.data_ptr(),
+                                          workspace.numel(), int(copy_mode), _stream_handle(stream))
     if st != OK:
-        raise RingError(st, "ring_allreduce_host")
+        raise RingError(st, "ring_allreduce_host" if copy_mode is None else "ring_allreduce_host_ex")
     return host_outs
 
 

@@ -621,8 +621,13 @@ rr_status pipe_for_current_device(Pipe **out) {
   return RR_OK;
 }
 
+// copy_mode RR_HOST_COPIES_OVERLAP: piece k+1 copied in on one internal
+// stream while piece k-1 is copied out on the other (both directions of the
+// host link at once).  RR_HOST_COPIES_ONE_WAY: both directions on one copy
+// stream, in the order copy-in k+1, copy-out k, so the link carries one
+// direction at a time and the fold of piece k still overlaps the copies.
 rr_status host_pipeline(const void *const *host_in, void *const *host_out, int R, size_t count, int dtype, int wire,
-                        int group_size, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                        int group_size, void *ws, size_t ws_bytes, int copy_mode, cudaStream_t stream) {
   Checked ck;
   rr_status st = check_scalars(RR_OP_ALLREDUCE, R, count, dtype, wire, group_size, nullptr, &ck);
   if (st != RR_OK) return st;
@@ -650,6 +655,44 @@ rr_status host_pipeline(const void *const *host_in, void *const *host_out, int R
   // the copies start after the work already enqueued on `stream`
   if (!ok(cudaEventRecord(pp->start, stream)) || !ok(cudaStreamWaitEvent(pp->h2d, pp->start, 0))) return RR_ERR_CUDA;
   const size_t pieces = (count + piece - 1) / piece;
+  if (copy_mode == RR_HOST_COPIES_ONE_WAY) {
+    // one copy stream (h2d) for both directions: in k+1, then out k
+    auto slot_ptr = [&](size_t k) { return static_cast<unsigned char *>(ws) + (k % kHostSlots) * slot_bytes; };
+    auto copy_in = [&](size_t k) -> bool {
+      const size_t first = k * piece, n = (count - first < piece) ? count - first : piece;
+      for (int r = 0; r < R; ++r)
+        if (!ok(cudaMemcpyAsync(slot_ptr(k) + (size_t)r * piece * E, static_cast<const unsigned char *>(host_in[r]) + first * E,
+                                n * E, cudaMemcpyHostToDevice, pp->h2d)))
+          return false;
+      return ok(cudaEventRecord(pp->copied_in[k % kHostSlots], pp->h2d));
+    };
+    if (!copy_in(0)) return RR_ERR_CUDA;
+    for (size_t k = 0; k < pieces; ++k) {
+      const int sl = (int)(k % kHostSlots);
+      const size_t first = k * piece, n = (count - first < piece) ? count - first : piece;
+      if (k + 1 < pieces && !copy_in(k + 1)) return RR_ERR_CUDA;  // its slot's copy-out (k - 2) is earlier on h2d
+      if (!ok(cudaStreamWaitEvent(stream, pp->copied_in[sl], 0))) return RR_ERR_CUDA;
+      const void *dev_in[RR_MAX_RANKS];
+      void *dev_out[RR_MAX_RANKS];
+      for (int r = 0; r < R; ++r) dev_in[r] = dev_out[r] = slot_ptr(k) + (size_t)r * piece * E;
+      Checked pk = ck;
+      pk.first = first;
+      pk.n = n;
+      pk.all_16b_aligned = true;
+      st = launch_checked(pk, dev_in, dev_out, nullptr, stream);
+      if (st != RR_OK) return st;
+      if (!ok(cudaEventRecord(pp->folded[sl], stream)) || !ok(cudaStreamWaitEvent(pp->h2d, pp->folded[sl], 0)))
+        return RR_ERR_CUDA;
+      for (int r = 0; r < R; ++r)
+        if (!ok(cudaMemcpyAsync(static_cast<unsigned char *>(host_out[r]) + first * E, slot_ptr(k) + (size_t)r * piece * E,
+                                n * E, cudaMemcpyDeviceToHost, pp->h2d)))
+          return RR_ERR_CUDA;
+    }
+    // work enqueued on `stream` after this call sees every output copied
+    if (!ok(cudaEventRecord(pp->copied_out[0], pp->h2d)) || !ok(cudaStreamWaitEvent(stream, pp->copied_out[0], 0)))
+      return RR_ERR_CUDA;
+    return RR_OK;
+  }
   for (size_t k = 0; k < pieces; ++k) {
     const int sl = (int)(k % kHostSlots);
     const size_t first = k * piece, n = (count - first < piece) ? count - first : piece;
@@ -906,7 +949,16 @@ size_t ring_allreduce_host_workspace(int R, size_t piece_count, rr_dtype dtype) 
 rr_status ring_allreduce_host(const void *const *host_in, void *const *host_out, int R, size_t count,
                               rr_dtype dtype, rr_dtype wire, int group_size, void *dev_workspace,
                               size_t workspace_bytes, cudaStream_t stream) {
-  return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, dev_workspace, workspace_bytes, stream);
+  return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, dev_workspace, workspace_bytes,
+                       RR_HOST_COPIES_OVERLAP, stream);
+}
+
+rr_status ring_allreduce_host_ex(const void *const *host_in, void *const *host_out, int R, size_t count,
+                                 rr_dtype dtype, rr_dtype wire, int group_size, void *dev_workspace,
+                                 size_t workspace_bytes, rr_host_copies copy_mode, cudaStream_t stream) {
+  if (copy_mode != RR_HOST_COPIES_OVERLAP && copy_mode != RR_HOST_COPIES_ONE_WAY) return RR_ERR_INVALID_ARG;
+  return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, dev_workspace, workspace_bytes,
+                       copy_mode, stream);
 }
 
 rr_status ring_allreduce_host_static(const void *const *host_in, void *const *host_out, int R, size_t count,
@@ -922,7 +974,8 @@ rr_status ring_allreduce_host_static(const void *const *host_in, void *const *ho
   rr_status st = static_scratch_for_current_device(&scratch);
   if (st != RR_OK) return st;
   // the pipeline never reads a slot it has not first filled, so nothing needs clearing
-  return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, scratch, piece * per_slot_elem, stream);
+  return host_pipeline(host_in, host_out, R, count, dtype, wire, group_size, scratch, piece * per_slot_elem,
+                       RR_HOST_COPIES_OVERLAP, stream);
 }
 
 }  // extern "C"

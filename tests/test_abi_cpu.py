@@ -394,6 +394,13 @@ def test_host_pipeline_arguments(L):
     assert call_host(L, hin, hout, R, N, F16, ws, need, wire=BF16) == EUNSUP
     assert call_host(L, hin, hout, R, 0, F32, ws, need) == OK                # nothing to do
     assert call_host(L, hin, list(hin), R, N, F32, ws, need) not in (EINVAL, EALIAS, EUNSUP)  # in place
+    # the copy schedule of ring_allreduce_host_ex: 0 or 1
+    L.ring_allreduce_host_ex.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
+                                         ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    L.ring_allreduce_host_ex.restype = ctypes.c_int
+    for mode, want in ((2, EINVAL), (-1, EINVAL)):
+        assert L.ring_allreduce_host_ex(ptrs(hin), ptrs(hout), R, N, F32, F32, 0, ws, need, mode, None) == want
 
 
 def test_algo_arguments(L):

@@ -802,6 +802,12 @@ def test_host_pipeline_parity(rr, dtype, wire, R, L, N, piece):
         torch.cuda.current_stream().synchronize()
         for r in range(R):
             assert_same(host(hin2[r]), ref2.outs[r], f"host pipeline second call rank {r}")
+        # the one-direction-at-a-time copy schedule, twice on the same workspace
+        for call in range(2):
+            hout3 = rr.allreduce_host(hin, workspace=ws, wire=wire, group_size=L, copy_mode=rr.HOST_COPIES_ONE_WAY)
+            torch.cuda.current_stream().synchronize()
+            for r in range(R):
+                assert_same(host(hout3[r]), ref.outs[r], f"host pipeline one-way call {call} pinned={pinned} rank {r}")
 
 
 def test_host_pipeline_orders_after_prior_stream_work(rr):
