@@ -713,17 +713,19 @@ def run_ours(args):
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         if pg:
             pg.barrier()
-        a.record(stream)
-        for _ in range(args.e2e_steps):
+        marks[0].record(stream)
+        for k in range(args.e2e_steps):
             e2e_step()
-        b.record(stream)
+            marks[k + 1].record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = combine_ranks(pg, [a.elapsed_time(b) / args.e2e_steps], dev)[0]
+        step_ms = [marks[k].elapsed_time(marks[k + 1]) for k in range(args.e2e_steps)]
+        e_ms = combine_ranks(pg, [marks[0].elapsed_time(marks[-1]) / args.e2e_steps], dev)[0]
         e2e = {"value": round(job_throughput(world, msg, e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": R * msg, "d2h_bytes_per_step": R * msg, "ms_per_step": round(e_ms, 4),
+               "step_ms_min": round(min(step_ms), 3), "step_ms_max": round(max(step_ms), 3),
                "steps": args.e2e_steps, "api": "ring_allreduce_host_ex",
                "copy_mode": "one_way" if one_way else "overlap",
                "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity, "link": link}
@@ -996,7 +998,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--msg-mib", type=int, default=MSG_MIB)
     ap.add_argument("--sweep-iters", type=int, default=40)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--e2e-piece-mib", type=int, default=32)
     ap.add_argument("--cpu-sample-mib", type=int, default=CPU_SAMPLE_MIB)
     ap.add_argument("--ref-sample-mib", type=int, default=REF_SAMPLE_MIB)
