@@ -234,12 +234,6 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     const unsigned long long V = 16 / ck.E;
     p->chunks_on_grid = (p->base == 0 || (p->base % V == 0 && (unsigned long long)ck.first % V == 0)) ? 1 : 0;
   }
-  // The direct folds' chunk lookup: the per-thread cache for ReduceScatter and
-  // for AllReduce over two ranks a group, the plain division for larger
-  // AllReduce groups (same-box A/B at 256 MiB per rank, binary16, us, division
-  // / cache: ReduceScatter R = 2 165 / 144, R = 3 180 / 161; AllReduce R = 2
-  // 204 / 179, R = 3 243 / 254, R = 4 322 / 326).
-  p->chunk_cache = (ck.op != RR_OP_ALLREDUCE || ck.L <= 2) ? 1 : 0;
   p->algo = ck.algo;
   int P = 1, log2p = 0;
   while (P * 2 <= ck.R) {

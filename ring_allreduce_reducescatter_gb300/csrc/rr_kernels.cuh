@@ -702,13 +702,10 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         c[k] = 0;
         if (live[k] && !naive) {  // the naive order starts every element at rank 0
           const unsigned long long g0 = p.first + v * V;
-          // the cache where the planner measured it faster (chunk_cache), the
-          // plain lookup otherwise; one vector a thread (five or more ranks a
-          // group) always takes the plain lookup, whose kernel then carries no
-          // cache state in its registers
-          const bool cached = U > 1 && p.chunk_cache;
-          c[k] = cached ? cached_chunk(cc, p, g0) : chunk_of(p, g0);
-          if (!p.chunks_on_grid && (cached ? g0 + V - 1 >= cc.hi : c[k] != chunk_of(p, g0 + V - 1))) {
+          // one vector a thread (five or more ranks a group): the plain lookup
+          // measured faster than the cache, whose state costs registers
+          c[k] = U == 1 ? chunk_of(p, g0) : cached_chunk(cc, p, g0);
+          if (!p.chunks_on_grid && (U == 1 ? c[k] != chunk_of(p, g0 + V - 1) : g0 + V - 1 >= cc.hi)) {
             if (!p.straddle_cta)
               for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
             live[k] = false;
@@ -805,10 +802,9 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     const unsigned long long ipl = (len_last / V + per_item - 1) / per_item;  // items in the last chunk
     const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
     // work item w: its chunk and its index among the chunk's items
-    const bool small_items = n_items < (1ull << 32);  // the item's chunk by a 32-bit division
     auto locate = [&](unsigned long long w, int &c, unsigned long long &item) {
       if (w < (unsigned long long)(L - 1) * ipc) {
-        c = small_items ? (int)((unsigned)w / (unsigned)ipc) : (int)(w / ipc);
+        c = (int)(w / ipc);
         item = w - (unsigned long long)c * ipc;
       } else {
         c = L - 1;
@@ -910,10 +906,9 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     const unsigned long long rpc = (base / V + 64) / 32, rpl = (len_last / V + 64) / 32;  // rows per chunk, at most
     const unsigned long long ipc = (rpc + US - 1) / US, ipl = (rpl + US - 1) / US;        // items per chunk
     const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
-    const bool small_items = n_items < (1ull << 32);  // the item's chunk by a 32-bit division
     auto locate = [&](unsigned long long w, int &c, unsigned long long &item) {
       if (w < (unsigned long long)(L - 1) * ipc) {
-        c = small_items ? (int)((unsigned)w / (unsigned)ipc) : (int)(w / ipc);
+        c = (int)(w / ipc);
         item = w - (unsigned long long)c * ipc;
       } else {
         c = L - 1;

@@ -49,7 +49,6 @@ struct RingParams {
   int prefetch;                   // direct path: kPrefetch* bits
   unsigned long long debug_margin;  // debug build: bytes taken off every buffer's extent by the checks
   int chunks_on_grid;             // every chunk boundary of this launch falls on the 16-byte vector grid
-  int chunk_cache;                // direct path, folds of two or more vectors a thread: cached chunk lookup
 };
 
 // L2 prefetch of the direct path's inputs (no data reaches the SM, so no
