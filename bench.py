@@ -70,9 +70,8 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-DEVICE_SOURCES = ("rr_kernels.cuh", "rr_device.cuh", "rr_params.h", "rr_inst_f32.cu", "rr_inst_f16.cu",
-                  "rr_inst_bf16.cu", "rr_hd_direct.cuh", "rr_inst_hd_f32.cu", "rr_inst_hd_f16.cu",
-                  "rr_inst_hd_bf16.cu", "rr_inst_f32_narrow.cu")
+DEVICE_SOURCES = ("rr_kernels.cuh", "rr_device.cuh", "rr_params.h", "rr_inst_one.cu", "rr_dispatch.cu",
+                  "rr_hd_direct.cuh", "rr_inst_hd_f32.cu", "rr_inst_hd_f16.cu", "rr_inst_hd_bf16.cu")
 
 
 def code_only(text):

@@ -1,7 +1,9 @@
 """Build libringred.so in-tree with nvcc for sm_103a (GB300).
 
 Each translation unit under csrc/ compiles in parallel to an object under
-_build/, then nvcc links the shared library next to this file.  No fast-math
+_build/ (rr_inst_one.cu once for every collective / storage / wire
+combination, INSTANCES), then nvcc links the shared library next to this
+file.  No fast-math
 and no FMA contraction: the kernels' results are defined bit for bit.
 
 A build is reused only when the digest recorded beside it (under _build/)
@@ -31,6 +33,17 @@ DEBUG_LIB = os.path.join(PKG, "libringred_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",
          "-I", INCLUDE, "-I", CSRC]
+
+
+# (collective, storage format, wire format) combinations, each compiled from
+# rr_inst_one.cu into an object of its own (values of rr_params.h's kOp* / kF*)
+OPS = {"allreduce": 0, "reduce_scatter": 1, "allgather": 2}
+FMTS = {"f32": 0, "f16": 1, "bf16": 2}
+FOLD_PAIRS = (("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"), ("f32", "bf16"), ("f32", "f16"), ("f16", "f32"),
+              ("bf16", "f32"))
+INSTANCES = ([(op, dt, wt) for op in ("allreduce", "reduce_scatter") for dt, wt in FOLD_PAIRS] +
+             [("allgather", dt, dt) for dt in ("f32", "f16", "bf16")])
+INST_ONE = "rr_inst_one.cu"
 
 
 def nvcc() -> str:
@@ -78,19 +91,28 @@ def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False)
     if not force and os.path.exists(lib) and _recorded_digest(lib) == digest:
         return lib
     os.makedirs(objdir, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    # (source, object name, defines): every .cu once, rr_inst_one.cu once per instance
+    jobs = [(src, os.path.basename(src), []) for src in sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+            if os.path.basename(src) != INST_ONE]
+    for op, dt, wt in INSTANCES:
+        jobs.append((os.path.join(CSRC, INST_ONE), f"rr_inst_{op}_{dt}_{wt}.cu",
+                     [f"-DRR_INST_OP={OPS[op]}", f"-DRR_INST_DT={FMTS[dt]}", f"-DRR_INST_WT={FMTS[wt]}"]))
+    # the longest units first, so they start at once
+    jobs.sort(key=lambda j: j[0].endswith(INST_ONE), reverse=True)
 
-    def compile_one(src):
-        obj = os.path.join(objdir, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *flags, *extra, "-c", src, "-o", obj]
+    def compile_one(job):
+        src, name, defs = job
+        obj = os.path.join(objdir, name + ".o")
+        cmd = [cc, *ARCH, *flags, *defs, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {name}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        results = list(ex.map(compile_one, srcs))
+    workers = max(1, min(len(jobs), (os.cpu_count() or 1) + 2))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        results = list(ex.map(compile_one, jobs))
     if verbose_ptxas:
         for _, log in results:
             print(log)

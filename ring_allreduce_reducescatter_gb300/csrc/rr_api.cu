@@ -566,13 +566,7 @@ rr_status launch_checked(const Checked &ck, const void *const *in, void *const *
   rr::Launch l;
   st = plan(ck, in, out, cfg, dev, &p, &l);
   if (st != RR_OK) return st;
-  cudaError_t e;
-  if (ck.dtype == RR_FP32)
-    e = rr::launch_f32(ck.op, ck.wire, p, l, stream);
-  else if (ck.dtype == RR_FP16)
-    e = rr::launch_f16(ck.op, ck.wire, p, l, stream);
-  else
-    e = rr::launch_bf16(ck.op, ck.wire, p, l, stream);
+  const cudaError_t e = rr::launch_collective(ck.op, ck.dtype, ck.wire, p, l, stream);
   return cuda_ok(e) ? RR_OK : RR_ERR_CUDA;
 }
 

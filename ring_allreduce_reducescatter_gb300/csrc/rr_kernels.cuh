@@ -640,7 +640,10 @@ __device__ __forceinline__ void prefetch_vectors(const RingParams &p, unsigned l
   }
 }
 
-template <int OP, int DT, int WT, int U, int OCC>
+// CACHE: folds of two or more vectors a thread look their chunk up through
+// the per-thread cache (false: the plain division, for AllReduce groups of
+// three or more ranks, where the division measured faster).
+template <int OP, int DT, int WT, int U, int OCC, bool CACHE = true>
 __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __grid_constant__ RingParams p) {
   using VT = Vec<DT, WT>;
   using W = typename VT::W;
@@ -702,10 +705,12 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
         c[k] = 0;
         if (live[k] && !naive) {  // the naive order starts every element at rank 0
           const unsigned long long g0 = p.first + v * V;
-          // one vector a thread (five or more ranks a group): the plain lookup
-          // measured faster than the cache, whose state costs registers
-          c[k] = U == 1 ? chunk_of(p, g0) : cached_chunk(cc, p, g0);
-          if (!p.chunks_on_grid && (U == 1 ? c[k] != chunk_of(p, g0 + V - 1) : g0 + V - 1 >= cc.hi)) {
+          // one vector a thread (five or more ranks a group), and AllReduce
+          // kernels built without the cache: the plain lookup, which measured
+          // faster there than the cache, whose state costs registers
+          constexpr bool cached = U > 1 && CACHE;
+          c[k] = cached ? cached_chunk(cc, p, g0) : chunk_of(p, g0);
+          if (!p.chunks_on_grid && (cached ? g0 + V - 1 >= cc.hi : c[k] != chunk_of(p, g0 + V - 1))) {
             if (!p.straddle_cta)
               for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
             live[k] = false;
@@ -753,10 +758,6 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
   for (unsigned long long i = p.n_bulk + (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.count; i += T)
     element_op<OP, DT, WT>(p, i);
 }
-
-// A single CTA waits on a barrier that nothing completes; the bounded wait
-// must give up and record it.
-__global__ void rr_wait_probe_kernel(unsigned int *status, unsigned long long limit_ns);
 
 // --------------------------------------------------------------------------
 // ReduceScatter / AllGather whose chunk boundaries are off the 16-byte grid:
@@ -1075,6 +1076,15 @@ cudaError_t launch_direct(const RingParams &p, const Launch &l, cudaStream_t s) 
     if (U == 1) return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
     if (U == 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2>, l, 0, s, p);
   } else {
+    // AllReduce over groups of three or more ranks at two vectors a thread:
+    // the kernels without the lookup cache (same-box A/B at 256 MiB per rank,
+    // binary16: R = 3 254 -> 242 us, R = 4 326 -> 321 us)
+    if constexpr (OP == kOpAllReduce) {
+      if (U == 2 && p.L >= 3 && p.algo == kAlgoRing) {
+        if (occ == 3) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 3, false>, l, 0, s, p);
+        if (occ == 2) return launch_kernel(rr_direct_kernel<OP, DT, WT, 2, 2, false>, l, 0, s, p);
+      }
+    }
     switch (U * 8 + occ) {
       case 1 * 8 + 2: return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 2>, l, 0, s, p);
       case 1 * 8 + 3: return launch_kernel(rr_direct_kernel<OP, DT, WT, 1, 3>, l, 0, s, p);

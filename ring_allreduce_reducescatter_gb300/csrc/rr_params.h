@@ -1,6 +1,6 @@
 // rr_params.h -- the parameter block of every libringred kernel and the
 // internal launcher interface between the C ABI (rr_api.cu) and the kernel
-// translation units (rr_inst_*.cu).
+// translation units (rr_dispatch.cu, rr_inst_one.cu, rr_inst_hd_*.cu).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -98,11 +98,14 @@ struct Launch {
   int direct_occ = 2;  // direct path, one vector per thread: 256-thread CTAs per SM it is compiled for (2 or 3)
 };
 
-// Defined in rr_inst_<storage>.cu: launch the kernel of (op, storage dtype,
-// wire) on `stream`; returns the launch error.
-cudaError_t launch_f32(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
-cudaError_t launch_f32_narrow(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
-cudaError_t launch_f16(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
+// The kernel of (OP, storage DT, wire WT) on `stream`; returns the launch
+// error.  Explicitly instantiated once per supported combination, each in its
+// own object of rr_inst_one.cu.
+template <int OP, int DT, int WT>
+cudaError_t launch_op(const RingParams &p, const Launch &l, cudaStream_t s);
+
+// Defined in rr_dispatch.cu: the launch_op of (op, storage dtype, wire).
+cudaError_t launch_collective(int op, int dtype, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
 // Defined in rr_inst_hd_<storage>.cu: the halving-doubling AllReduce on the
 // direct path (one kernel per tree size).
 cudaError_t launch_hd_direct_f32(int wire, const RingParams &p, const Launch &l, cudaStream_t s);
@@ -112,8 +115,7 @@ inline cudaError_t launch_hd_direct(int dt, int wire, const RingParams &p, const
   return dt == kF32 ? launch_hd_direct_f32(wire, p, l, s)
                     : dt == kF16 ? launch_hd_direct_f16(wire, p, l, s) : launch_hd_direct_bf16(wire, p, l, s);
 }
-cudaError_t launch_bf16(int op, int wire, const RingParams &p, const Launch &l, cudaStream_t s);
-// Defined in rr_inst_f32.cu: the bounded-wait self test kernel.
+// Defined in rr_dispatch.cu: the bounded-wait self test kernel.
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace rr
