@@ -286,6 +286,13 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // R = 9 at 4 MiB lost 3 %.  (Three ranks at three vectors, nine loads but
     // two CTAs per SM: 0.60 against 0.875 at 256 MiB, binary16.)
     if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && msg_bytes >= (64ull << 20)) U = 2;
+    // AllGather over two ranks loads one vector for every two it stores: two
+    // vectors a thread, on two waves of two 256-thread CTAs per SM (below).
+    // Measured, binary16, of the copy bandwidth, median of two buffer layouts:
+    // 8 / 16 / 32 MiB per rank 0.65 / 0.75 / 0.86 -> 0.70 / 0.81 / 0.88; over
+    // three ranks it lost 0-2 %.
+    const bool ag_pair = ck.op == RR_OP_ALLGATHER && ck.algo == RR_ALGO_RING && ck.R == 2 && msg_bytes < (64ull << 20);
+    if (ag_pair) U = 2;
     if (p->shifted) {
       // rows a warp takes at once.  Measured, binary16, of the copy bandwidth
       // at 16 / 256 MiB per rank: ReduceScatter R = 2 four rows 0.56 / 0.81
@@ -413,6 +420,19 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
       cap = (unsigned long long)sms * (unsigned long long)l->direct_occ * (256ull / l->threads) * 2ull;
     if (one_wave)  // one wave of the CTAs the registers let reside
       cap = (unsigned long long)sms * (unsigned long long)l->direct_occ * (256ull / l->threads);
+    if (ag_pair && !p->shifted)
+      cap = (unsigned long long)sms * (unsigned long long)l->direct_occ * (256ull / l->threads) * 2ull;
+    // The shifted ReduceScatter: twelve 128-thread CTAs per SM (two whole waves
+    // of the two- and three-row kernels, three of the four-row one) instead of
+    // sixteen, over groups of up to four ranks and, for more, from 32 MiB per
+    // rank.  Measured, binary16, of the copy bandwidth, median of two buffer
+    // layouts, at 16 / 64 / 256 MiB per rank: R = 2 0.59 / 0.75 / 0.85 ->
+    // 0.60 / 0.76 / 0.84; R = 3 0.64 / 0.80 / 0.87 -> 0.69 / 0.84 / 0.87; R = 4
+    // 0.73 / 0.88 / 0.91 -> 0.77 / 0.92 / 0.93; R = 5 (64 / 256) 0.79 / 0.85 ->
+    // 0.83 / 0.89; R = 9 0.91 / 0.92 -> 0.94 / 0.95; R = 16 0.98 / 0.97 ->
+    // 0.98 / 0.98.  At 16 MiB five or more ranks lost 2-5 %.
+    if (p->shifted && ck.op == RR_OP_REDUCE_SCATTER && (ck.L <= 4 || msg_bytes >= (32ull << 20)))
+      cap = (unsigned long long)sms * 1536ull / (unsigned long long)l->threads;
     // Vectors over a chunk boundary (ring order, boundaries off the 16-byte
     // grid): one extra CTA folds them, so the main loop stays lean.
     const unsigned long long V = 16 / E;

@@ -482,8 +482,20 @@ def test_direct_grid_waves(L):
     # not one batch of eight loads (which would keep two CTAs per SM): three
     # CTAs per SM, two waves
     assert plan_dev(L, RS, 8, n, F32)[2] == sms * 6 * 2
-    # chunk boundaries off the 16-byte grid: the shifted kernel keeps sixteen
-    assert plan_dev(L, RS, 8, (64 << 20) // 4 - 8, F32)[2] == sms * 16
+    # chunk boundaries off the 16-byte grid: the shifted ReduceScatter takes
+    # twelve 128-thread CTAs per SM for up to four ranks and, for more, from 32
+    # MiB per rank; sixteen otherwise
+    assert plan_dev(L, RS, 8, (64 << 20) // 4 - 8, F32)[2] == sms * 12
+    assert plan_dev(L, RS, 8, (16 << 20) // 2 - 8 + 3, F16)[2] == sms * 16
+    assert plan_dev(L, RS, 4, (16 << 20) // 2 - 4 + 3, F16)[2] == sms * 12
+    assert plan_dev(L, RS, 2, (64 << 20) // 2 + 2, F16)[2] == sms * 12
+    st, _, grid, _ = plan_dev(L, RS, 4, (16 << 20) // 2 - 4 + 3, F16, cfg=(0, 0, 0, 0, 256))
+    assert st == OK and grid == sms * 6                       # the same share of threads at 256 a CTA
+    # AllGather over two ranks below 64 MiB per rank: two waves of two
+    # 256-thread CTAs' worth of registers per SM
+    assert plan_dev(L, AG, 2, 2 * (8 << 20), F16)[2] == sms * 4 * 2
+    assert plan_dev(L, AG, 2, 2 * (64 << 20), F16)[2] == sms * 16
+    assert plan_dev(L, AG, 3, 3 * (8 << 20), F16)[2] == sms * 16
     # a grid that fits under the cap is not changed (five ranks: no one-wave rule)
     assert plan_dev(L, RS, 5, 5 * (1 << 16), F32)[2] == 5 * (1 << 16) * 4 // 16 // 128  # one vector a thread
 
@@ -607,13 +619,14 @@ def test_forced_vectors_and_register_budget(L):
 def test_planner_vectors_for_few_ranks(L):
     """The measured choices of vectors (rows) a thread: ReduceScatter over three
     ranks two vectors at three CTAs per SM; AllGather one vector (the L2
-    prefetch keeps its loads in flight); the shifted ReduceScatter 4 rows for
-    two ranks, 3 for three from 64 MiB per rank, else 2; the shifted
-    AllGather 2."""
+    prefetch keeps its loads in flight), two over two ranks below 64 MiB per
+    rank; the shifted ReduceScatter 4 rows for two ranks, 3 for three from 64
+    MiB per rank, else 2; the shifted AllGather 2."""
     st, ch, _, _ = plan_dev(L, RS, 3, 3 * (1 << 22), F32)
     assert st == OK and ch["path"] == 3 and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
-    st, ch, _, _ = plan_dev(L, AG, 2, 2 * (1 << 22), F32)
-    assert st == OK and ch["path"] == 3 and ch["vectors"] == 1
+    for R, n, vectors in ((2, 1 << 22, 2), (2, 1 << 24, 1), (3, 1 << 22, 1), (4, 1 << 22, 1)):
+        st, ch, _, _ = plan_dev(L, AG, R, R * n, F32)
+        assert st == OK and ch["path"] == 3 and ch["vectors"] == vectors and ch["ctas_per_sm"] == 2, (R, n, ch)
     for R, n, rows in ((2, 100_000, 4), (3, 100_000, 2), (3, 2_000_000, 3), (4, 100_000, 2), (8, 100_000, 2),
                        (16, 100_000, 2)):
         st, ch, _, _ = plan_dev(L, RS, R, R * (8 * n + 3), F16)
