@@ -781,9 +781,10 @@ def sweep_variants(rr, op, wide, shifted, all_variants, prefetch=False, explicit
         for item in explicit.split(";"):
             vals = [int(v) for v in item.split(",")]
             path, u, occ, pf = vals[:4]
-            cap = vals[4] if len(vals) > 4 else 0
-            out.append((f"path={path} U={u} occ={occ} prefetch={pf}" + (f" max_ctas={cap}" if cap else ""),
-                        rr.LaunchCfg(path, 0, 0, occ, 0, cap, 0, u, 0, pf)))
+            cap, threads, early = (vals[4:] + [0, 0, 0])[:3]
+            label = f"path={path} U={u} occ={occ} prefetch={pf}" + (f" max_ctas={cap}" if cap else "")
+            label += (f" threads={threads}" if threads else "") + (f" early={early}" if early else "")
+            out.append((label, rr.LaunchCfg(path, 0, 0, occ, threads, cap, early, u, 0, pf)))
         return out
     if prefetch and not shifted:
         for pf, name in ((1, "none"), (2, "head"), (3, "ahead"), (4, "head+ahead")):
@@ -839,7 +840,7 @@ def path_sweep_layout(rr, dev, l2_bytes, peak, op, R_, mib, dtype, wire, off_gri
 
     E = torch.tensor([], dtype=dtype).element_size()
     V = 16 // E
-    base = max(V, (mib * MIB // E) // R_ // V * V) + (1 if off_grid else 0)
+    base = max(V, (int(mib * MIB) // E) // R_ // V * V) + (1 if off_grid else 0)
     N = R_ * base
     lens = [rr.chunk_count(N, R_, c) for c in range(R_)]
     in_lens = lens if op == 2 else [N] * R_
@@ -905,7 +906,7 @@ def run_path_sweep(args):
     for op_name in args.sweep_ops.split(","):
         op = SWEEP_OPS[op_name]
         for R_ in (int(v) for v in args.sweep_ranks.split(",")):
-            for mib in (int(v) for v in args.sweep_mib.split(",")):
+            for mib in (float(v) for v in args.sweep_mib.split(",")):
                 for off_grid in ((False, True) if args.sweep_off_grid == "both" else
                                  ((True,) if args.sweep_off_grid == "only" else (False,))):
                     if off_grid and op == 0:
@@ -1022,7 +1023,8 @@ def main():
     ap.add_argument("--sweep-layouts", type=int, default=1, help="buffer layouts per point (median reported)")
     ap.add_argument("--sweep-table", default="", help="also write the tile-vs-direct table (markdown) to this file")
     ap.add_argument("--sweep-cfg", default="",
-                    help="explicit launch configurations 'path,vectors,ctas_per_sm,prefetch[,max_ctas];...' "
+                    help="explicit launch configurations "
+                         "'path,vectors,ctas_per_sm,prefetch[,max_ctas[,threads[,early_launch]]];...' "
                          "(with auto)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps

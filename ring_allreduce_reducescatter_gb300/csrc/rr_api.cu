@@ -263,6 +263,16 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
                                                                                              : RR_PATH_BULK;
   }
   p->shifted = (path == RR_PATH_DIRECT && !chunks_aligned) ? 1 : 0;
+  // ReduceScatter over two ranks from 64 MiB per rank: the chunk-by-chunk
+  // (shifted) kernel also where the chunks sit on the 16-byte grid (it then
+  // shifts by nothing).  It knows each work item's chunk, where the direct
+  // kernel looks up every vector's, and its four rows keep eight loads in
+  // flight a lane.  Measured, binary16, of the copy bandwidth, at 16 / 64 /
+  // 256 MiB per rank: direct 0.70 / 0.84 / 0.89, chunk by chunk 0.70 / 0.88 /
+  // 0.96; over three or more ranks the direct kernel is as fast or faster.
+  if (path == RR_PATH_DIRECT && ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && ck.L == 2 &&
+      (unsigned long long)ck.count * E >= (64ull << 20) && c.vectors == 0 && c.ctas_per_sm == 0)
+    p->shifted = 1;
 
   l->path = path;
   // 128-thread CTAs on the direct path: finer grid granularity, measured 1-5 %
@@ -286,25 +296,41 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     // R = 9 at 4 MiB lost 3 %.  (Three ranks at three vectors, nine loads but
     // two CTAs per SM: 0.60 against 0.875 at 256 MiB, binary16.)
     if (ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && msg_bytes >= (64ull << 20)) U = 2;
-    // AllGather over two ranks loads one vector for every two it stores: two
-    // vectors a thread, on two waves of two 256-thread CTAs per SM (below).
-    // Measured, binary16, of the copy bandwidth, median of two buffer layouts:
-    // 8 / 16 / 32 MiB per rank 0.65 / 0.75 / 0.86 -> 0.70 / 0.81 / 0.88; over
-    // three ranks it lost 0-2 %.
-    const bool ag_pair = ck.op == RR_OP_ALLGATHER && ck.algo == RR_ALGO_RING && ck.R == 2 && msg_bytes < (64ull << 20);
-    if (ag_pair) U = 2;
+    // AllGather from 4 MiB per rank: two vectors a thread over up to five
+    // ranks below 16 MiB, and over two ranks below 64 MiB on two waves of two
+    // 256-thread CTAs per SM (below).  Measured, of the copy bandwidth, median
+    // of two buffer layouts: binary32 at 4 / 8 MiB per rank R = 3 0.61 / 0.73
+    // -> 0.64 / 0.75, R = 4 0.68 / 0.82 -> 0.71 / 0.83, R = 5 0.72 / 0.84 ->
+    // 0.74 / 0.88; binary16 R = 2 at 8 / 16 / 32 MiB 0.65 / 0.75 / 0.86 -> 0.70
+    // / 0.81 / 0.88.  Not below 4 MiB (R = 2 at 1 MiB lost 14 %; grids of 1.3
+    // waves at two vectors lost 7-16 % at 3 MiB), nor over eight ranks or
+    // more (R = 8 at 4 MiB lost 3 %, R = 16 12 %), nor for three ranks from 16
+    // MiB (0-1 % either way).
+    const bool ag_pair = ck.op == RR_OP_ALLGATHER && ck.algo == RR_ALGO_RING && ck.R == 2 &&
+                         msg_bytes >= (4ull << 20) && msg_bytes < (64ull << 20);
+    if (ag_pair || (ck.op == RR_OP_ALLGATHER && ck.algo == RR_ALGO_RING && ck.R <= 5 && msg_bytes >= (4ull << 20) &&
+                    msg_bytes < (16ull << 20)))
+      U = 2;
     if (p->shifted) {
-      // rows a warp takes at once.  Measured, binary16, of the copy bandwidth
-      // at 16 / 256 MiB per rank: ReduceScatter R = 2 four rows 0.56 / 0.81
-      // (two: 0.55 / 0.72); R = 3 two rows 0.62 / 0.79, three 0.58 / 0.81;
-      // R = 4 two rows 0.68 / 0.83; R = 8 two rows 0.81 / 0.84, one 0.77 /
-      // 0.85.  AllGather R = 2 two rows 0.68 / 0.82, four 0.63 / 0.83; R = 3
-      // two rows 0.79 / 0.92; R = 4 two rows 0.84 / 0.94; R = 8 two vectors
-      // a thread 0.83 / 0.93, one 0.84 / 0.86.
-      if (ck.op == RR_OP_REDUCE_SCATTER)
-        U = ck.L == 2 ? 4 : (ck.L == 3 && msg_bytes >= (64ull << 20)) ? 3 : 2;
-      else
+      // rows a warp takes at once.  ReduceScatter, measured, binary16, of the
+      // copy bandwidth, median of two buffer layouts: two rows, but four for
+      // two ranks from 8 MiB per rank (R = 2 at 16 / 64 / 256 MiB: two 0.68 /
+      // 0.83 / 0.90, four 0.70 / 0.88 / 0.96; at 4 MiB two 0.31, four 0.28),
+      // one for four or more ranks below 8 MiB (4 MiB: R = 4 0.38 -> 0.39, R =
+      // 5 0.40 -> 0.47, R = 8 0.66 -> 0.71, R = 16 0.72 -> 0.82; at 16 MiB
+      // one row lost 1-18 %), four for eight or more ranks from 128 MiB (256
+      // MiB: R = 8 0.95 -> 0.98, R = 16 0.97 -> 1.00; at 64 MiB 0-1 % lost).
+      // AllGather, at 16 / 256 MiB per rank: R = 2 two rows 0.68 / 0.82, four
+      // 0.63 / 0.83; R = 3 two rows 0.79 / 0.92; R = 4 two rows 0.84 / 0.94;
+      // R = 8 two vectors a thread 0.83 / 0.93, one 0.84 / 0.86.
+      if (ck.op == RR_OP_REDUCE_SCATTER) {
         U = 2;
+        if (ck.L == 2 && msg_bytes >= (8ull << 20)) U = 4;
+        if (ck.L >= 4 && msg_bytes < (8ull << 20)) U = 1;
+        if (ck.L >= 8 && msg_bytes >= (128ull << 20)) U = 4;
+      } else {
+        U = 2;
+      }
     }
     if (wide && U > 2) U = 2;
     // Flat rings of up to four ranks under 32 MiB per rank (ring order,
@@ -351,10 +377,17 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     }
     // The shifted kernels: the AllGather prefetches its first work item and
     // the next one (binary16, of the copy bandwidth: R = 2 at 256 MiB 0.80 ->
-    // 0.86, R = 8 at 16 MiB 0.83 -> 0.88); the ReduceScatter does not (one
-    // item ahead lost 10-17 %, the first item alone 0-1 % either way).
-    if (p->shifted && c.prefetch == 0)
-      p->prefetch = ck.op == RR_OP_ALLGATHER ? (rr::kPrefetchHead | rr::kPrefetchAhead) : 0;
+    // 0.86, R = 8 at 16 MiB 0.83 -> 0.88); the ReduceScatter its first item,
+    // over three to five ranks below 32 MiB per rank (4 / 16 MiB: R = 3 0.32 /
+    // 0.77 -> 0.35 / 0.82, R = 4 0.38 / 0.84 -> 0.39 / 0.87, R = 5 0.40 / 0.78
+    // -> 0.42 / 0.85; two ranks lost 1-3 %, eight or more 10-14 %; one item
+    // ahead lost 2-20 % everywhere).
+    if (p->shifted && c.prefetch == 0) {
+      if (ck.op == RR_OP_ALLGATHER)
+        p->prefetch = rr::kPrefetchHead | rr::kPrefetchAhead;
+      else
+        p->prefetch = (ck.L >= 3 && ck.L <= 5 && msg_bytes < (32ull << 20)) ? rr::kPrefetchHead : 0;
+    }
     if (ck.algo == RR_ALGO_HALVING_DOUBLING) p->prefetch = 0;
     // A third CTA per SM (registers capped at 85) keeps more loads in flight
     // once threads loop (measured at 256 MiB, of the copy bandwidth: R = 5

@@ -789,100 +789,136 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     // chunk are folded too and dropped); the folded block is also the upper
     // half lane t - 1 needs, so one shuffle and one funnel shift of the
     // result build each output vector, whatever R is.  Lane 31 only supplies
-    // its block.  A vector whose upper block would pass the end of the rank
-    // vectors goes element by element, and so do the elements past a chunk's
-    // last full vector.
+    // its block.  Every work item but a chunk's last lies wholly inside the
+    // chunk and the rank vectors, so it loads and stores without a check;
+    // the last items go first, a row to a warp.  A vector whose upper block
+    // would pass the end of the rank vectors goes element by element, and so
+    // do the elements past a chunk's last full vector.
     constexpr int NB = direct_batch_ranks(US);  // ranks per batch: 8 (US = 3: 9) loads in flight a lane
+    constexpr unsigned long long VB = (unsigned long long)V * E;  // bytes of a vector (16)
     const unsigned lane = threadIdx.x & 31u;
     const unsigned long long warp = tid >> 5, n_warps = T >> 5;
     const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
-    // work items: one per 31 * US output vectors of a chunk, numbered across
-    // all chunks so that every warp's items spread over the chunks
+    // work items: one per 31 * US output vectors of a chunk
     constexpr unsigned long long per_item = 31ull * US;
     const unsigned long long ipc = (base / V + per_item - 1) / per_item;      // items in chunks 0..L-2
     const unsigned long long ipl = (len_last / V + per_item - 1) / per_item;  // items in the last chunk
-    const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
-    // work item w: its chunk and its index among the chunk's items
-    auto locate = [&](unsigned long long w, int &c, unsigned long long &item) {
-      if (w < (unsigned long long)(L - 1) * ipc) {
-        c = (int)(w / ipc);
-        item = w - (unsigned long long)c * ipc;
-      } else {
-        c = L - 1;
-        item = w - (unsigned long long)(L - 1) * ipc;
-      }
-    };
-    // L2 prefetch of the blocks lane `lane` loads for item w
-    auto prefetch_item = [&](unsigned long long w) {
-      if (w >= n_items) return;
-      int c;
-      unsigned long long item;
-      locate(w, c, item);
-      const unsigned long long len = c < L - 1 ? base : len_last, nv = len / V, g0 = (unsigned long long)c * base;
-      const unsigned long long shift = g0 % V;
+    // inner items (all but each chunk's last), numbered across the chunks so
+    // that every warp's items spread over them
+    const unsigned long long inc = ipc ? ipc - 1 : 0, inl = ipl ? ipl - 1 : 0;
+    const unsigned long long n_inner = (unsigned long long)(L - 1) * inc + inl;
+    // the blocks lane `lane` loads for item `item` of chunk c, into L2
+    auto prefetch_item = [&](int c, unsigned long long item) {
+      const unsigned long long g0 = (unsigned long long)c * base, a0 = g0 - g0 % V;
+      const unsigned long long off = (a0 + (item * per_item + lane) * V) * E;
 #pragma unroll
-      for (int k = 0; k < US; ++k) {
-        const unsigned long long u = item * per_item + 31ull * k + lane, ga = g0 + u * V - shift;
-        if (u <= nv && ga + V <= N)
-          for (int r = 0; r < L; ++r) prefetch_in<false, E>(p, r, ga * E);
+      for (int k = 0; k < US; ++k)
+        for (int r = 0; r < L; ++r) prefetch_in<false, E>(p, r, off + 31ull * VB * k);
+    };
+    // the inner item n_warps on: across chunk ends one at a time (at most L - 1 steps)
+    auto advance = [&](int &c, unsigned long long &item) {
+      item += n_warps;
+      while (c < L - 1 && item >= inc) {
+        item -= inc;
+        ++c;
       }
     };
-    if (p.prefetch & kPrefetchHead) prefetch_item(warp);
+    // work units, dealt to the warps in turn: first the rows of each chunk's
+    // last item (L * US units), then the inner items; w0 is this warp's
+    // first inner item
+    const unsigned long long n_edge = (unsigned long long)L * US;
+    const unsigned long long w0 =
+        warp < n_edge ? warp + (n_edge - warp + n_warps - 1) / n_warps * n_warps - n_edge : warp - n_edge;
+    int c = L - 1;
+    unsigned long long item = 0;
+    if (w0 < n_inner) {
+      if (w0 < (unsigned long long)(L - 1) * inc) {
+        c = (int)(w0 / inc);
+        item = w0 - (unsigned long long)c * inc;
+      } else {
+        item = w0 - (unsigned long long)(L - 1) * inc;
+      }
+      if (p.prefetch & kPrefetchHead) prefetch_item(c, item);
+    }
     grid_dependency_wait();
     grid_dependents_launch();
-    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
-      if (p.prefetch & kPrefetchAhead) prefetch_item(w + n_warps);
-      int c;
-      unsigned long long item;
-      locate(w, c, item);
-      const unsigned long long len = c < L - 1 ? base : len_last, nv = len / V, g0 = (unsigned long long)c * base;
-      const int shift = (int)(g0 % V);  // elements
-      const int sh = shift * E;         // bytes
-      {
-        const unsigned long long u0 = item * per_item;
-        unsigned long long u[US], ga[US];
-        bool load[US], act[US], tail[US];
+    // the rows of each chunk's last item, one to a warp
+    for (unsigned long long e = warp; e < n_edge; e += n_warps) {  // warp-uniform
+      const int ce = (int)(e / US), k = (int)(e % US);
+      const unsigned long long len = ce < L - 1 ? base : len_last, nv = len / V, n_c = ce < L - 1 ? ipc : ipl;
+      if (n_c == 0) continue;
+      const unsigned long long g0 = (unsigned long long)ce * base;
+      const int shift = (int)(g0 % V), sh = shift * E;
+      const unsigned long long u = (n_c - 1) * per_item + 31ull * k + lane, ga = g0 - (unsigned long long)shift + u * V;
+      const bool load = u <= nv && ga + V <= N;  // the block under vector u's start
+      const bool act = lane < 31u && u < nv;
+      const bool tail = act && sh != 0 && ga + 2 * V > N;  // no upper block to shift in
+      W acc;
+      for (int k0 = 0; k0 < L; k0 += NB) {
+        uint4 blk[NB];
 #pragma unroll
-        for (int k = 0; k < US; ++k) {
-          u[k] = u0 + 31ull * k + lane;
-          ga[k] = g0 + u[k] * V - (unsigned long long)shift;  // block under vector u's start
-          load[k] = u[k] <= nv && ga[k] + V <= N;
-          act[k] = lane < 31u && u[k] < nv;
-          tail[k] = act[k] && sh != 0 && ga[k] + 2 * V > N;  // no upper block to shift in
-        }
-        W acc[US];
-        for (int k0 = 0; k0 < L; k0 += NB) {
-          uint4 blk[US][NB];
-#pragma unroll
-          for (int k = 0; k < US; ++k)
-#pragma unroll
-            for (int j = 0; j < NB; ++j)
-              if (k0 + j < L) {
-                int r = c + k0 + j;
-                r -= (r >= L) ? L : 0;
-                blk[k][j] = load[k] ? load_in<false, E>(p, r, ga[k] * E) : make_uint4(0u, 0u, 0u, 0u);
-              }
-#pragma unroll
-          for (int k = 0; k < US; ++k)
-#pragma unroll
-            for (int j = 0; j < NB; ++j)
-              if (k0 + j < L) {
-                const W x = VT::in(blk[k][j]);
-                acc[k] = (k0 + j == 0) ? x : VT::hop(acc[k], x);
-              }
-        }
-#pragma unroll
-        for (int k = 0; k < US; ++k) {
-          const uint4 res = VT::out(acc[k]);  // the folded block under output vector u[k]'s start
-          const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, res.x, 1), __shfl_down_sync(0xffffffffu, res.y, 1),
-                                      __shfl_down_sync(0xffffffffu, res.z, 1), __shfl_down_sync(0xffffffffu, res.w, 1));
-          if (tail[k]) {
-            for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, g0 + u[k] * V + e);
-          } else if (act[k]) {
-            store_out<true, E>(p, c, u[k] * V * E, sh ? funnel16(res, up, sh) : res);
+        for (int j = 0; j < NB; ++j)
+          if (k0 + j < L) {
+            int r = ce + k0 + j;
+            r -= (r >= L) ? L : 0;
+            blk[j] = load ? load_in<false, E>(p, r, ga * E) : make_uint4(0u, 0u, 0u, 0u);
           }
-        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          if (k0 + j < L) {
+            const W x = VT::in(blk[j]);
+            acc = (k0 + j == 0) ? x : VT::hop(acc, x);
+          }
       }
+      const uint4 res = VT::out(acc);
+      const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, res.x, 1), __shfl_down_sync(0xffffffffu, res.y, 1),
+                                  __shfl_down_sync(0xffffffffu, res.z, 1), __shfl_down_sync(0xffffffffu, res.w, 1));
+      if (tail) {
+        for (int e2 = 0; e2 < V; ++e2) element_op<OP, DT, WT>(p, g0 + u * V + e2);
+      } else if (act) {
+        store_out<true, E>(p, ce, u * VB, sh ? funnel16(res, up, sh) : res);
+      }
+    }
+    for (unsigned long long w = w0; w < n_inner; w += n_warps) {  // warp-uniform
+      if (p.prefetch & kPrefetchAhead) {
+        int c2 = c;
+        unsigned long long item2 = item;
+        advance(c2, item2);
+        if (w + n_warps < n_inner) prefetch_item(c2, item2);
+      }
+      const unsigned long long g0 = (unsigned long long)c * base;
+      const int sh = (int)(g0 % V) * E;  // bytes the chunk's vectors start into their aligned blocks
+      // row 0's block of this lane; row k's sits 31 k vectors further on
+      const unsigned long long u = item * per_item + lane, off = (g0 - g0 % V + u * V) * E;
+      W acc[US];
+      for (int k0 = 0; k0 < L; k0 += NB) {
+        uint4 blk[US][NB];
+#pragma unroll
+        for (int k = 0; k < US; ++k)
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            if (k0 + j < L) {
+              int r = c + k0 + j;
+              r -= (r >= L) ? L : 0;
+              blk[k][j] = load_in<false, E>(p, r, off + 31ull * VB * k);
+            }
+#pragma unroll
+        for (int k = 0; k < US; ++k)
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            if (k0 + j < L) {
+              const W x = VT::in(blk[k][j]);
+              acc[k] = (k0 + j == 0) ? x : VT::hop(acc[k], x);
+            }
+      }
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const uint4 res = VT::out(acc[k]);  // the folded block under output vector u + 31 k's start
+        const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, res.x, 1), __shfl_down_sync(0xffffffffu, res.y, 1),
+                                    __shfl_down_sync(0xffffffffu, res.z, 1), __shfl_down_sync(0xffffffffu, res.w, 1));
+        if (lane < 31u) store_out<true, E>(p, c, (u + 31ull * k) * VB, sh ? funnel16(res, up, sh) : res);
+      }
+      advance(c, item);
     }
     for (unsigned long long t = tid; t < (unsigned long long)L * V; t += T) {
       const int c = (int)(t / V), e = (int)(t % V);

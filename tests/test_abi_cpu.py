@@ -491,9 +491,19 @@ def test_direct_grid_waves(L):
     assert plan_dev(L, RS, 2, (64 << 20) // 2 + 2, F16)[2] == sms * 12
     st, _, grid, _ = plan_dev(L, RS, 4, (16 << 20) // 2 - 4 + 3, F16, cfg=(0, 0, 0, 0, 256))
     assert st == OK and grid == sms * 6                       # the same share of threads at 256 a CTA
+    # ReduceScatter over two ranks from 64 MiB per rank, chunks on the grid:
+    # the chunk-by-chunk kernel at four rows (two 256-thread CTAs' worth of
+    # registers per SM), twelve CTAs per SM; below 64 MiB the direct kernel
+    st, ch, grid, _ = plan_dev(L, RS, 2, 2 * (16 << 20), F16)
+    assert st == OK and ch["vectors"] == 4 and ch["ctas_per_sm"] == 2 and grid == sms * 12
+    st, ch, grid, _ = plan_dev(L, RS, 2, 2 * (4 << 20), F16)
+    assert st == OK and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3 and grid == sms * 6   # one wave
+    st, ch, _, _ = plan_dev(L, RS, 2, 2 * (16 << 20), F16, cfg=(3, 0, 0, 0, 0, 0, 0, 2))  # forced vectors: direct
+    assert st == OK and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
     # AllGather over two ranks below 64 MiB per rank: two waves of two
     # 256-thread CTAs' worth of registers per SM
     assert plan_dev(L, AG, 2, 2 * (8 << 20), F16)[2] == sms * 4 * 2
+    assert plan_dev(L, AG, 2, 2 * (256 << 10), F16)[2] == 2 * (256 << 10) * 2 // 16 // 128   # 1 MiB: one vector
     assert plan_dev(L, AG, 2, 2 * (64 << 20), F16)[2] == sms * 16
     assert plan_dev(L, AG, 3, 3 * (8 << 20), F16)[2] == sms * 16
     # a grid that fits under the cap is not changed (five ranks: no one-wave rule)
@@ -520,7 +530,7 @@ def test_one_wave_for_small_flat_rings(L):
     assert (v, occ, pf) == (1, 2, 3) and grid <= sms * 4
     assert plan(AR, 4, 64)[2] == sms * 6 * 2 or plan(AR, 4, 64)[2] == sms * 16   # the usual rules from 32 MiB
     vecs = 4 * MiB // 16
-    assert plan(AG, 4, 4)[0] == 1 and plan(AG, 4, 4)[2] == vecs // 128         # AllGather keeps its grid
+    assert plan(AG, 4, 4)[0] == 2 and plan(AG, 4, 4)[2] == vecs // 256         # AllGather keeps its grid
     assert plan(AR, 8, 4)[2] == vecs // 128                                     # five or more ranks too
     assert plan(AR, 8, 4, group=4)[2] == vecs // 256                            # two-level rings too
 
@@ -620,15 +630,22 @@ def test_planner_vectors_for_few_ranks(L):
     """The measured choices of vectors (rows) a thread: ReduceScatter over three
     ranks two vectors at three CTAs per SM; AllGather one vector (the L2
     prefetch keeps its loads in flight), two over two ranks below 64 MiB per
-    rank; the shifted ReduceScatter 4 rows for two ranks, 3 for three from 64
-    MiB per rank, else 2; the shifted AllGather 2."""
+    rank from 4 MiB, two over up to five ranks from 4 to 16 MiB; the shifted
+    ReduceScatter 2 rows, but 4 for two ranks from 8 MiB per rank, 1 for four
+    or more ranks below 8 MiB and 4 for eight or more from 128 MiB; the
+    shifted AllGather 2."""
     st, ch, _, _ = plan_dev(L, RS, 3, 3 * (1 << 22), F32)
     assert st == OK and ch["path"] == 3 and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
-    for R, n, vectors in ((2, 1 << 22, 2), (2, 1 << 24, 1), (3, 1 << 22, 1), (4, 1 << 22, 1)):
+    # (R, N / R, vectors): binary32, so N / R = 2^18 is 4 MiB per rank for R = 4
+    for R, n, vectors in ((2, 1 << 22, 2), (2, 1 << 24, 1), (2, 1 << 18, 1), (3, 1 << 20, 2), (4, 1 << 19, 2),
+                          (4, 1 << 18, 2), (5, 1 << 19, 2), (5, 1 << 22, 1), (8, 1 << 17, 1), (4, 1 << 17, 1),
+                          (4, 1 << 20, 1)):
         st, ch, _, _ = plan_dev(L, AG, R, R * n, F32)
         assert st == OK and ch["path"] == 3 and ch["vectors"] == vectors and ch["ctas_per_sm"] == 2, (R, n, ch)
-    for R, n, rows in ((2, 100_000, 4), (3, 100_000, 2), (3, 2_000_000, 3), (4, 100_000, 2), (8, 100_000, 2),
-                       (16, 100_000, 2)):
+    # (R, N / (8 R), rows): binary16, N = R (8 n + 3), so 8 n + 3 elements a chunk
+    for R, n, rows in ((2, 100_000, 2), (2, 1_000_000, 4), (3, 100_000, 2), (3, 2_000_000, 2), (4, 100_000, 1),
+                       (4, 1_000_000, 2), (5, 100_000, 1), (8, 100_000, 2), (8, 1_000_000, 2), (8, 10_000_000, 4),
+                       (16, 100_000, 2), (16, 10_000, 1)):
         st, ch, _, _ = plan_dev(L, RS, R, R * (8 * n + 3), F16)
         assert st == OK and ch["path"] == 3 and ch["vectors"] == rows, (R, ch)
     for R in (2, 3, 4, 5, 8):
@@ -655,8 +672,9 @@ def test_planner_prefetch_policy(L):
     rank or for up to four ranks a group; one iteration ahead for two ranks,
     AllGather, ReduceScatter over three ranks, and 8-64 MiB messages other
     than ReduceScatter over five or more ranks; never on the halving-doubling
-    kernels; the shifted AllGather both, the shifted ReduceScatter none
-    (prefetch reported as 1 + the bits)."""
+    kernels; the shifted AllGather both, the shifted ReduceScatter the first
+    item over three to five ranks below 32 MiB per rank, else none (prefetch
+    reported as 1 + the bits)."""
     MiB = 1 << 20
     def pf(op, R, mib, dt=F16, E=2, **kw):
         st, ch, _, _ = plan_dev(L, op, R, R * (mib * MiB // E // R // 8 * 8), dt, **kw)
@@ -675,6 +693,9 @@ def test_planner_prefetch_policy(L):
     assert pf(AR, 16, 64, group=8) == 0
     st, ch, _, _ = plan_dev(L, RS, 8, 8 * 1001, F16)  # shifted ReduceScatter: none
     assert st == OK and ch["prefetch"] == 1
+    for R, n, bits in ((2, 100_000, 0), (3, 100_000, HEAD), (5, 100_000, HEAD), (4, 3_000_000, 0)):
+        st, ch, _, _ = plan_dev(L, RS, R, R * (8 * n + 3), F16)
+        assert st == OK and ch["prefetch"] == 1 + bits, (R, n, ch)
     st, ch, _, _ = plan_dev(L, AG, 8, 8 * 1001, F16)  # shifted AllGather: both
     assert st == OK and ch["prefetch"] == 1 + (HEAD | AHEAD)
 

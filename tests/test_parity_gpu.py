@@ -681,6 +681,29 @@ def test_workload2_full_oracle(rr, wl, mib):
     check_ar(rr, xs, what=f"workload 2 {mib} MiB")
 
 
+@pytest.mark.parametrize("dtype,wire", [(torch.float16, None), (torch.float32, "bf16")], ids=lambda v: str(v))
+def test_reduce_scatter_two_ranks_chunk_by_chunk(rr, dtype, wire):
+    """ReduceScatter over two ranks from 64 MiB per rank with chunk boundaries
+    on the 16-byte grid: the planner takes the chunk-by-chunk (shifted) kernel,
+    which then shifts by nothing; the last chunk is ragged.  Every output
+    element equals the oracle's closed form."""
+    E = torch.tensor([], dtype=dtype).element_size()
+    base = (32 << 20) // E  # a multiple of the vector: 64 MiB per rank over two chunks
+    N = 2 * base + 3
+    xs = gen(2, N, dtype, 83 + E)
+    parts = [torch.full((rr.chunk_count(N, 2, c),), float("nan"), dtype=dtype, device="cuda") for c in range(2)]
+    plan = rr.plan(rr.OP_REDUCE_SCATTER, xs, parts, N, wire)
+    assert plan["path"] == rr.PATH_DIRECT and plan["vectors"] == 4 and plan["ctas_per_sm"] == 2, plan
+    rr.collective(rr.OP_REDUCE_SCATTER, xs, parts, N, wire)
+    torch.cuda.synchronize()
+    what = f"RS chunk by chunk {NAME[dtype]}/{wire} N={N}"
+    for c in range(2):
+        assert not torch.isnan(parts[c]).any(), f"{what}: chunk {c} has unwritten elements"
+    check_full(rr, xs, [torch.cat(parts)], wire=wire, what=what)
+    del parts, xs
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("mib", [128, 512])
 def test_workload2_full_size(rr, wl, mib):
     """The benchmark's workload in its launch configuration (staggered rank
