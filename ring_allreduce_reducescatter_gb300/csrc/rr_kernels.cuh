@@ -928,90 +928,136 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
   } else if (L <= 4) {
     // AllGather with few ranks, where the loads weigh most: rows of 32 output
     // vectors aligned to 32 vectors (512-byte store segments), clipped to one
-    // chunk; a warp's work item is US consecutive rows of one chunk, items
-    // numbered across the chunks.  Lane t loads the aligned source block under
-    // vector t's start, which is also the upper block lane t - 1 needs (a
-    // shuffle), and lane 31 loads its upper block itself; every row's loads
-    // are issued before any store.  Vectors over a chunk boundary (at most one
-    // per boundary, taken by the first boundary inside it), vectors whose
-    // upper block would pass the end of the chunk's buffer and the ragged end
-    // go element by element.
+    // chunk; a warp's work item is US consecutive rows of one chunk.  Lane t
+    // loads the aligned source block under vector t's start, which is also
+    // the upper block lane t - 1 needs (a shuffle), and lane 31 loads its
+    // upper block itself; every row's loads are issued before any store.
+    // Output vector v of chunk c (first vector wholly inside it: vf) starts
+    // (v - vf) V + s elements into the chunk's buffer, s = vf V - c base.
+    // With m = floor(len / V) for a chunk of len elements, every vector from
+    // vf to vf + m - 2 lies wholly in the chunk with both its source blocks
+    // inside the buffer, and the chunk has n = ceil((floor(m / 32) + 2) / US)
+    // items: the items from the second to the fourth last hold only such
+    // vectors (at most three items lie past vf + m - 2, one before vf), so
+    // they load and store without a check, and each chunk's first item and
+    // last three go first, a row to a warp, with the checks.  Vectors over a
+    // chunk boundary (at most one per boundary, taken by the first boundary
+    // inside it), vectors whose upper block would pass the end of the chunk's
+    // buffer and the ragged end go element by element.
     const unsigned lane = threadIdx.x & 31u;
     const unsigned long long warp = tid >> 5, n_warps = T >> 5;
     const unsigned long long nvec = p.n_bulk / V;  // output vectors wholly before the ragged end
     const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
     const unsigned long long rpc = (base / V + 64) / 32, rpl = (len_last / V + 64) / 32;  // rows per chunk, at most
     const unsigned long long ipc = (rpc + US - 1) / US, ipl = (rpl + US - 1) / US;        // items per chunk
-    const unsigned long long n_items = (unsigned long long)(L - 1) * ipc + ipl;
-    auto locate = [&](unsigned long long w, int &c, unsigned long long &item) {
-      if (w < (unsigned long long)(L - 1) * ipc) {
-        c = (int)(w / ipc);
-        item = w - (unsigned long long)c * ipc;
-      } else {
-        c = L - 1;
-        item = w - (unsigned long long)(L - 1) * ipc;
+    const unsigned long long inc = ipc > 4 ? ipc - 4 : 0, inl = ipl > 4 ? ipl - 4 : 0;    // inner items
+    const unsigned long long epc = (ipc - inc) * US, epl = (ipl - inl) * US;              // checked rows
+    const unsigned long long n_edge = (unsigned long long)(L - 1) * epc + epl;
+    const unsigned long long n_inner = (unsigned long long)(L - 1) * inc + inl;
+    // chunk c: its buffer's length, its first and (one past) last output
+    // vectors wholly inside it, the shift
+    struct Chunk {
+      unsigned long long len, vf, ve;
+      int sh;  // bytes a vector's source starts into its aligned block
+    };
+    auto chunk = [&](int c) {
+      Chunk k;
+      const unsigned long long cb = (unsigned long long)c * base;
+      k.len = c < L - 1 ? base : len_last;
+      k.vf = (cb + V - 1) / V;
+      k.ve = (cb + k.len) / V < nvec ? (cb + k.len) / V : nvec;
+      k.sh = (int)(k.vf * V - cb) * E;
+      return k;
+    };
+    // the inner item n_warps on (i counts a chunk's inner items): across
+    // chunk ends one at a time
+    auto advance = [&](int &c, unsigned long long &i) {
+      i += n_warps;
+      while (c < L - 1 && i >= inc) {
+        i -= inc;
+        ++c;
       }
     };
-    // L2 prefetch of the source block lane `lane` loads for item w
-    auto prefetch_item = [&](unsigned long long w) {
-      if (w >= n_items) return;
-      int c;
-      unsigned long long item;
-      locate(w, c, item);
-      const unsigned long long cb = (unsigned long long)c * base, len = c < L - 1 ? base : len_last;
-      const unsigned long long vf = (cb + V - 1) / V;
-      const unsigned long long ve = (cb + len) / V < nvec ? (cb + len) / V : nvec;
+    // the source blocks lane `lane` loads for inner item i of chunk c, into L2
+    auto prefetch_item = [&](int c, unsigned long long i) {
+      const Chunk k = chunk(c);
 #pragma unroll
-      for (int k = 0; k < US; ++k) {
-        const unsigned long long v = (vf / 32 + item * US + k) * 32 + lane;
-        if (v >= vf && v <= ve) {
-          const unsigned long long o = v * V - cb, oa = o - (o % V);
-          if (oa + V <= len) prefetch_in<true, E>(p, c, oa * E);
-        }
+      for (int r = 0; r < US; ++r) {
+        const unsigned long long v = (k.vf / 32 + (1 + i) * US + r) * 32 + lane;
+        prefetch_in<true, E>(p, c, (v - k.vf) * V * E);
       }
     };
-    if (p.prefetch & kPrefetchHead) prefetch_item(warp);
+    // work units, dealt to the warps in turn: first the checked rows, then
+    // the inner items; w0 is this warp's first inner item
+    const unsigned long long w0 =
+        warp < n_edge ? warp + (n_edge - warp + n_warps - 1) / n_warps * n_warps - n_edge : warp - n_edge;
+    int c = L - 1;
+    unsigned long long item = 0;
+    if (w0 < n_inner) {
+      if (w0 < (unsigned long long)(L - 1) * inc) {
+        c = (int)(w0 / inc);
+        item = w0 - (unsigned long long)c * inc;
+      } else {
+        item = w0 - (unsigned long long)(L - 1) * inc;
+      }
+      if (p.prefetch & kPrefetchHead) prefetch_item(c, item);
+    }
     grid_dependency_wait();
     grid_dependents_launch();
-    for (unsigned long long w = warp; w < n_items; w += n_warps) {  // warp-uniform
-      if (p.prefetch & kPrefetchAhead) prefetch_item(w + n_warps);
-      int c;
-      unsigned long long item;
-      locate(w, c, item);
-      const unsigned long long cb = (unsigned long long)c * base, len = c < L - 1 ? base : len_last;
-      const unsigned long long vf = (cb + V - 1) / V;  // first output vector wholly in the chunk
-      const unsigned long long ve = (cb + len) / V < nvec ? (cb + len) / V : nvec;  // one past the last
-      const int sh = (int)((vf * V - cb) % V) * E;     // where a vector's source starts in its aligned block
+    for (unsigned long long e = warp; e < n_edge; e += n_warps) {  // warp-uniform
+      // checked row e: chunk ce's first item, then its last ones
+      const int ce = e < (unsigned long long)(L - 1) * epc ? (int)(e / epc) : L - 1;
+      const unsigned long long u = e - (unsigned long long)ce * epc, j = u / US;
+      const unsigned long long in_c = ce < L - 1 ? inc : inl;
+      const unsigned long long it = (j == 0 || in_c == 0) ? j : j + in_c;  // the item
+      const Chunk k = chunk(ce);
+      const unsigned long long v = (k.vf / 32 + it * US + u % US) * 32 + lane;
+      const bool act = v >= k.vf && v < k.ve;
+      const unsigned long long oa = v >= k.vf ? (v - k.vf) * V : 0;  // the aligned source block under v's start
+      const bool load = v >= k.vf && v <= k.ve && oa + V <= k.len;
+      const bool tail = act && k.sh != 0 && oa + 2 * V > k.len;
+      const uint4 blk = load ? load_in<true, E>(p, ce, oa * E) : make_uint4(0u, 0u, 0u, 0u);
+      uint4 nxt = (lane == 31u && act && k.sh != 0 && !tail) ? load_in<true, E>(p, ce, (oa + V) * E)
+                                                             : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, blk.x, 1), __shfl_down_sync(0xffffffffu, blk.y, 1),
+                                  __shfl_down_sync(0xffffffffu, blk.z, 1), __shfl_down_sync(0xffffffffu, blk.w, 1));
+      if (lane != 31u) nxt = up;
+      if (tail) {
+        for (int e2 = 0; e2 < V; ++e2) element_op<OP, DT, WT>(p, v * V + e2);
+      } else if (act) {
+        const uint4 x = k.sh ? funnel16(blk, nxt, k.sh) : blk;
+        for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, v * V * E, x);
+      }
+    }
+    for (unsigned long long w = w0; w < n_inner; w += n_warps) {  // warp-uniform
+      if (p.prefetch & kPrefetchAhead) {
+        int c2 = c;
+        unsigned long long item2 = item;
+        advance(c2, item2);
+        if (w + n_warps < n_inner) prefetch_item(c2, item2);
+      }
+      const Chunk k = chunk(c);
+      const unsigned long long v0 = (k.vf / 32 + (1 + item) * US) * 32 + lane;  // row 0's vector
+      const unsigned long long oa0 = (v0 - k.vf) * V;  // its source block, elements into the buffer
       uint4 blk[US], nxt[US];
-      bool act[US], tail[US];
 #pragma unroll
-      for (int k = 0; k < US; ++k) {
-        const unsigned long long v = (vf / 32 + item * US + k) * 32 + lane;
-        act[k] = v >= vf && v < ve;
-        // the aligned source block under vector v's start (o - oa = sh / E for every v of the chunk)
-        const unsigned long long o = v * V - cb, oa = o - (o % V);
-        const bool load = v >= vf && v <= ve && oa + V <= len;
-        tail[k] = act[k] && sh != 0 && oa + 2 * V > len;
-        blk[k] = load ? load_in<true, E>(p, c, oa * E) : make_uint4(0u, 0u, 0u, 0u);
-        nxt[k] = (lane == 31u && act[k] && sh != 0 && !tail[k]) ? load_in<true, E>(p, c, (oa + V) * E)
-                                                               : make_uint4(0u, 0u, 0u, 0u);
+      for (int r = 0; r < US; ++r) {
+        blk[r] = load_in<true, E>(p, c, (oa0 + 32ull * V * r) * E);
+        nxt[r] = (lane == 31u && k.sh != 0) ? load_in<true, E>(p, c, (oa0 + 32ull * V * r + V) * E)
+                                            : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int k = 0; k < US; ++k) {
-        const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, blk[k].x, 1), __shfl_down_sync(0xffffffffu, blk[k].y, 1),
-                                    __shfl_down_sync(0xffffffffu, blk[k].z, 1), __shfl_down_sync(0xffffffffu, blk[k].w, 1));
-        if (lane != 31u) nxt[k] = up;
+      for (int r = 0; r < US; ++r) {
+        const uint4 up = make_uint4(__shfl_down_sync(0xffffffffu, blk[r].x, 1), __shfl_down_sync(0xffffffffu, blk[r].y, 1),
+                                    __shfl_down_sync(0xffffffffu, blk[r].z, 1), __shfl_down_sync(0xffffffffu, blk[r].w, 1));
+        if (lane != 31u) nxt[r] = up;
       }
 #pragma unroll
-      for (int k = 0; k < US; ++k) {
-        const unsigned long long v = (vf / 32 + item * US + k) * 32 + lane;
-        if (tail[k]) {
-          for (int e = 0; e < V; ++e) element_op<OP, DT, WT>(p, v * V + e);
-        } else if (act[k]) {
-          const uint4 x = sh ? funnel16(blk[k], nxt[k], sh) : blk[k];
-          for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, v * V * E, x);
-        }
+      for (int r = 0; r < US; ++r) {
+        const uint4 x = k.sh ? funnel16(blk[r], nxt[r], k.sh) : blk[r];
+        for (int q = 0; q < p.R; ++q) store_out<false, E>(p, q, (v0 + 32ull * r) * V * E, x);
       }
+      advance(c, item);
     }
     for (unsigned long long b = 1 + tid; b < (unsigned long long)L; b += T) {  // vectors over a boundary
       const unsigned long long gb = b * base, vb = gb / V;

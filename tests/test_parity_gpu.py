@@ -573,8 +573,9 @@ def check_full(rr, xs, outs, wire=None, group=0, algo="ring", what="", piece=1 <
     element's fold depends only on its own chunk), so the split cannot change
     a bit, and ctypes releases the interpreter lock during the oracle call.
     Inputs and output come back from the device one piece at a time, so host
-    memory stays bounded.  Every other output must equal output 0 bit for bit
-    (compared on the device)."""
+    memory stays bounded.  Every other output in outs must equal output 0 bit
+    for bit (compared on the device); a ReduceScatter passes its chunks joined
+    as the one output."""
     R, N = len(xs), xs[0].numel()
     dt = NAME[xs[0].dtype]
     workers = full_check_workers()
@@ -609,7 +610,7 @@ def check_full(rr, xs, outs, wire=None, group=0, algo="ring", what="", piece=1 <
                 failures.append(err)
     assert not failures, f"{what} rank 0: " + "; ".join(failures[:4])
     iv = torch.int16 if outs[0].element_size() == 2 else torch.int32
-    for r in range(1, R):
+    for r in range(1, len(outs)):
         assert torch.equal(outs[r].view(iv), outs[0].view(iv)), f"{what}: output {r} differs from output 0"
 
 
