@@ -725,7 +725,7 @@ def run_ours(args):
         e2e = {"value": round(job_throughput(world, msg, e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": R * msg, "d2h_bytes_per_step": R * msg, "ms_per_step": round(e_ms, 4),
                "step_ms_min": round(min(step_ms), 3), "step_ms_median": round(statistics.median(step_ms), 3),
-               "step_ms_max": round(max(step_ms), 3),
+               "step_ms_max": round(max(step_ms), 3), "step_ms_all": [round(t, 3) for t in step_ms],
                "steps": args.e2e_steps, "api": "ring_allreduce_host_ex",
                "copy_mode": "one_way" if one_way else "overlap",
                "piece_mib_per_rank": args.e2e_piece_mib, "host_affinity": affinity, "link": link}

@@ -320,16 +320,23 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
       // 5 0.40 -> 0.47, R = 8 0.66 -> 0.71, R = 16 0.72 -> 0.82; at 16 MiB
       // one row lost 1-18 %), four for eight or more ranks from 128 MiB (256
       // MiB: R = 8 0.95 -> 0.98, R = 16 0.97 -> 1.00; at 64 MiB 0-1 % lost).
-      // AllGather, at 16 / 256 MiB per rank: R = 2 two rows 0.68 / 0.82, four
-      // 0.63 / 0.83; R = 3 two rows 0.79 / 0.92; R = 4 two rows 0.84 / 0.94;
-      // R = 8 two vectors a thread 0.83 / 0.93, one 0.84 / 0.86.
+      // AllGather: rows of 32 vectors for up to four ranks (two rows; R = 2
+      // at 16 / 256 MiB: two 0.68 / 0.82, four 0.63 / 0.83) and for more from
+      // 16 MiB per rank, two rows, four for eight or more ranks from 64 MiB;
+      // below 16 MiB five or more ranks take one vector a thread a grid-stride
+      // apart.  Measured, binary16, of the copy bandwidth, against vectors a
+      // thread at 16 / 64 / 256 MiB: R = 5 0.82 / 0.91 / 0.91 -> 0.94 / 0.94 /
+      // 0.95, R = 8 0.88 / 0.92 / 0.93 -> 0.96 / 0.95 / 0.93, R = 16 0.94 /
+      // 0.94 / 0.94 -> 0.96 / 0.95 / 0.94; at 1 and 4 MiB rows lost 7-25 %,
+      // and one vector a thread beat two by 1-13 %.
       if (ck.op == RR_OP_REDUCE_SCATTER) {
         U = 2;
         if (ck.L == 2 && msg_bytes >= (8ull << 20)) U = 4;
         if (ck.L >= 4 && msg_bytes < (8ull << 20)) U = 1;
         if (ck.L >= 8 && msg_bytes >= (128ull << 20)) U = 4;
       } else {
-        U = 2;
+        p->shift_rows = (ck.L <= 4 || msg_bytes >= (16ull << 20)) ? 1 : 0;
+        U = !p->shift_rows ? 1 : (ck.L >= 8 && msg_bytes >= (64ull << 20)) ? 4 : 2;
       }
     }
     if (wide && U > 2) U = 2;

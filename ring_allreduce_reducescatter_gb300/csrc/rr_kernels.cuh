@@ -925,10 +925,11 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
       const unsigned long long len = c < L - 1 ? base : len_last, full = len / V * V;
       if (full + e < len) element_op<OP, DT, WT>(p, (unsigned long long)c * base + full + e);
     }
-  } else if (L <= 4) {
-    // AllGather with few ranks, where the loads weigh most: rows of 32 output
-    // vectors aligned to 32 vectors (512-byte store segments), clipped to one
-    // chunk; a warp's work item is US consecutive rows of one chunk.  Lane t
+  } else if (p.shift_rows) {
+    // AllGather over up to four ranks (where the loads weigh most), and over
+    // more from 16 MiB per rank: rows of 32 output vectors aligned to 32
+    // vectors (512-byte store segments), clipped to one chunk; a warp's work
+    // item is US consecutive rows of one chunk.  Lane t
     // loads the aligned source block under vector t's start, which is also
     // the upper block lane t - 1 needs (a shuffle), and lane 31 loads its
     // upper block itself; every row's loads are issued before any store.
@@ -1067,9 +1068,10 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     }
     for (unsigned long long i = p.n_bulk + tid; i < p.count; i += T) element_op<OP, DT, WT>(p, i);
   } else {
-    // AllGather: each thread takes US output vectors a grid-stride apart and
-    // builds each from the two aligned blocks of its chunk's input under it
-    // (the second served by L1); all loads before the stores
+    // AllGather over five or more ranks below 16 MiB per rank: each thread
+    // takes US output vectors a grid-stride apart and builds each from the
+    // two aligned blocks of its chunk's input under it (the second served by
+    // L1); all loads before the stores
     const unsigned long long nvec = p.n_bulk / V;
     // L2 prefetch of the lower source blocks of vectors v0, v0 + T, ...
     auto prefetch_vecs = [&](unsigned long long v0) {

@@ -49,6 +49,7 @@ struct RingParams {
   int prefetch;                   // direct path: kPrefetch* bits
   unsigned long long debug_margin;  // debug build: bytes taken off every buffer's extent by the checks
   int chunks_on_grid;             // every chunk boundary of this launch falls on the 16-byte vector grid
+  int shift_rows;                 // shifted AllGather: rows of 32 output vectors a warp item (else vectors a thread)
 };
 
 // L2 prefetch of the direct path's inputs (no data reaches the SM, so no

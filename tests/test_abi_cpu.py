@@ -632,8 +632,7 @@ def test_planner_vectors_for_few_ranks(L):
     prefetch keeps its loads in flight), two over two ranks below 64 MiB per
     rank from 4 MiB, two over up to five ranks from 4 to 16 MiB; the shifted
     ReduceScatter 2 rows, but 4 for two ranks from 8 MiB per rank, 1 for four
-    or more ranks below 8 MiB and 4 for eight or more from 128 MiB; the
-    shifted AllGather 2."""
+    or more ranks below 8 MiB and 4 for eight or more from 128 MiB."""
     st, ch, _, _ = plan_dev(L, RS, 3, 3 * (1 << 22), F32)
     assert st == OK and ch["path"] == 3 and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
     # (R, N / R, vectors): binary32, so N / R = 2^18 is 4 MiB per rank for R = 4
@@ -648,9 +647,13 @@ def test_planner_vectors_for_few_ranks(L):
                        (16, 100_000, 2), (16, 10_000, 1)):
         st, ch, _, _ = plan_dev(L, RS, R, R * (8 * n + 3), F16)
         assert st == OK and ch["path"] == 3 and ch["vectors"] == rows, (R, ch)
-    for R in (2, 3, 4, 5, 8):
-        st, ch, _, _ = plan_dev(L, AG, R, R * (8 * 100_000 + 3), F16)
-        assert st == OK and ch["path"] == 3 and ch["vectors"] == 2, (R, ch)
+    # the shifted AllGather: two rows for up to four ranks; for more, one
+    # vector a thread below 16 MiB per rank, else two rows (four for eight or
+    # more ranks from 64 MiB)
+    for R, n, vectors in ((2, 100_000, 2), (3, 100_000, 2), (4, 100_000, 2), (5, 100_000, 1), (8, 100_000, 1),
+                          (5, 1_000_000, 2), (8, 1_000_000, 4), (16, 200_000, 2), (16, 2_000_000, 4)):
+        st, ch, _, _ = plan_dev(L, AG, R, R * (8 * n + 3), F16)
+        assert st == OK and ch["path"] == 3 and ch["vectors"] == vectors, (R, n, ch)
 
 
 def test_beside_compute_caps_the_grid(L):

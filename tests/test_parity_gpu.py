@@ -262,6 +262,32 @@ def test_shifted_reduce_scatter_and_allgather(rr, dtype, wire):
                 check_ag(rr, chunks, N, cfg=cfg, what="AG " + tag)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16], ids=lambda v: str(v))
+def test_shifted_allgather_rows_many_ranks(rr, dtype):
+    """AllGather over five and eight ranks from 16 MiB per rank with chunk
+    boundaries off the 16-byte grid: the shifted kernel in rows of 32 vectors,
+    each row count the library builds.  Every output is the chunks joined, bit
+    for bit."""
+    E = torch.tensor([], dtype=dtype).element_size()
+    V = 16 // E
+    iv = torch.int16 if E == 2 else torch.int32
+    for R in (5, 8):
+        base = (16 << 20) // (E * R) // V * V + 1  # off the grid; R * base * E >= 16 MiB
+        N = R * base + (R - 2)
+        lens = [rr.chunk_count(N, R, c) for c in range(R)]
+        chunks = gen(R, 0, dtype, 29 * R + E, lengths=lens)
+        want = torch.cat(chunks).view(iv)
+        for rows in (0, 1, 2, 4):  # 0: the planner's choice
+            cfg = rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, 0, 0, rows) if rows else None
+            outs = [torch.full((N,), float("nan"), dtype=dtype, device="cuda") for _ in range(R)]
+            rr.collective(rr.OP_ALLGATHER, chunks, outs, N, None, 0, None, cfg)
+            torch.cuda.synchronize()
+            for r in range(R):
+                assert torch.equal(outs[r].view(iv), want), f"AG rows {NAME[dtype]} R={R} rows={rows} rank {r}"
+            del outs
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("algo", ["hd", "naive"])
 def test_allgather_equals_every_schedule(rr, algo):
     """On one GPU the AllGather is a copy: ring_allgather's outputs equal the
