@@ -273,6 +273,19 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   if (path == RR_PATH_DIRECT && ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && ck.L == 2 &&
       (unsigned long long)ck.count * E >= (64ull << 20) && c.vectors == 0 && c.ctas_per_sm == 0)
     p->shifted = 1;
+  // AllGather from 12 MiB per rank (two ranks: 64 MiB) likewise, in rows of 32
+  // vectors of one chunk that end on 512-byte store segments.  Measured,
+  // binary16, of the copy bandwidth, direct -> rows on aligned chunks at 16 /
+  // 64 / 256 MiB per rank: R = 4 0.87 / 0.89 / 0.93 -> 0.94 / 0.95 / 0.95, R =
+  // 8 0.89 / 0.91 / 0.92 -> 0.96 / 0.95 / 0.94, R = 16 0.90 / 0.90 / 0.90 ->
+  // 0.96 / 0.95 / 0.94; R = 3 / 5 at 64 MiB 0.88 / 0.91 -> 0.93 / 0.94; R = 2
+  // at 64 / 256 MiB 0.88 / 0.92 -> 0.92 / 0.96 (at 16 MiB 0.80 -> 0.77); at
+  // 12 MiB R = 8 / 16 0.88 / 0.89 -> 0.95 / 0.96; at 8 MiB rows lost up to 6 %,
+  // at 4 MiB up to 35 %.
+  if (path == RR_PATH_DIRECT && ck.op == RR_OP_ALLGATHER && ck.algo == RR_ALGO_RING &&
+      (unsigned long long)ck.count * E >= (ck.L == 2 ? (64ull << 20) : (12ull << 20)) && c.vectors == 0 &&
+      c.ctas_per_sm == 0)
+    p->shifted = 1;
 
   l->path = path;
   // 128-thread CTAs on the direct path: finer grid granularity, measured 1-5 %
@@ -322,20 +335,21 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
       // MiB: R = 8 0.95 -> 0.98, R = 16 0.97 -> 1.00; at 64 MiB 0-1 % lost).
       // AllGather: rows of 32 vectors for up to four ranks (two rows; R = 2
       // at 16 / 256 MiB: two 0.68 / 0.82, four 0.63 / 0.83) and for more from
-      // 16 MiB per rank, two rows, four for eight or more ranks from 64 MiB;
-      // below 16 MiB five or more ranks take one vector a thread a grid-stride
+      // 12 MiB per rank, two rows, four for eight or more ranks from 64 MiB;
+      // below that five or more ranks take one vector a thread a grid-stride
       // apart.  Measured, binary16, of the copy bandwidth, against vectors a
-      // thread at 16 / 64 / 256 MiB: R = 5 0.82 / 0.91 / 0.91 -> 0.94 / 0.94 /
-      // 0.95, R = 8 0.88 / 0.92 / 0.93 -> 0.96 / 0.95 / 0.93, R = 16 0.94 /
-      // 0.94 / 0.94 -> 0.96 / 0.95 / 0.94; at 1 and 4 MiB rows lost 7-25 %,
-      // and one vector a thread beat two by 1-13 %.
+      // thread at 12 / 16 / 64 / 256 MiB: R = 5 0.83 / 0.82 / 0.91 / 0.91 ->
+      // 0.86 / 0.94 / 0.94 / 0.95, R = 8 0.85 / 0.88 / 0.92 / 0.93 -> 0.92 /
+      // 0.96 / 0.95 / 0.93, R = 16 0.92 / 0.94 / 0.94 / 0.94 -> 0.95 / 0.96 /
+      // 0.95 / 0.94; at 8 MiB rows lost up to 4 %, at 1 and 4 MiB 7-25 %, and
+      // one vector a thread beat two by 1-13 %.
       if (ck.op == RR_OP_REDUCE_SCATTER) {
         U = 2;
         if (ck.L == 2 && msg_bytes >= (8ull << 20)) U = 4;
         if (ck.L >= 4 && msg_bytes < (8ull << 20)) U = 1;
         if (ck.L >= 8 && msg_bytes >= (128ull << 20)) U = 4;
       } else {
-        p->shift_rows = (ck.L <= 4 || msg_bytes >= (16ull << 20)) ? 1 : 0;
+        p->shift_rows = (ck.L <= 4 || msg_bytes >= (12ull << 20)) ? 1 : 0;
         U = !p->shift_rows ? 1 : (ck.L >= 8 && msg_bytes >= (64ull << 20)) ? 4 : 2;
       }
     }

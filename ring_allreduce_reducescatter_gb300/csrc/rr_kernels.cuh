@@ -34,8 +34,9 @@
 //    from HBM in batches of eight loads, folds them in registers and stores
 //    the result to every output; one extra CTA folds the AllReduce vectors
 //    that straddle a chunk boundary.
-//  rr_shift_kernel: ReduceScatter / AllGather whose chunk boundaries are off
-//    the 16-byte grid (vectors built from two aligned blocks).
+//  rr_shift_kernel: ReduceScatter / AllGather chunk by chunk, for chunk
+//    boundaries off the 16-byte grid (vectors built from two aligned blocks)
+//    and, unshifted, for large AllGathers and two-rank ReduceScatters.
 //  The halving-doubling direct kernels are in rr_hd_direct.cuh.
 //  Every kernel starts with the programmatic-launch wait, so a launch may
 //  overlap the kernel before it on the stream.
@@ -760,11 +761,12 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
 }
 
 // --------------------------------------------------------------------------
-// ReduceScatter / AllGather whose chunk boundaries are off the 16-byte grid:
-// the chunk-local buffers (the ReduceScatter outputs, the AllGather inputs)
-// are then shifted against the rank vectors by (c * base) mod V elements.
-// Each thread takes one 16-byte vector aligned in the shifted buffer and
-// builds the matching bytes of the other side from two aligned loads.
+// ReduceScatter / AllGather chunk by chunk.  Where the chunk boundaries are
+// off the 16-byte grid, the chunk-local buffers (the ReduceScatter outputs,
+// the AllGather inputs) are shifted against the rank vectors by (c * base)
+// mod V elements, and each 16-byte vector aligned in the shifted buffer is
+// built from two aligned blocks of the other side; on the grid the shift is
+// zero and each vector is one block.
 // --------------------------------------------------------------------------
 
 // US: rows of output vectors a warp takes at once (ReduceScatter, and
@@ -927,9 +929,10 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     }
   } else if (p.shift_rows) {
     // AllGather over up to four ranks (where the loads weigh most), and over
-    // more from 16 MiB per rank: rows of 32 output vectors aligned to 32
-    // vectors (512-byte store segments), clipped to one chunk; a warp's work
-    // item is US consecutive rows of one chunk.  Lane t
+    // more from 12 MiB per rank (also with the chunks on the grid, unshifted,
+    // from 12 MiB, two ranks from 64 MiB): rows of 32 output vectors aligned
+    // to 32 vectors (512-byte store segments), clipped to one chunk; a warp's
+    // work item is US consecutive rows of one chunk.  Lane t
     // loads the aligned source block under vector t's start, which is also
     // the upper block lane t - 1 needs (a shuffle), and lane 31 loads its
     // upper block itself; every row's loads are issued before any store.
@@ -1068,7 +1071,7 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
     }
     for (unsigned long long i = p.n_bulk + tid; i < p.count; i += T) element_op<OP, DT, WT>(p, i);
   } else {
-    // AllGather over five or more ranks below 16 MiB per rank: each thread
+    // AllGather over five or more ranks below 12 MiB per rank: each thread
     // takes US output vectors a grid-stride apart and builds each from the
     // two aligned blocks of its chunk's input under it (the second served by
     // L1); all loads before the stores

@@ -635,12 +635,16 @@ def test_planner_vectors_for_few_ranks(L):
     or more ranks below 8 MiB and 4 for eight or more from 128 MiB."""
     st, ch, _, _ = plan_dev(L, RS, 3, 3 * (1 << 22), F32)
     assert st == OK and ch["path"] == 3 and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
-    # (R, N / R, vectors): binary32, so N / R = 2^18 is 4 MiB per rank for R = 4
-    for R, n, vectors in ((2, 1 << 22, 2), (2, 1 << 24, 1), (2, 1 << 18, 1), (3, 1 << 20, 2), (4, 1 << 19, 2),
-                          (4, 1 << 18, 2), (5, 1 << 19, 2), (5, 1 << 22, 1), (8, 1 << 17, 1), (4, 1 << 17, 1),
-                          (4, 1 << 20, 1)):
+    # (R, N / R, vectors, register budget): binary32, so N / R = 2^18 is 4 MiB
+    # per rank for R = 4; from 12 MiB per rank (two ranks: 64 MiB) the rows of
+    # the chunk-by-chunk kernel (two rows at three CTAs per SM, four rows at
+    # two for eight or more ranks from 64 MiB)
+    for R, n, vectors, occ in ((2, 1 << 22, 2, 2), (2, 1 << 24, 2, 3), (2, 1 << 18, 1, 2), (3, 1 << 20, 2, 3),
+                               (4, 1 << 19, 2, 2), (4, 1 << 18, 2, 2), (5, 1 << 19, 2, 2), (5, 1 << 22, 2, 3),
+                               (8, 1 << 17, 1, 2), (4, 1 << 17, 1, 2), (4, 1 << 20, 2, 3), (8, 1 << 21, 4, 2),
+                               (16, 1 << 18, 2, 3)):
         st, ch, _, _ = plan_dev(L, AG, R, R * n, F32)
-        assert st == OK and ch["path"] == 3 and ch["vectors"] == vectors and ch["ctas_per_sm"] == 2, (R, n, ch)
+        assert st == OK and ch["path"] == 3 and ch["vectors"] == vectors and ch["ctas_per_sm"] == occ, (R, n, ch)
     # (R, N / (8 R), rows): binary16, N = R (8 n + 3), so 8 n + 3 elements a chunk
     for R, n, rows in ((2, 100_000, 2), (2, 1_000_000, 4), (3, 100_000, 2), (3, 2_000_000, 2), (4, 100_000, 1),
                        (4, 1_000_000, 2), (5, 100_000, 1), (8, 100_000, 2), (8, 1_000_000, 2), (8, 10_000_000, 4),
@@ -648,9 +652,10 @@ def test_planner_vectors_for_few_ranks(L):
         st, ch, _, _ = plan_dev(L, RS, R, R * (8 * n + 3), F16)
         assert st == OK and ch["path"] == 3 and ch["vectors"] == rows, (R, ch)
     # the shifted AllGather: two rows for up to four ranks; for more, one
-    # vector a thread below 16 MiB per rank, else two rows (four for eight or
+    # vector a thread below 12 MiB per rank, else two rows (four for eight or
     # more ranks from 64 MiB)
-    for R, n, vectors in ((2, 100_000, 2), (3, 100_000, 2), (4, 100_000, 2), (5, 100_000, 1), (8, 100_000, 1),
+    for R, n, vectors in ((2, 100_000, 2), (3, 100_000, 2), (4, 100_000, 2), (5, 100_000, 1), (8, 50_000, 1),
+                          (8, 100_000, 2),
                           (5, 1_000_000, 2), (8, 1_000_000, 4), (16, 200_000, 2), (16, 2_000_000, 4)):
         st, ch, _, _ = plan_dev(L, AG, R, R * (8 * n + 3), F16)
         assert st == OK and ch["path"] == 3 and ch["vectors"] == vectors, (R, n, ch)
@@ -691,7 +696,9 @@ def test_planner_prefetch_policy(L):
     assert pf(AR, 2, 256) == HEAD | AHEAD
     assert pf(RS, 8, 16) == HEAD
     assert pf(RS, 3, 256) == HEAD | AHEAD
-    assert pf(AG, 8, 256) == AHEAD
+    assert pf(AG, 8, 256) == HEAD | AHEAD  # the chunk-by-chunk rows from 16 MiB: both
+    assert pf(AG, 8, 4) == HEAD | AHEAD
+    assert pf(AG, 2, 128) == HEAD | AHEAD
     assert pf(AR, 4, 4, F32, 4) == HEAD | AHEAD  # a small flat ring of four: one wave, both
     assert pf(AR, 16, 64, group=8) == 0
     st, ch, _, _ = plan_dev(L, RS, 8, 8 * 1001, F16)  # shifted ReduceScatter: none

@@ -288,6 +288,32 @@ def test_shifted_allgather_rows_many_ranks(rr, dtype):
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=lambda v: str(v))
+def test_allgather_rows_aligned_chunks(rr, dtype):
+    """AllGather from 16 MiB per rank (two ranks: 64 MiB) with chunk boundaries
+    on the 16-byte grid: the planner takes the chunk-by-chunk rows, which then
+    shift by nothing; a ragged last chunk.  Every output is the chunks joined,
+    bit for bit."""
+    E = torch.tensor([], dtype=dtype).element_size()
+    V = 16 // E
+    iv = torch.int16 if E == 2 else torch.int32
+    for R, mib in ((2, 64), (3, 16), (8, 16)):
+        base = -(-(mib << 20) // (E * R * V)) * V  # a multiple of V; R * base * E >= mib MiB
+        N = R * base + (R - 1)
+        lens = [rr.chunk_count(N, R, c) for c in range(R)]
+        chunks = gen(R, 0, dtype, 31 * R + E, lengths=lens)
+        outs = [torch.full((N,), float("nan"), dtype=dtype, device="cuda") for _ in range(R)]
+        plan = rr.plan(rr.OP_ALLGATHER, chunks, outs, N)
+        assert plan["path"] == rr.PATH_DIRECT and plan["vectors"] == 2 and plan["ctas_per_sm"] == 3, (R, plan)
+        rr.collective(rr.OP_ALLGATHER, chunks, outs, N)
+        torch.cuda.synchronize()
+        want = torch.cat(chunks).view(iv)
+        for r in range(R):
+            assert torch.equal(outs[r].view(iv), want), f"AG rows aligned {NAME[dtype]} R={R} rank {r}"
+        del outs
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("algo", ["hd", "naive"])
 def test_allgather_equals_every_schedule(rr, algo):
     """On one GPU the AllGather is a copy: ring_allgather's outputs equal the
