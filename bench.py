@@ -781,10 +781,11 @@ def sweep_variants(rr, op, wide, shifted, all_variants, prefetch=False, explicit
         for item in explicit.split(";"):
             vals = [int(v) for v in item.split(",")]
             path, u, occ, pf = vals[:4]
-            cap, threads, early = (vals[4:] + [0, 0, 0])[:3]
+            cap, threads, early, tile, stages = (vals[4:] + [0, 0, 0, 0, 0])[:5]
             label = f"path={path} U={u} occ={occ} prefetch={pf}" + (f" max_ctas={cap}" if cap else "")
             label += (f" threads={threads}" if threads else "") + (f" early={early}" if early else "")
-            out.append((label, rr.LaunchCfg(path, 0, 0, occ, threads, cap, early, u, 0, pf)))
+            label += (f" tile={tile}" if tile else "") + (f" stages={stages}" if stages else "")
+            out.append((label, rr.LaunchCfg(path, tile, stages, occ, threads, cap, early, u, 0, pf)))
         return out
     if prefetch and not shifted:
         for pf, name in ((1, "none"), (2, "head"), (3, "ahead"), (4, "head+ahead")):
@@ -1024,7 +1025,8 @@ def main():
     ap.add_argument("--sweep-table", default="", help="also write the tile-vs-direct table (markdown) to this file")
     ap.add_argument("--sweep-cfg", default="",
                     help="explicit launch configurations "
-                         "'path,vectors,ctas_per_sm,prefetch[,max_ctas[,threads[,early_launch]]];...' "
+                         "'path,vectors,ctas_per_sm,prefetch[,max_ctas[,threads[,early_launch[,tile_bytes"
+                         "[,stages]]]]];...' "
                          "(with auto)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
