@@ -286,6 +286,20 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
       (unsigned long long)ck.count * E >= (ck.L == 2 ? (64ull << 20) : (12ull << 20)) && c.vectors == 0 &&
       c.ctas_per_sm == 0)
     p->shifted = 1;
+  // AllReduce over flat rings of two to four ranks from 16 MiB per rank, the
+  // chunks on the grid and the whole rank vectors in one call (no range): the
+  // same chunk-by-chunk rows, folding each row's vectors and storing the sum
+  // to every output.  Measured, binary16, of the copy bandwidth, direct ->
+  // rows at 16 / 32 / 128 / 256 MiB per rank: R = 2 0.82 / 0.88 / 0.94 / 0.93
+  // -> 0.87 / 0.90 / 0.99 / 0.98, R = 3 (24 / 32 / 128 / 256 MiB) 0.93 / 0.91
+  // / 0.96 / 0.96 -> 0.94 / 0.95 / 1.00 / 1.00, R = 4 0.94 / 0.98 / 0.97 /
+  // 0.97 -> 0.97 / 0.97 / 1.00 / 0.99; binary32 at 64 MiB R = 2 / 4 0.94 /
+  // 0.96 -> 0.95 / 0.99.  (R = 2 at 24 MiB lost 2-3 %.)
+  if (path == RR_PATH_DIRECT && ck.op == RR_OP_ALLREDUCE && ck.algo == RR_ALGO_RING && ck.L == ck.R && ck.L >= 2 &&
+      ck.L <= 4 && ck.first == 0 && ck.n == ck.count && (p->base * E) % 16 == 0 &&
+      !(ck.dtype != RR_FP32 && ck.wire == RR_FP32) && (unsigned long long)ck.count * E >= (16ull << 20) &&
+      c.ctas_per_sm == 0)
+    p->shifted = 1;
 
   l->path = path;
   // 128-thread CTAs on the direct path: finer grid granularity, measured 1-5 %
@@ -343,7 +357,9 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
       // 0.96 / 0.95 / 0.93, R = 16 0.92 / 0.94 / 0.94 / 0.94 -> 0.95 / 0.96 /
       // 0.95 / 0.94; at 8 MiB rows lost up to 4 %, at 1 and 4 MiB 7-25 %, and
       // one vector a thread beat two by 1-13 %.
-      if (ck.op == RR_OP_REDUCE_SCATTER) {
+      if (ck.op == RR_OP_ALLREDUCE) {  // four rows for two ranks from 64 MiB, for more from 128 MiB
+        U = ((ck.L == 2 && msg_bytes >= (64ull << 20)) || msg_bytes >= (128ull << 20)) ? 4 : 2;
+      } else if (ck.op == RR_OP_REDUCE_SCATTER) {
         U = 2;
         if (ck.L == 2 && msg_bytes >= (8ull << 20)) U = 4;
         if (ck.L >= 4 && msg_bytes < (8ull << 20)) U = 1;
@@ -355,9 +371,10 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     }
     if (wide && U > 2) U = 2;
     // Flat rings of up to four ranks under 32 MiB per rank (ring order,
-    // AllReduce / ReduceScatter, chunks on the grid): one wave of resident
-    // CTAs whose threads loop, with the L2 prefetch of the first and the next
-    // iteration, instead of several waves with a partial last one.  One vector
+    // AllReduce below the chunk-by-chunk rows' 16 MiB and ReduceScatter,
+    // chunks on the grid): one wave of resident CTAs whose threads loop, with
+    // the L2 prefetch of the first and the next iteration, instead of several
+    // waves with a partial last one.  One vector
     // a thread where two would leave SMs idle (under two vectors per thread of
     // a wave of two 256-thread CTAs per SM); two CTAs per SM up to 8 MiB, three
     // above.  Measured (binary16 unless stated, of the copy bandwidth, median of
@@ -406,6 +423,8 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
     if (p->shifted && c.prefetch == 0) {
       if (ck.op == RR_OP_ALLGATHER)
         p->prefetch = rr::kPrefetchHead | rr::kPrefetchAhead;
+      else if (ck.op == RR_OP_ALLREDUCE)  // the first item below 24 MiB (16 MiB: R = 2 0.84 -> 0.87, R = 4
+        p->prefetch = msg_bytes < (24ull << 20) ? rr::kPrefetchHead : 0;  // 0.94 -> 0.97), none above (1-3 %)
       else
         p->prefetch = (ck.L >= 3 && ck.L <= 5 && msg_bytes < (32ull << 20)) ? rr::kPrefetchHead : 0;
     }

@@ -36,7 +36,8 @@
 //    that straddle a chunk boundary.
 //  rr_shift_kernel: ReduceScatter / AllGather chunk by chunk, for chunk
 //    boundaries off the 16-byte grid (vectors built from two aligned blocks)
-//    and, unshifted, for large AllGathers and two-rank ReduceScatters.
+//    and, unshifted, for large AllGathers, two-rank ReduceScatters and
+//    AllReduces over two to four ranks.
 //  The halving-doubling direct kernels are in rr_hd_direct.cuh.
 //  Every kernel starts with the programmatic-launch wait, so a launch may
 //  overlap the kernel before it on the stream.
@@ -761,8 +762,8 @@ __global__ void __launch_bounds__(kDirectThreads, OCC) rr_direct_kernel(const __
 }
 
 // --------------------------------------------------------------------------
-// ReduceScatter / AllGather chunk by chunk.  Where the chunk boundaries are
-// off the 16-byte grid, the chunk-local buffers (the ReduceScatter outputs,
+// ReduceScatter / AllGather (and AllReduce, chunks on the grid) chunk by
+// chunk.  Where the chunk boundaries are off the 16-byte grid, the chunk-local buffers (the ReduceScatter outputs,
 // the AllGather inputs) are shifted against the rank vectors by (c * base)
 // mod V elements, and each 16-byte vector aligned in the shifted buffer is
 // built from two aligned blocks of the other side; on the grid the shift is
@@ -927,6 +928,118 @@ __global__ void __launch_bounds__(kDirectThreads, shift_occupancy(US)) rr_shift_
       const unsigned long long len = c < L - 1 ? base : len_last, full = len / V * V;
       if (full + e < len) element_op<OP, DT, WT>(p, (unsigned long long)c * base + full + e);
     }
+  } else if constexpr (OP == kOpAllReduce) {
+    // AllReduce over a flat ring of few ranks with every chunk boundary on the
+    // 16-byte grid and whole rank vectors (no range): chunk by chunk in rows of
+    // 32 vectors; lane t folds every rank's vector t of a row in the chunk's
+    // ring order and stores the sum to every output.  As in the
+    // ReduceScatter, every item but a chunk's last holds only whole vectors of
+    // the chunk, so it loads and stores without a check; the last items go
+    // first, a row to a warp; the elements past the last chunk's last whole
+    // vector go one by one.
+    constexpr int NB = direct_batch_ranks(US);
+    constexpr unsigned long long VB = (unsigned long long)V * E;
+    const unsigned lane = threadIdx.x & 31u;
+    const unsigned long long warp = tid >> 5, n_warps = T >> 5;
+    const unsigned long long len_last = N - (unsigned long long)(L - 1) * base;
+    constexpr unsigned long long per_item = 32ull * US;
+    const unsigned long long nvc = base / V, nvl = len_last / V;  // whole vectors of a chunk, of the last
+    const unsigned long long ipc = (nvc + per_item - 1) / per_item, ipl = (nvl + per_item - 1) / per_item;
+    const unsigned long long inc = ipc ? ipc - 1 : 0, inl = ipl ? ipl - 1 : 0;
+    const unsigned long long n_inner = (unsigned long long)(L - 1) * inc + inl;
+    const unsigned long long n_edge = (unsigned long long)L * US;
+    auto advance = [&](int &c, unsigned long long &item) {
+      item += n_warps;
+      while (c < L - 1 && item >= inc) {
+        item -= inc;
+        ++c;
+      }
+    };
+    auto prefetch_item = [&](int c, unsigned long long item) {
+      const unsigned long long off = ((unsigned long long)c * base + (item * per_item + lane) * V) * E;
+#pragma unroll
+      for (int k = 0; k < US; ++k)
+        for (int r = 0; r < L; ++r) prefetch_in<false, E>(p, r, off + 32ull * VB * k);
+    };
+    const unsigned long long w0 =
+        warp < n_edge ? warp + (n_edge - warp + n_warps - 1) / n_warps * n_warps - n_edge : warp - n_edge;
+    int c = L - 1;
+    unsigned long long item = 0;
+    if (w0 < n_inner) {
+      if (w0 < (unsigned long long)(L - 1) * inc) {
+        c = (int)(w0 / inc);
+        item = w0 - (unsigned long long)c * inc;
+      } else {
+        item = w0 - (unsigned long long)(L - 1) * inc;
+      }
+      if (p.prefetch & kPrefetchHead) prefetch_item(c, item);
+    }
+    grid_dependency_wait();
+    grid_dependents_launch();
+    for (unsigned long long e = warp; e < n_edge; e += n_warps) {  // a chunk's last item, a row to a warp
+      const int ce = (int)(e / US), k = (int)(e % US);
+      const unsigned long long nv = ce < L - 1 ? nvc : nvl, n_c = ce < L - 1 ? ipc : ipl;
+      if (n_c == 0) continue;
+      const unsigned long long u = (n_c - 1) * per_item + 32ull * k + lane;
+      if (u >= nv) continue;
+      const unsigned long long off = ((unsigned long long)ce * base + u * V) * E;
+      W acc;
+      for (int k0 = 0; k0 < L; k0 += NB) {
+        uint4 blk[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          if (k0 + j < L) {
+            int r = ce + k0 + j;
+            r -= (r >= L) ? L : 0;
+            blk[j] = load_in<false, E>(p, r, off);
+          }
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          if (k0 + j < L) {
+            const W x = VT::in(blk[j]);
+            acc = (k0 + j == 0) ? x : VT::hop(acc, x);
+          }
+      }
+      const uint4 res = VT::out(acc);
+      for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, off, res);
+    }
+    for (unsigned long long w = w0; w < n_inner; w += n_warps) {  // warp-uniform
+      if (p.prefetch & kPrefetchAhead) {
+        int c2 = c;
+        unsigned long long item2 = item;
+        advance(c2, item2);
+        if (w + n_warps < n_inner) prefetch_item(c2, item2);
+      }
+      const unsigned long long off = ((unsigned long long)c * base + (item * per_item + lane) * V) * E;
+      W acc[US];
+      for (int k0 = 0; k0 < L; k0 += NB) {
+        uint4 blk[US][NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          if (k0 + j < L) {
+            int r = c + k0 + j;
+            r -= (r >= L) ? L : 0;
+#pragma unroll
+            for (int k = 0; k < US; ++k) blk[k][j] = load_in<false, E>(p, r, off + 32ull * VB * k);
+          }
+#pragma unroll
+        for (int k = 0; k < US; ++k)
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            if (k0 + j < L) {
+              const W x = VT::in(blk[k][j]);
+              acc[k] = (k0 + j == 0) ? x : VT::hop(acc[k], x);
+            }
+      }
+#pragma unroll
+      for (int k = 0; k < US; ++k) {
+        const uint4 res = VT::out(acc[k]);
+        for (int r = 0; r < p.R; ++r) store_out<false, E>(p, r, off + 32ull * VB * k, res);
+      }
+      advance(c, item);
+    }
+    for (unsigned long long i = (unsigned long long)(L - 1) * base + nvl * V + tid; i < N; i += T)
+      element_op<OP, DT, WT>(p, i);
   } else if (p.shift_rows) {
     // AllGather over up to four ranks (where the loads weigh most), and over
     // more from 12 MiB per rank (also with the chunks on the grid, unshifted,
@@ -1188,15 +1301,23 @@ cudaError_t launch_direct(const RingParams &p, const Launch &l, cudaStream_t s) 
 template <int OP, int DT, int WT>
 cudaError_t launch_shift(const RingParams &p, const Launch &l, cudaStream_t s) {
   constexpr bool wide = DT != kF32 && WT == kF32;
-  switch (p.direct_u) {
-    case 1: return launch_kernel(rr_shift_kernel<OP, DT, WT, 1>, l, 0, s, p);
-    case 2: return launch_kernel(rr_shift_kernel<OP, DT, WT, 2>, l, 0, s, p);
-    case 3:
-      if constexpr (OP == kOpReduceScatter && !wide) return launch_kernel(rr_shift_kernel<OP, DT, WT, 3>, l, 0, s, p);
-      break;
-    case 4:
-      if constexpr (!wide) return launch_kernel(rr_shift_kernel<OP, DT, WT, 4>, l, 0, s, p);
-      break;
+  if constexpr (OP == kOpAllReduce) {  // two or four rows, accumulators of the fold's own type
+    if constexpr (!wide) {
+      if (p.direct_u == 2) return launch_kernel(rr_shift_kernel<OP, DT, WT, 2>, l, 0, s, p);
+      if (p.direct_u == 4) return launch_kernel(rr_shift_kernel<OP, DT, WT, 4>, l, 0, s, p);
+    }
+  } else {
+    switch (p.direct_u) {
+      case 1: return launch_kernel(rr_shift_kernel<OP, DT, WT, 1>, l, 0, s, p);
+      case 2: return launch_kernel(rr_shift_kernel<OP, DT, WT, 2>, l, 0, s, p);
+      case 3:
+        if constexpr (OP == kOpReduceScatter && !wide)
+          return launch_kernel(rr_shift_kernel<OP, DT, WT, 3>, l, 0, s, p);
+        break;
+      case 4:
+        if constexpr (!wide) return launch_kernel(rr_shift_kernel<OP, DT, WT, 4>, l, 0, s, p);
+        break;
+    }
   }
   return cudaErrorInvalidConfiguration;  // not a variant the planner picks
 }
@@ -1226,9 +1347,7 @@ cudaError_t launch_variant(const RingParams &p, const Launch &l, cudaStream_t s)
     if constexpr (HD) {
       return launch_hd_direct(DT, WT, p, l, s);
     } else {
-      if constexpr (OP != kOpAllReduce) {
-        if (p.shifted) return launch_shift<OP, DT, WT>(p, l, s);
-      }
+      if (p.shifted) return launch_shift<OP, DT, WT>(p, l, s);
       return launch_direct<OP, DT, WT>(p, l, s);
     }
   }

@@ -80,9 +80,13 @@ __host__ __device__ constexpr bool direct_variant_exists(int op, bool wide, int 
 
 // The shifted ReduceScatter / AllGather kernels (chunk boundaries off the
 // 16-byte grid): US rows of output vectors per warp work item.
-// ReduceScatter: US = 1..4 (wide: 1, 2); AllGather: US = 1, 2, 4.
+// ReduceScatter: US = 1..4 (wide: 1, 2); AllGather: US = 1, 2, 4; AllReduce
+// (chunks on the grid): US = 2, 4, not wide.
 __host__ __device__ constexpr bool shift_variant_exists(int op, bool wide, int US) {
-  return op == kOpAllGather ? (US == 1 || US == 2 || US == 4) : wide ? (US == 1 || US == 2) : (US >= 1 && US <= 4);
+  return op == kOpAllGather     ? (US == 1 || US == 2 || US == 4)
+         : op == kOpAllReduce   ? (!wide && (US == 2 || US == 4))
+         : wide                 ? (US == 1 || US == 2)
+                                : (US >= 1 && US <= 4);
 }
 
 // 256-thread CTAs per SM the shifted kernel of US rows is compiled for.

@@ -469,11 +469,16 @@ def test_direct_grid_waves(L):
     """Looping direct grids: ReduceScatter and AllReduce over groups of at most
     three ranks take two whole waves of the resident CTAs (three 256-thread
     CTAs' worth of registers per SM: 6 CTAs of 128 a wave); other AllReduce
-    and AllGather launches take sixteen 128-thread CTAs per SM."""
+    and AllGather launches take sixteen 128-thread CTAs per SM, and so do the
+    chunk-by-chunk rows of AllReduce over flat rings of up to four ranks from
+    16 MiB per rank."""
     sms, n = GB300["sms"], 1 << 26  # 256 MiB of binary32 per rank
     assert plan_dev(L, RS, 4, n, F32)[2] == sms * 6 * 2
     assert plan_dev(L, RS, 16, n, F32)[2] == sms * 6 * 2
-    assert plan_dev(L, AR, 3, 3 << 24, F16)[2] == sms * 6 * 2
+    assert plan_dev(L, AR, 3, 3 << 24, F16, wire=F32)[2] == sms * 2 * 2 * 2  # fp32 accumulators: two CTAs per SM
+    # a flat ring of up to four ranks from 16 MiB: the chunk-by-chunk rows, sixteen CTAs per SM
+    st, ch, grid, _ = plan_dev(L, AR, 3, 3 << 24, F16)
+    assert st == OK and grid == sms * 16 and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
     assert plan_dev(L, AR, 8, 1 << 26, F32, group=2)[2] == sms * 6 * 2
     assert plan_dev(L, AR, 4, 1 << 27, F16)[2] == sms * 16
     assert plan_dev(L, AR, 8, 1 << 28, F16)[2] == sms * 16
@@ -511,8 +516,8 @@ def test_direct_grid_waves(L):
 
 
 def test_one_wave_for_small_flat_rings(L):
-    """Flat AllReduce / ReduceScatter over up to four ranks under 32 MiB per
-    rank: one wave of resident CTAs (128 threads; two 256-thread CTAs' worth of
+    """Flat AllReduce under 16 MiB per rank and ReduceScatter under 32 MiB over
+    up to four ranks: one wave of resident CTAs (128 threads; two 256-thread CTAs' worth of
     registers per SM up to 8 MiB, three above), one vector a thread when two
     would leave SMs idle, both L2 prefetches; not for AllGather, five or more
     ranks, two-level rings or 32 MiB and up."""
@@ -524,7 +529,7 @@ def test_one_wave_for_small_flat_rings(L):
         return ch["vectors"], ch["ctas_per_sm"], grid, ch["prefetch"] - 1
     assert plan(AR, 4, 4, F32, 4) == (2, 2, sms * 4, 3)      # workload 1
     assert plan(RS, 4, 4, F32, 4) == (2, 2, sms * 4, 3)
-    assert plan(AR, 2, 16) == (2, 3, sms * 6, 3)
+    assert plan(AR, 2, 8) == (2, 2, sms * 4, 3)
     assert plan(RS, 3, 16) == (2, 3, sms * 6, 3)
     v, occ, grid, pf = plan(AR, 4, 1)                         # 1 MiB: one vector, the grid under a wave
     assert (v, occ, pf) == (1, 2, 3) and grid <= sms * 4
@@ -681,8 +686,9 @@ def test_planner_prefetch_policy(L):
     AllGather, ReduceScatter over three ranks, and 8-64 MiB messages other
     than ReduceScatter over five or more ranks; never on the halving-doubling
     kernels; the shifted AllGather both, the shifted ReduceScatter the first
-    item over three to five ranks below 32 MiB per rank, else none (prefetch
-    reported as 1 + the bits)."""
+    item over three to five ranks below 32 MiB per rank, else none; the
+    AllReduce rows the first item below 24 MiB, else none (prefetch reported
+    as 1 + the bits)."""
     MiB = 1 << 20
     def pf(op, R, mib, dt=F16, E=2, **kw):
         st, ch, _, _ = plan_dev(L, op, R, R * (mib * MiB // E // R // 8 * 8), dt, **kw)
@@ -692,8 +698,10 @@ def test_planner_prefetch_policy(L):
     assert pf(AR, 8, 1) == HEAD
     assert pf(AR, 8, 16) == HEAD | AHEAD
     assert pf(AR, 8, 256) == 0
-    assert pf(AR, 4, 256) == HEAD
-    assert pf(AR, 2, 256) == HEAD | AHEAD
+    assert pf(AR, 4, 256, F16, 2, wire=F32) == HEAD          # fp32 accumulators: the direct kernel
+    assert pf(AR, 2, 256, F16, 2, wire=F32) == HEAD | AHEAD
+    assert pf(AR, 4, 256) == 0                               # the chunk-by-chunk rows: the first item
+    assert pf(AR, 2, 16) == HEAD                             # below 24 MiB only
     assert pf(RS, 8, 16) == HEAD
     assert pf(RS, 3, 256) == HEAD | AHEAD
     assert pf(AG, 8, 256) == HEAD | AHEAD  # the chunk-by-chunk rows from 16 MiB: both

@@ -734,6 +734,30 @@ def test_workload2_full_oracle(rr, wl, mib):
     check_ar(rr, xs, what=f"workload 2 {mib} MiB")
 
 
+@pytest.mark.parametrize("dtype,wire", [(torch.float16, None), (torch.bfloat16, None), (torch.float32, "f16")],
+                         ids=lambda v: str(v))
+def test_allreduce_rows_few_ranks(rr, dtype, wire):
+    """AllReduce over two to four ranks from 16 MiB per rank with chunk
+    boundaries on the 16-byte grid and a ragged last chunk: the chunk-by-chunk
+    rows (forced two and four rows, and the planner's choice).  Every element
+    of every output equals the oracle's closed form."""
+    E = torch.tensor([], dtype=dtype).element_size()
+    V = 16 // E
+    for R in (2, 3, 4):
+        base = -(-(16 << 20) // (E * R * V)) * V + 37 * V  # a multiple of V; R * base * E > 16 MiB
+        N = R * base + (R - 1) * V + (V - 1)               # the last chunk: R - 1 more vectors and a ragged end
+        xs = gen(R, N, dtype, 89 * R + E)
+        for rows in (0, 2, 4):
+            cfg = rr.LaunchCfg(rr.PATH_DIRECT, 0, 0, 0, 0, 0, 0, rows) if rows else None
+            outs = [torch.full((N,), float("nan"), dtype=dtype, device="cuda") for _ in range(R)]
+            rr.collective(rr.OP_ALLREDUCE, xs, outs, N, wire, 0, None, cfg)
+            torch.cuda.synchronize()
+            check_full(rr, xs, outs, wire=wire, what=f"AR rows {NAME[dtype]}/{wire} R={R} rows={rows}")
+            del outs
+        del xs
+        torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("dtype,wire", [(torch.float16, None), (torch.float32, "bf16")], ids=lambda v: str(v))
 def test_reduce_scatter_two_ranks_chunk_by_chunk(rr, dtype, wire):
     """ReduceScatter over two ranks from 64 MiB per rank with chunk boundaries

@@ -2,8 +2,8 @@
 
 rr_shift_kernel (csrc/rr_kernels.cuh) splits each chunk's output vectors into
 work items of US rows and runs most items with no bounds check at all; the
-rest (a ReduceScatter chunk's last item, an AllGather chunk's first item and
-last three) go through the checked code, one row to a warp, and the warps take
+rest (a ReduceScatter or AllReduce chunk's last item, an AllGather chunk's
+first item and last three) go through the checked code, one row to a warp, and the warps take
 the checked rows first and the inner items after, in turn.  These tests
 restate that index arithmetic in Python and check, over many chunk lengths,
 rank counts and row counts, that every output vector wholly inside a chunk is
@@ -139,6 +139,45 @@ def allgather_partition(N, L, V, US, n_warps):
     assert all(any(chunk(c)[1] <= v < chunk(c)[2] for c in range(L)) for v in written)
 
 
+def allreduce_partition(N, L, V, US, n_warps):
+    """The AllReduce rows (chunks on the grid): rows of 32 whole vectors."""
+    base = N // L
+    len_last = N - (L - 1) * base
+    per_item = 32 * US
+    nvc, nvl = base // V, len_last // V
+    ipc, ipl = (nvc + per_item - 1) // per_item, (nvl + per_item - 1) // per_item
+    inc, inl = max(ipc - 1, 0), max(ipl - 1, 0)
+    n_inner, n_edge = (L - 1) * inc + inl, L * US
+    written = {}
+    for e in range(n_edge):
+        ce, k = e // US, e % US
+        nv, n_c = (nvc, ipc) if ce < L - 1 else (nvl, ipl)
+        if n_c == 0:
+            continue
+        for lane in range(32):
+            u = (n_c - 1) * per_item + 32 * k + lane
+            if u < nv:
+                written[(ce, u)] = written.get((ce, u), 0) + 1
+    for warp in range(n_warps):
+        w = first_inner_item(warp, n_warps, n_edge)
+        if w >= n_inner:
+            continue
+        c, item = walk(w, inc, L)
+        while w < n_inner:
+            nv = nvc if c < L - 1 else nvl
+            for k in range(US):
+                for lane in range(32):
+                    u = item * per_item + 32 * k + lane
+                    assert u < nv, (N, L, V, US, c, item, u)  # a whole vector of the chunk: no check needed
+                    written[(c, u)] = written.get((c, u), 0) + 1
+            c, item = step(c, item, n_warps, inc, L)
+            w += n_warps
+    for c in range(L):
+        for u in range(nvc if c < L - 1 else nvl):
+            assert written.get((c, u)) == 1, (N, L, V, US, c, u, written.get((c, u)))
+    assert all(u < (nvc if c < L - 1 else nvl) for c, u in written)
+
+
 def lengths(seed):
     """Chunk lengths from under one vector to several items' worth of rows."""
     rng = random.Random(seed)
@@ -162,3 +201,13 @@ def test_allgather_inner_items_stay_in_bounds(L):
             for n in lengths(20 * L + US):
                 for n_warps in (1, 7, 97):
                     allgather_partition(n * L + L // 2, L, V, US, n_warps)
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4])
+def test_allreduce_rows_inner_items_stay_in_bounds(L):
+    for V in (4, 8):
+        for US in (2, 4):
+            for n in lengths(30 * L + US):
+                n = n // V * V or V  # chunks on the 16-byte grid
+                for n_warps in (1, 7, 97):
+                    allreduce_partition(n * L + V // 2, L, V, US, n_warps)
