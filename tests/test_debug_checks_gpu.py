@@ -31,7 +31,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 EDGE_GRIDS = ("edge_grid or maximum_rank_counts or two_level_grid or reduce_scatter_grid or allgather_grid or "
               "shifted or misaligned or outputs_do_not_write_outside or vectors_over_chunk_boundaries or "
               "every_direct_variant or capped_grids or algorithm_grid or ranges_concatenate or "
-              "direct_occupancy_variants or algorithm_occupancy_variants or workload1_full")
+              "direct_occupancy_variants or algorithm_occupancy_variants or workload1_full or allreduce_rows or "
+              "allgather_rows or chunk_by_chunk")
 
 
 def test_edge_grids_under_the_debug_build():
@@ -79,7 +80,8 @@ def host(t):
 
 def cases(rr):
     """(what, op, ins, outs, count, wire, cfg, algo) on every path: tile
-    pipeline, direct (aligned, shifted, halving-doubling), one element."""
+    pipeline, direct (aligned, shifted, halving-doubling, the chunk-by-chunk
+    rows on aligned chunks), one element."""
     g = torch.Generator(device="cuda")
     g.manual_seed(7)
     out = []
@@ -99,6 +101,22 @@ def cases(rr):
                         [torch.empty(N, dtype=dtype, device="cuda") for _ in range(R)], N, None, cfg, "ring"))
         out.append((f"AR R={R} halving-doubling", rr.OP_ALLREDUCE, xs, [torch.empty_like(x) for x in xs], N, None,
                     rr.LaunchCfg(rr.PATH_DIRECT), "hd"))
+    # the chunk-by-chunk rows on chunks on the grid: AllReduce over two ranks
+    # from 16 MiB, AllGather over four from 12 MiB, ReduceScatter over two
+    # from 64 MiB (binary16; ragged last chunks)
+    for what, op, R, N in (("AR rows", rr.OP_ALLREDUCE, 2, 2 * (4 << 20) + 1),
+                           ("AG rows", rr.OP_ALLGATHER, 4, 4 * (3 << 19) + 3),
+                           ("RS rows", rr.OP_REDUCE_SCATTER, 2, 2 * (16 << 20) + 1)):
+        xs = [torch.randn(N, generator=g, device="cuda").to(torch.float16) for _ in range(R)]
+        lens = [rr.chunk_count(N, R, c) for c in range(R)]
+        if op == rr.OP_ALLGATHER:
+            ins, outs = [x[:n].clone() for x, n in zip(xs, lens)], [torch.empty(N, dtype=torch.float16,
+                                                                               device="cuda") for _ in range(R)]
+        elif op == rr.OP_REDUCE_SCATTER:
+            ins, outs = xs, [torch.empty(n, dtype=torch.float16, device="cuda") for n in lens]
+        else:
+            ins, outs = xs, [torch.empty_like(x) for x in xs]
+        out.append((f"{what} R={R} N={N}", op, ins, outs, N, None, rr.LaunchCfg(rr.PATH_DIRECT), "ring"))
     return out
 
 
