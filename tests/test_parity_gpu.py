@@ -754,6 +754,11 @@ def test_allreduce_rows_few_ranks(rr, dtype, wire):
             torch.cuda.synchronize()
             check_full(rr, xs, outs, wire=wire, what=f"AR rows {NAME[dtype]}/{wire} R={R} rows={rows}")
             del outs
+        # in place: each vector is read and written by one lane only
+        outs = run_ar(rr, xs, wire, inplace=True)
+        torch.cuda.synchronize()
+        check_full(rr, xs, outs, wire=wire, what=f"AR rows in place {NAME[dtype]}/{wire} R={R}")
+        del outs
         del xs
         torch.cuda.empty_cache()
 
