@@ -263,15 +263,16 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
                                                                                              : RR_PATH_BULK;
   }
   p->shifted = (path == RR_PATH_DIRECT && !chunks_aligned) ? 1 : 0;
-  // ReduceScatter over two ranks from 64 MiB per rank: the chunk-by-chunk
+  // ReduceScatter over two ranks from 32 MiB per rank: the chunk-by-chunk
   // (shifted) kernel also where the chunks sit on the 16-byte grid (it then
   // shifts by nothing).  It knows each work item's chunk, where the direct
   // kernel looks up every vector's, and its four rows keep eight loads in
-  // flight a lane.  Measured, binary16, of the copy bandwidth, at 16 / 64 /
-  // 256 MiB per rank: direct 0.70 / 0.84 / 0.89, chunk by chunk 0.70 / 0.88 /
-  // 0.96; over three or more ranks the direct kernel is as fast or faster.
+  // flight a lane.  Measured, binary16, of the copy bandwidth, at 16 / 32 /
+  // 64 / 256 MiB per rank: direct 0.70 / 0.75 / 0.84 / 0.89, chunk by chunk
+  // 0.70 / 0.79 / 0.88 / 0.96; over three or more ranks the direct kernel is
+  // as fast or faster.
   if (path == RR_PATH_DIRECT && ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && ck.L == 2 &&
-      (unsigned long long)ck.count * E >= (64ull << 20) && c.vectors == 0 && c.ctas_per_sm == 0)
+      (unsigned long long)ck.count * E >= (32ull << 20) && c.vectors == 0 && c.ctas_per_sm == 0)
     p->shifted = 1;
   // AllGather from 12 MiB per rank (two ranks: 64 MiB) likewise, in rows of 32
   // vectors of one chunk that end on 512-byte store segments.  Measured,

@@ -496,11 +496,13 @@ def test_direct_grid_waves(L):
     assert plan_dev(L, RS, 2, (64 << 20) // 2 + 2, F16)[2] == sms * 12
     st, _, grid, _ = plan_dev(L, RS, 4, (16 << 20) // 2 - 4 + 3, F16, cfg=(0, 0, 0, 0, 256))
     assert st == OK and grid == sms * 6                       # the same share of threads at 256 a CTA
-    # ReduceScatter over two ranks from 64 MiB per rank, chunks on the grid:
+    # ReduceScatter over two ranks from 32 MiB per rank, chunks on the grid:
     # the chunk-by-chunk kernel at four rows (two 256-thread CTAs' worth of
-    # registers per SM), twelve CTAs per SM; below 64 MiB the direct kernel
+    # registers per SM), twelve CTAs per SM; below 32 MiB the direct kernel
     st, ch, grid, _ = plan_dev(L, RS, 2, 2 * (16 << 20), F16)
     assert st == OK and ch["vectors"] == 4 and ch["ctas_per_sm"] == 2 and grid == sms * 12
+    st, ch, grid, _ = plan_dev(L, RS, 2, 2 * (8 << 20), F16)
+    assert st == OK and ch["vectors"] == 4 and ch["ctas_per_sm"] == 2 and grid == sms * 12   # 32 MiB
     st, ch, grid, _ = plan_dev(L, RS, 2, 2 * (4 << 20), F16)
     assert st == OK and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3 and grid == sms * 6   # one wave
     st, ch, _, _ = plan_dev(L, RS, 2, 2 * (16 << 20), F16, cfg=(3, 0, 0, 0, 0, 0, 0, 2))  # forced vectors: direct

@@ -765,8 +765,8 @@ def test_allreduce_rows_few_ranks(rr, dtype, wire):
 
 @pytest.mark.parametrize("dtype,wire", [(torch.float16, None), (torch.float32, "bf16")], ids=lambda v: str(v))
 def test_reduce_scatter_two_ranks_chunk_by_chunk(rr, dtype, wire):
-    """ReduceScatter over two ranks from 64 MiB per rank with chunk boundaries
-    on the 16-byte grid: the planner takes the chunk-by-chunk (shifted) kernel,
+    """ReduceScatter over two ranks from 32 MiB per rank (here 64 MiB) with chunk
+    boundaries on the 16-byte grid: the planner takes the chunk-by-chunk kernel,
     which then shifts by nothing; the last chunk is ragged.  Every output
     element equals the oracle's closed form."""
     E = torch.tensor([], dtype=dtype).element_size()
