@@ -150,7 +150,8 @@ rr_status ring_allgather(const void *const *in_bufs, void *const *out_bufs, int 
  * every thread load its ranks' 16-byte vectors straight from global memory
  * and store the results straight back (16-byte aligned buffers, at most 256
  * threads per CTA; chunk offsets off the 16-byte grid are handled by building
- * each vector from two aligned loads); RR_PATH_SIMPLE is one element per
+ * each vector from two aligned loads, chunk by chunk in rows of vectors, the
+ * form larger calls over few ranks also take); RR_PATH_SIMPLE is one element per
  * thread with plain loads and stores (any alignment). */
 typedef enum { RR_PATH_AUTO = 0, RR_PATH_BULK = 1, RR_PATH_SIMPLE = 2, RR_PATH_DIRECT = 3 } rr_path;
 
@@ -177,10 +178,16 @@ typedef struct {
                       2: plain stream order. */
   int vectors;     /* direct path: 16-byte vectors a thread takes at once,
                       1..4 (AllGather 1, 2 or 4; 16-bit storage summed in
-                      binary32 1 or 2); with chunk boundaries off the 16-byte
-                      grid, rows of 31-32 vectors a warp takes at once
-                      (ReduceScatter 1..4, AllGather 1, 2 or 4).  A value
-                      outside these is RR_ERR_UNSUPPORTED. */
+                      binary32 1 or 2); where the direct path works chunk by
+                      chunk (chunk boundaries off the 16-byte grid; on it,
+                      AllGather from 12 MiB per rank, two-rank ReduceScatter
+                      from 32 MiB and AllReduce over two to four ranks from
+                      16 MiB, unless ctas_per_sm is given or vectors is not a
+                      row count below), rows of 31-32 vectors a warp takes at
+                      once (ReduceScatter 1..4, AllGather 1, 2 or 4,
+                      AllReduce 2 or 4; 16-bit storage summed in binary32: 1
+                      or 2, AllReduce none).  A value outside these is
+                      RR_ERR_UNSUPPORTED. */
   int beside_compute; /* 1: the call runs beside compute kernels on other
                       streams; unless max_ctas is given, the grid is capped at
                       RR_BESIDE_COMPUTE_SM_EIGHTHS eighths of the SMs (one CTA each),

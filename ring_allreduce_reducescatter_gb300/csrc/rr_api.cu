@@ -263,6 +263,12 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
                                                                                              : RR_PATH_BULK;
   }
   p->shifted = (path == RR_PATH_DIRECT && !chunks_aligned) ? 1 : 0;
+  // The chunk-by-chunk rows on aligned chunks (below) are taken when no
+  // register budget is asked for and the vectors asked for, if any, are a row
+  // count the rows are built for; otherwise the direct kernel runs.
+  const bool rows_ok = c.ctas_per_sm == 0 &&
+                       (c.vectors == 0 || rr::shift_variant_exists(ck.op, ck.dtype != RR_FP32 && ck.wire == RR_FP32,
+                                                                   c.vectors));
   // ReduceScatter over two ranks from 32 MiB per rank: the chunk-by-chunk
   // (shifted) kernel also where the chunks sit on the 16-byte grid (it then
   // shifts by nothing).  It knows each work item's chunk, where the direct
@@ -272,7 +278,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   // 0.70 / 0.79 / 0.88 / 0.96; over three or more ranks the direct kernel is
   // as fast or faster.
   if (path == RR_PATH_DIRECT && ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && ck.L == 2 &&
-      (unsigned long long)ck.count * E >= (32ull << 20) && c.vectors == 0 && c.ctas_per_sm == 0)
+      (unsigned long long)ck.count * E >= (32ull << 20) && rows_ok)
     p->shifted = 1;
   // AllGather from 12 MiB per rank (two ranks: 64 MiB) likewise, in rows of 32
   // vectors of one chunk that end on 512-byte store segments.  Measured,
@@ -284,8 +290,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   // 12 MiB R = 8 / 16 0.88 / 0.89 -> 0.95 / 0.96; at 8 MiB rows lost up to 6 %,
   // at 4 MiB up to 35 %.
   if (path == RR_PATH_DIRECT && ck.op == RR_OP_ALLGATHER && ck.algo == RR_ALGO_RING &&
-      (unsigned long long)ck.count * E >= (ck.L == 2 ? (64ull << 20) : (12ull << 20)) && c.vectors == 0 &&
-      c.ctas_per_sm == 0)
+      (unsigned long long)ck.count * E >= (ck.L == 2 ? (64ull << 20) : (12ull << 20)) && rows_ok)
     p->shifted = 1;
   // AllReduce over flat rings of two to four ranks from 16 MiB per rank, the
   // chunks on the grid and the whole rank vectors in one call (no range): the
@@ -298,8 +303,7 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   // 0.96 -> 0.95 / 0.99.  (R = 2 at 24 MiB lost 2-3 %.)
   if (path == RR_PATH_DIRECT && ck.op == RR_OP_ALLREDUCE && ck.algo == RR_ALGO_RING && ck.L == ck.R && ck.L >= 2 &&
       ck.L <= 4 && ck.first == 0 && ck.n == ck.count && (p->base * E) % 16 == 0 &&
-      !(ck.dtype != RR_FP32 && ck.wire == RR_FP32) && (unsigned long long)ck.count * E >= (16ull << 20) &&
-      c.ctas_per_sm == 0)
+      !(ck.dtype != RR_FP32 && ck.wire == RR_FP32) && (unsigned long long)ck.count * E >= (16ull << 20) && rows_ok)
     p->shifted = 1;
 
   l->path = path;

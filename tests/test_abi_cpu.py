@@ -479,6 +479,16 @@ def test_direct_grid_waves(L):
     # a flat ring of up to four ranks from 16 MiB: the chunk-by-chunk rows, sixteen CTAs per SM
     st, ch, grid, _ = plan_dev(L, AR, 3, 3 << 24, F16)
     assert st == OK and grid == sms * 16 and ch["vectors"] == 2 and ch["ctas_per_sm"] == 3
+    # forcing four rows keeps the rows (two 256-thread CTAs' worth of registers);
+    # one or three vectors, or a register budget, select the direct kernel
+    DIRECT = 3
+    st, ch, grid, _ = plan_dev(L, AR, 2, 2 << 23, F16, cfg=(DIRECT, 0, 0, 0, 0, 0, 0, 4))
+    assert st == OK and ch["vectors"] == 4 and ch["ctas_per_sm"] == 2 and grid == sms * 16
+    for cfg in ((DIRECT, 0, 0, 0, 0, 0, 0, 1), (DIRECT, 0, 0, 0, 0, 0, 0, 3), (DIRECT, 0, 0, 3, 0, 0, 0, 2)):
+        st, ch, grid, _ = plan_dev(L, AR, 2, 2 << 23, F16, cfg=cfg)
+        # the direct kernel: two whole waves of its resident CTAs (two ranks)
+        assert st == OK and ch["vectors"] == (cfg[7] or 2), (cfg, ch)
+        assert grid == sms * ch["ctas_per_sm"] * 2 * 2, (cfg, ch, grid)
     assert plan_dev(L, AR, 8, 1 << 26, F32, group=2)[2] == sms * 6 * 2
     assert plan_dev(L, AR, 4, 1 << 27, F16)[2] == sms * 16
     assert plan_dev(L, AR, 8, 1 << 28, F16)[2] == sms * 16
