@@ -274,8 +274,8 @@ rr_status plan_launch(const Checked &ck, const rr_launch_cfg *cfg, int sms, int 
   // shifts by nothing).  It knows each work item's chunk, where the direct
   // kernel looks up every vector's, and its four rows keep eight loads in
   // flight a lane.  Measured, binary16, of the copy bandwidth, at 16 / 32 /
-  // 64 / 256 MiB per rank: direct 0.70 / 0.75 / 0.84 / 0.89, chunk by chunk
-  // 0.70 / 0.79 / 0.88 / 0.96; over three or more ranks the direct kernel is
+  // 64 / 256 MiB per rank: direct 0.70 / 0.74 / 0.84 / 0.89, chunk by chunk
+  // 0.70 / 0.80 / 0.88 / 0.96; over three or more ranks the direct kernel is
   // as fast or faster.
   if (path == RR_PATH_DIRECT && ck.op == RR_OP_REDUCE_SCATTER && ck.algo == RR_ALGO_RING && ck.L == 2 &&
       (unsigned long long)ck.count * E >= (32ull << 20) && rows_ok)
